@@ -1,0 +1,45 @@
+"""Plant plausible mistakes in the oracle (CPU only) and require that at least
+one pin catches each.  Each mutant replaces one step of ``oracle.attention``
+through monkeypatch, so the oracle's own code is what runs, with one error."""
+
+import numpy as np
+import pytest
+
+from oracle import attention as att
+
+from oracle_pins import ALL_PINS
+
+
+def _fails_some_pin():
+    failed = []
+    for pin in ALL_PINS:
+        try:
+            with np.errstate(all="ignore"):
+                pin(att)
+        except (AssertionError, FloatingPointError, ValueError, IndexError):
+            failed.append(pin.__name__)
+    return failed
+
+
+MUTANTS = {
+    # forward
+    "scale_dropped": ("_scores", lambda q, k, scale: q @ k.T),
+    "operands_transposed": ("_scores", lambda q, k, scale: scale * (k @ q.T)),
+    "mask_flipped": ("_visible", lambda rows, n_k: np.arange(n_k)[None, :] >= rows[:, None]),
+    "mask_strict": ("_visible", lambda rows, n_k: np.arange(n_k)[None, :] < rows[:, None]),
+    "mask_off_by_one": ("_visible", lambda rows, n_k: np.arange(n_k)[None, :] <= rows[:, None] + 1),
+    "max_sign": ("_softmax_stats", lambda s: (lambda m: (m, np.exp(s + m[:, None]), np.sum(np.exp(s + m[:, None]), axis=1)))(np.max(s, axis=1))),
+    "lse_without_max": ("_lse", lambda m, l: np.log(l)),
+    "lse_log2": ("_lse", lambda m, l: m + np.log2(l)),
+    # backward
+    "d_dropped": ("_d_vector", lambda do, o: np.zeros(do.shape[0])),
+    "d_wrong_axis": ("_d_vector", lambda do, o: np.sum(do * o, axis=1)[::-1].copy()),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, monkeypatch):
+    attr, fn = MUTANTS[name]
+    monkeypatch.setattr(att, attr, fn)
+    failed = _fails_some_pin()
+    assert failed, f"no pin caught the planted mistake {name!r}"
