@@ -1,0 +1,223 @@
+"""ctypes binding of libfa.so (include/fa.h), argument marshalling only.
+
+Every function named ``fa_*`` here has the name and argument order of the C
+entry point and passes torch tensors' device pointers plus the current torch
+stream.  All arithmetic runs in the CUDA kernels of libfa.so; nothing here
+computes attention.  If libfa.so is missing or fails to load, every call
+raises FaError: there is no fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import re
+import threading
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfa.so")
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "fa.h")
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_CUDA = 3
+FA_ERR_NO_MEMORY = 4
+FA_ERR_TIMEOUT = 5
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        msg = _strerror(status) if _lib is not None else f"fa_status {status}"
+        super().__init__(f"{what}: {msg}" if what else msg)
+
+
+_lib = None
+_lock = threading.Lock()
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_f = ctypes.c_float
+_u64 = ctypes.c_uint64
+
+_SIGNATURES = {
+    "fa_fwd": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp], _i),
+    "fa_fwd_ex": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp], _i),
+    "fa_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp], _i),
+    "fa_poll_status": ([_vp], _i),
+    "fa_set_wait_timeout_ns": ([_u64], _u64),
+    "fa_selftest_wait_timeout": ([_u64, _vp], _i),
+    "fa_strerror": ([_i], ctypes.c_char_p),
+    "fa_abi_version": ([], _i),
+    "fa_timing_enable": ([_i], _i),
+    "fa_timing_read": ([_i, ctypes.POINTER(_i), ctypes.POINTER(ctypes.c_double)], _i),
+}
+
+
+def load():
+    """Load libfa.so once; raise FaError if it is not built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise FaError(FA_ERR_CUDA, f"{LIB_PATH} is not built (run exact_attention_92_gb300.build.build())")
+            lib = ctypes.CDLL(LIB_PATH)
+            for name, (args, res) in _SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = lib
+    return _lib
+
+
+def declared_symbols():
+    """Entry points declared in include/fa.h."""
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:int|uint64_t|const char\*)\s+(fa_\w+)\s*\(", text, re.M)))
+
+
+def _strerror(status: int) -> str:
+    return load().fa_strerror(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != FA_OK:
+        raise FaError(status, what)
+
+
+def _stream_ptr(stream, device):
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _check_bhnd(name, t, shape=None):
+    import torch
+
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device")
+    if t.dtype != torch.bfloat16:
+        raise ValueError(f"{name} must be bfloat16, got {t.dtype}")
+    if t.dim() != 4 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous [B, H, N, d] tensor")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _check_lse(t, shape):
+    import torch
+
+    if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.float32 and t.is_contiguous()
+            and tuple(t.shape) == tuple(shape)):
+        raise ValueError(f"lse must be a contiguous float32 CUDA tensor of shape {tuple(shape)}")
+
+
+def _scale(scale, d):
+    return 1.0 / math.sqrt(d) if scale is None else float(scale)
+
+
+# ---------------------------------------------------------------- C names
+
+def fa_fwd(q, k, v, o, lse, causal=False, scale=None, stream=None):
+    """C fa_fwd: O and LSE of softmax(scale Q K^T [+ causal mask]) V."""
+    return fa_fwd_ex(q, k, v, o, lse, causal, scale, 0, stream)
+
+
+def fa_fwd_ex(q, k, v, o, lse, causal=False, scale=None, num_splits=0, stream=None):
+    """C fa_fwd_ex: fa_fwd with an explicit key-split count (0 = automatic)."""
+    _check_bhnd("q", q)
+    B, H, N, d = q.shape
+    for name, t in (("k", k), ("v", v), ("o", o)):
+        _check_bhnd(name, t, q.shape)
+    _check_lse(lse, (B, H, N))
+    lib = load()
+    st = lib.fa_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, 1 if causal else 0,
+                       _scale(scale, d), int(num_splits), _stream_ptr(stream, q.device))
+    _check(st, "fa_fwd_ex")
+
+
+def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, causal=False, scale=None, stream=None):
+    """C fa_bwd: dQ, dK, dV from the forward inputs, O, LSE and dO."""
+    _check_bhnd("q", q)
+    B, H, N, d = q.shape
+    for name, t in (("k", k), ("v", v), ("o", o), ("dout", dout), ("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_bhnd(name, t, q.shape)
+    _check_lse(lse, (B, H, N))
+    lib = load()
+    st = lib.fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                    B, H, N, d, 1 if causal else 0, _scale(scale, d), _stream_ptr(stream, q.device))
+    _check(st, "fa_bwd")
+
+
+def fa_poll_status(stream=None):
+    """C fa_poll_status: synchronise the stream, return and clear the device status."""
+    import torch
+
+    return load().fa_poll_status(_stream_ptr(stream, torch.device("cuda")))
+
+
+def fa_set_wait_timeout_ns(ns: int) -> int:
+    return int(load().fa_set_wait_timeout_ns(int(ns)))
+
+
+def fa_selftest_wait_timeout(timeout_ns: int, stream=None):
+    import torch
+
+    _check(load().fa_selftest_wait_timeout(int(timeout_ns), _stream_ptr(stream, torch.device("cuda"))),
+           "fa_selftest_wait_timeout")
+
+
+def fa_strerror(status: int) -> str:
+    return _strerror(status)
+
+
+def fa_abi_version() -> int:
+    return int(load().fa_abi_version())
+
+
+def fa_timing_enable(on: bool) -> None:
+    _check(load().fa_timing_enable(1 if on else 0), "fa_timing_enable")
+
+
+def fa_timing_read(kernel: int):
+    """(launches, total milliseconds) of one kernel since timing was enabled or last read."""
+    n = ctypes.c_int(0)
+    ms = ctypes.c_double(0.0)
+    _check(load().fa_timing_read(int(kernel), ctypes.byref(n), ctypes.byref(ms)), "fa_timing_read")
+    return n.value, ms.value
+
+
+# ------------------------------------------------------- convenience calls
+
+def forward(q, k, v, causal=False, scale=None, num_splits=0):
+    """Allocate O and LSE and run fa_fwd_ex; returns (o, lse)."""
+    import torch
+
+    B, H, N, d = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    fa_fwd_ex(q, k, v, o, lse, causal, scale, num_splits)
+    return o, lse
+
+
+def backward(q, k, v, o, lse, dout, causal=False, scale=None):
+    """Allocate dQ, dK, dV and run fa_bwd; returns (dq, dk, dv)."""
+    import torch
+
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, causal, scale)
+    return dq, dk, dv

@@ -1,0 +1,396 @@
+// Host side of the C ABI declared in include/fa.h: argument validation,
+// tensor-map encoding, the split-KV decision, stream-ordered workspace and the
+// device status word read by fa_poll_status.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "fa_common.h"
+
+namespace fa {
+cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const FwdParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_combine(int d, const CombineParams& p, cudaStream_t stream);
+cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& tdo, const BwdParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_bwd_preprocess(int d, const void* o, const void* dout, float* dvec, float* dq_acc, int rows,
+                                  cudaStream_t stream);
+cudaError_t launch_dq_convert(int d, const float* dq_acc, void* dq, size_t elems, float scale, cudaStream_t stream);
+cudaError_t launch_selftest_wait(unsigned int* status, unsigned long long timeout_ns, cudaStream_t stream);
+}  // namespace fa
+
+// One status word per device that loads the library.  Kernels record the
+// first failing wait here; fa_poll_status reads and clears it.
+static __device__ unsigned int g_fa_status_word;
+
+namespace {
+
+using fa::FwdParams;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  std::once_flag once;
+  int err = 0;  // fa_status of the set-up
+  int sm_count = 0;
+  unsigned int* status = nullptr;  // device address of g_fa_status_word
+};
+
+DeviceState g_dev[kMaxDevices];
+std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
+
+std::once_flag g_encode_once;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+void load_encode() {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+          cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+}
+
+// Set-up of the current device, once: compute capability check, SM count and
+// the address of the status word.
+int device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+  DeviceState& s = g_dev[dev];
+  std::call_once(s.once, [&s, dev]() {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) {
+      s.err = FA_ERR_CUDA;
+      return;
+    }
+    if (!(prop.major == 10 && prop.minor == 3)) {
+      s.err = FA_ERR_UNSUPPORTED;
+      return;
+    }
+    s.sm_count = prop.multiProcessorCount;
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_fa_status_word) != cudaSuccess) {
+      s.err = FA_ERR_CUDA;
+      return;
+    }
+    s.status = static_cast<unsigned int*>(addr);
+    if (cudaMemset(s.status, 0, sizeof(unsigned int)) != cudaSuccess) s.err = FA_ERR_CUDA;
+  });
+  if (s.err) return s.err;
+  std::call_once(g_encode_once, load_encode);
+  if (!g_encode) return FA_ERR_CUDA;
+  *out = &s;
+  return FA_OK;
+}
+
+bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int validate(int B, int H, int N, int d, float scale) {
+  if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+  if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  const long double elems = (long double)B * H * N * d;
+  if (elems >= 9.0e18L) return FA_ERR_INVALID_ARG;
+  if ((long long)B * H > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  if ((long long)B * H * ((N + 255) / 256) * 64 > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
+// [B*H, N, d] bf16 viewed as a 3-D tensor (d innermost); boxes of 64 x 128 x 1
+// with the 128-byte swizzle the MMA descriptors expect.  Rows past N read as
+// zero.
+int encode_bhnd(CUtensorMap* m, const void* ptr, int BH, int N, int d) {
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+// Number of key splits: only when the (batch*head, query block) units cannot
+// fill the GPU.  Picks the split count with the best last-wave occupancy,
+// keeping at least 4 key tiles per split.
+int choose_splits(int BH, int N, int sm_count) {
+  const int qblocks = (N + 255) / 256;
+  const int nkv = (N + 127) / 128;
+  const long long units = (long long)BH * qblocks;
+  if (units >= 2LL * sm_count) return 1;
+  int best = 1;
+  double best_eff = 0.0;
+  for (int s = 1; s <= 16; ++s) {
+    if (s > 1 && nkv / s < 4) break;
+    const long long u = units * s;
+    const long long waves = (u + sm_count - 1) / sm_count;
+    const double eff = (double)u / (double)(waves * sm_count) - 0.01 * (s - 1);
+    if (eff > best_eff + 1e-9) {
+      best_eff = eff;
+      best = s;
+    }
+  }
+  return best;
+}
+
+// ---------------------------------------------------------------- timing
+
+struct TimingRec {
+  cudaEvent_t a, b;
+  int kernel;
+};
+std::mutex g_tmu;
+bool g_timing = false;
+std::vector<TimingRec> g_recs;
+std::vector<cudaEvent_t> g_pool;
+
+cudaEvent_t pool_get() {
+  if (!g_pool.empty()) {
+    cudaEvent_t e = g_pool.back();
+    g_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+// Runs `launch` (returning cudaError_t); when timing is on, brackets it with
+// events on `stream`.
+template <typename F>
+cudaError_t timed(int kernel, cudaStream_t stream, F&& launch) {
+  TimingRec r{nullptr, nullptr, kernel};
+  {
+    std::lock_guard<std::mutex> g(g_tmu);
+    if (g_timing) {
+      r.a = pool_get();
+      r.b = pool_get();
+    }
+  }
+  if (r.a && r.b) cudaEventRecord(r.a, stream);
+  cudaError_t e = launch();
+  if (r.a && r.b) {
+    cudaEventRecord(r.b, stream);
+    std::lock_guard<std::mutex> g(g_tmu);
+    g_recs.push_back(r);
+  }
+  return e;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_timing_enable(int on) {
+  std::lock_guard<std::mutex> g(g_tmu);
+  for (auto& r : g_recs) {
+    cudaEventSynchronize(r.b);
+    g_pool.push_back(r.a);
+    g_pool.push_back(r.b);
+  }
+  g_recs.clear();
+  g_timing = on != 0;
+  return FA_OK;
+}
+
+int fa_timing_read(int kernel, int* launches, double* total_ms) {
+  if (!launches || !total_ms || kernel < 0 || kernel > FA_KERNEL_DQ_CONVERT) return FA_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> g(g_tmu);
+  int n = 0;
+  double ms = 0.0;
+  std::vector<TimingRec> keep;
+  for (auto& r : g_recs) {
+    if (r.kernel != kernel) {
+      keep.push_back(r);
+      continue;
+    }
+    if (cudaEventSynchronize(r.b) != cudaSuccess) return FA_ERR_CUDA;
+    float t = 0.f;
+    if (cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess) return FA_ERR_CUDA;
+    ms += t;
+    ++n;
+    g_pool.push_back(r.a);
+    g_pool.push_back(r.b);
+  }
+  g_recs.swap(keep);
+  *launches = n;
+  *total_ms = ms;
+  return FA_OK;
+}
+
+int fa_abi_version(void) { return FA_ABI_VERSION; }
+
+const char* fa_strerror(int status) {
+  switch (status) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: null or misaligned pointer, bad size or scale";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: head dim must be 64 or 128 on an sm_103 GPU";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA: CUDA runtime or launch failure";
+    case FA_ERR_NO_MEMORY: return "FA_ERR_NO_MEMORY: workspace allocation failed";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a device-side wait gave up";
+    default: return "unknown fa_status";
+  }
+}
+
+uint64_t fa_set_wait_timeout_ns(uint64_t ns) { return g_timeout_ns.exchange(ns); }
+
+int fa_poll_status(void* stream) {
+  DeviceState* s = nullptr;
+  int e = device_state(&s);
+  if (e) return e;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return FA_ERR_CUDA;
+  unsigned int word = 0;
+  if (cudaMemcpy(&word, s->status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+  if (word != 0u && cudaMemset(s->status, 0, sizeof(word)) != cudaSuccess) return FA_ERR_CUDA;
+  return (int)(word & 0xffu);
+}
+
+int fa_selftest_wait_timeout(uint64_t timeout_ns, void* stream) {
+  DeviceState* s = nullptr;
+  int e = device_state(&s);
+  if (e) return e;
+  return fa::launch_selftest_wait(s->status, timeout_ns, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? FA_OK
+             : FA_ERR_CUDA;
+}
+
+int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+              int causal, float scale, int num_splits, void* stream) {
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return FA_ERR_INVALID_ARG;
+  int e = validate(B, H, N, d, scale);
+  if (e) return e;
+  if (num_splits < 0) return FA_ERR_INVALID_ARG;
+  DeviceState* s = nullptr;
+  e = device_state(&s);
+  if (e) return e;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int BH = B * H;
+  const int nkv = (N + 127) / 128;
+  int S = num_splits == 0 ? choose_splits(BH, N, s->sm_count) : num_splits;
+  if (S > nkv) S = nkv;
+  if (S < 1) S = 1;
+  const int per_split = (nkv + S - 1) / S;
+  S = (nkv + per_split - 1) / per_split;  // no empty split
+
+  CUtensorMap tq, tk, tv;
+  if (encode_bhnd(&tq, q, BH, N, d) || encode_bhnd(&tk, k, BH, N, d) || encode_bhnd(&tv, v, BH, N, d))
+    return FA_ERR_CUDA;
+
+  FwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.B = B;
+  p.H = H;
+  p.N = N;
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.num_splits = S;
+  p.kv_tiles_per_split = per_split;
+  p.num_q_blocks = (N + 255) / 256;
+  p.num_units = BH * p.num_q_blocks * S;
+  p.o = o;
+  p.lse = lse;
+  p.status = s->status;
+  p.timeout_ns = g_timeout_ns.load();
+
+  void* ws = nullptr;
+  const size_t rows = (size_t)BH * N;
+  if (S > 1) {
+    const size_t bytes = (size_t)S * rows * ((size_t)d + 1) * sizeof(float);
+    if (cudaMallocAsync(&ws, bytes, st) != cudaSuccess) {
+      cudaGetLastError();
+      return FA_ERR_NO_MEMORY;
+    }
+    p.o_part = static_cast<float*>(ws);
+    p.lse_part = p.o_part + (size_t)S * rows * d;
+  }
+  const int grid = p.num_units < s->sm_count ? p.num_units : s->sm_count;
+  cudaError_t ce = timed(FA_KERNEL_FWD, st, [&] { return fa::launch_fwd(d, tq, tk, tv, p, grid, st); });
+  if (ce == cudaSuccess && S > 1) {
+    fa::CombineParams c;
+    c.rows = (int)rows;
+    c.num_splits = S;
+    c.o_part = p.o_part;
+    c.lse_part = p.lse_part;
+    c.o = o;
+    c.lse = lse;
+    ce = timed(FA_KERNEL_COMBINE, st, [&] { return fa::launch_combine(d, c, st); });
+  }
+  if (ws) cudaFreeAsync(ws, st);
+  return ce == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+           int causal, float scale, void* stream) {
+  return fa_fwd_ex(q, k, v, o, lse, B, H, N, d, causal, scale, 0, stream);
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+           void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale, void* stream) {
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_INVALID_ARG;
+  int e = validate(B, H, N, d, scale);
+  if (e) return e;
+  DeviceState* s = nullptr;
+  e = device_state(&s);
+  if (e) return e;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int BH = B * H;
+  const size_t rows = (size_t)BH * N;
+
+  CUtensorMap tq, tk, tv, tdo;
+  if (encode_bhnd(&tq, q, BH, N, d) || encode_bhnd(&tk, k, BH, N, d) || encode_bhnd(&tv, v, BH, N, d) ||
+      encode_bhnd(&tdo, dout, BH, N, d))
+    return FA_ERR_CUDA;
+
+  // Workspace: fp32 dQ accumulator [rows, d] and D [rows].
+  void* ws = nullptr;
+  const size_t bytes = rows * ((size_t)d + 1) * sizeof(float);
+  if (cudaMallocAsync(&ws, bytes, st) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_NO_MEMORY;
+  }
+  float* dq_acc = static_cast<float*>(ws);
+  float* dvec = dq_acc + rows * d;
+
+  fa::BwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.B = B;
+  p.H = H;
+  p.N = N;
+  p.causal = causal ? 1 : 0;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.lse = lse;
+  p.dvec = dvec;
+  p.dq_acc = dq_acc;
+  p.dk = dk;
+  p.dv = dv;
+  p.num_kv_tiles = (N + 127) / 128;
+  p.num_units = BH * p.num_kv_tiles;
+  p.status = s->status;
+  p.timeout_ns = g_timeout_ns.load();
+
+  cudaError_t ce = timed(FA_KERNEL_BWD_PRE, st,
+                         [&] { return fa::launch_bwd_preprocess(d, o, dout, dvec, dq_acc, (int)rows, st); });
+  if (ce == cudaSuccess) {
+    const int grid = p.num_units < s->sm_count ? p.num_units : s->sm_count;
+    ce = timed(FA_KERNEL_BWD, st, [&] { return fa::launch_bwd(d, tq, tk, tv, tdo, p, grid, st); });
+  }
+  if (ce == cudaSuccess)
+    ce = timed(FA_KERNEL_DQ_CONVERT, st, [&] { return fa::launch_dq_convert(d, dq_acc, dq, rows * d, scale, st); });
+  cudaFreeAsync(ws, st);
+  return ce == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // extern "C"

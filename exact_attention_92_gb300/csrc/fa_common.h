@@ -1,0 +1,74 @@
+// Internal declarations shared by the host API and the kernels.
+#pragma once
+
+#include <cstdint>
+
+#include "fa.h"
+
+namespace fa {
+
+// Tile sizes.  A CTA of the forward kernel owns two 128-row query tiles that
+// share one stream of 128-row key/value tiles.
+constexpr int kTileM = 128;   // query rows per tile (tcgen05 M)
+constexpr int kTileN = 128;   // keys per tile
+constexpr int kQTilesPerCta = 2;
+
+// Codes stored in bits [8,16) of the status word to say which wait gave up.
+enum WaitSite : uint32_t {
+  kWaitQFull = 1,
+  kWaitQEmpty,
+  kWaitKvFull,
+  kWaitKvEmpty,
+  kWaitSFull,
+  kWaitPFull,
+  kWaitOFull,
+  kWaitDrain,
+  kWaitSelfTest,
+  kWaitBwdLoad,
+  kWaitBwdMma,
+  kWaitBwdSoftmax,
+  kWaitBwdDq,
+};
+
+struct FwdParams {
+  int B, H, N;
+  int causal;
+  float scale_log2;            // scale * log2(e)
+  int num_splits;              // 1: write o/lse directly
+  int kv_tiles_per_split;
+  int num_q_blocks;            // ceil(N / 256)
+  int num_units;               // B*H*num_q_blocks*num_splits
+  void* o;                     // bf16 [B,H,N,d]            (num_splits == 1)
+  float* lse;                  // fp32 [B,H,N]              (num_splits == 1)
+  float* o_part;               // fp32 [S,B,H,N,d]          (num_splits > 1)
+  float* lse_part;             // fp32 [S,B,H,N]            (num_splits > 1)
+  unsigned int* status;
+  unsigned long long timeout_ns;
+};
+
+struct CombineParams {
+  int rows;                    // B*H*N
+  int num_splits;
+  const float* o_part;
+  const float* lse_part;
+  void* o;
+  float* lse;
+};
+
+struct BwdParams {
+  int B, H, N;
+  int causal;
+  float scale;                 // softmax scale
+  float scale_log2;            // scale * log2(e)
+  const float* lse;            // fp32 [B,H,N]
+  const float* dvec;           // fp32 [B,H,N], D = rowsum(dO * O)
+  float* dq_acc;               // fp32 [B,H,N,d]
+  void* dk;                    // bf16 [B,H,N,d]
+  void* dv;                    // bf16 [B,H,N,d]
+  int num_kv_tiles;            // ceil(N / 128)
+  int num_units;               // B*H*num_kv_tiles
+  unsigned int* status;
+  unsigned long long timeout_ns;
+};
+
+}  // namespace fa

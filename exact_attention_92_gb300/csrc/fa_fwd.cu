@@ -1,0 +1,501 @@
+// Forward pass of exact attention on sm_103a, FlashAttention-2 style
+// ("FlashAttention V2 in depth", section 6.1; FlashAttention-2 abstract).
+//
+// One persistent CTA per SM walks a static list of work units
+// (batch*head, 256-row query block, key split).  A unit holds two 128-row
+// query tiles Q0, Q1 that stay in shared memory (loaded once, section 2.3)
+// and share one stream of 128-key K/V tiles (the inner loop).  Roles:
+//   warp 9     TMA producer: Q tiles, then K_j, V_j into a ring of slots.
+//   warp 8     MMA issuer (one thread): S_t = Q_t K_j^T and O_t += P_t V_j
+//              with tcgen05 into tensor memory (TMEM).
+//   warps 0-3  softmax of query tile 0, warps 4-7 of tile 1: each thread owns
+//              one query row (the "split along Q" of section 4.2), so row max
+//              and row sum need no communication.
+// TMEM (512 columns): S0 | S1 | O0 | O1.  P (bf16) overwrites the first half
+// of its own S columns and feeds the PV MMA straight from TMEM.
+//
+// Online softmax (section 6.1): the running max m and sum l live in registers
+// of the row's thread, O~ stays unnormalised in TMEM and is divided by l
+// once at the end; L = m + log l is written for the backward pass.  The
+// exp(m_old - m_new) correction of O~ is applied only when a row's max grows
+// by more than 2^8 over the reference the row's O~ and l are kept at;
+// otherwise the old reference stays.  O~ and l always share one reference,
+// so the final O~/l is the same; the weights exp(S - m_ref) stay <= 2^8.
+//
+// Causal mask (section 5): key tiles past a query tile's last row are never
+// loaded or multiplied; only tiles crossing the diagonal (and the ragged last
+// key tile) are masked element by element.
+#include <cuda_runtime.h>
+
+#include "sm103_primitives.cuh"
+
+namespace fa {
+
+using namespace dev;
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kChunks = D / 64;               // 128-byte column blocks per row
+  static constexpr int kChunkBytes = kTileM * 128;     // one 128-row x 64-column block
+  static constexpr int kTileBytes = kTileM * D * 2;    // one 128 x D bf16 tile
+  static constexpr int kStages = (D == 128) ? 4 : 8;   // K/V ring slots
+  static constexpr int kThreads = 320;
+  __host__ __device__ static constexpr uint32_t col_s(int t) { return 128u * t; }
+  __host__ __device__ static constexpr uint32_t col_o(int t) { return 256u + (uint32_t)D * t; }
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffKV = 2 * kTileBytes;
+  static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
+  static constexpr int kNumBars = 2 + 2 + 2 * kStages + 2 + 2 + 2 + 1;
+  static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16;
+  static constexpr float kRescaleThreshold = 8.0f;     // log2 units
+};
+
+struct Unit {
+  int bh;
+  int q0;     // first query row of the 256-row block
+  int kvb;    // first key tile of this split
+  int n[2];   // key tiles processed by query tile 0 / 1 (0 = none)
+};
+
+__device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
+  Unit w;
+  const int split = u % p.num_splits;
+  const int r = u / p.num_splits;
+  const int BH = p.B * p.H;
+  w.bh = r % BH;
+  // Query blocks in decreasing order: with the causal mask the last blocks
+  // carry the most key tiles, so they start first (longest job first).
+  const int qb = p.num_q_blocks - 1 - r / BH;
+  w.q0 = qb * (kTileM * kQTilesPerCta);
+  const int nkv = (p.N + kTileN - 1) / kTileN;
+  const int lo = split * p.kv_tiles_per_split;
+  const int hi = min(nkv, lo + p.kv_tiles_per_split);
+  w.kvb = lo;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int row0 = w.q0 + kTileM * t;
+    if (row0 >= p.N) {
+      w.n[t] = 0;
+    } else {
+      const int last = min(p.N, row0 + kTileM) - 1;
+      const int h = p.causal ? min(hi, last / kTileN + 1) : hi;
+      w.n[t] = max(0, h - lo);
+    }
+  }
+  return w;
+}
+
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint32_t q_addr, uint32_t k_addr) {
+  using C = FwdCfg<D>;
+  constexpr uint32_t idesc = idesc_bf16(kTileM, kTileN, false, false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
+    mma_ss(tmem_s, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024), idesc,
+           kk > 0 ? 1u : 0u);
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_addr, bool accumulate) {
+  using C = FwdCfg<D>;
+  constexpr uint32_t idesc = idesc_bf16(kTileM, D, false, true);
+#pragma unroll
+  for (int kk = 0; kk < kTileN / 16; ++kk) {
+    mma_ts(tmem_o, tmem_p + kk * 8, sdesc_sw128(v_addr + kk * 16 * 128, C::kChunkBytes, 1024), idesc,
+           (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(320, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+  using C = FwdCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  // The 128-byte swizzle anchors at 1024-byte boundaries: refuse to run (and
+  // report) if the dynamic shared memory base is not aligned.
+  if ((smem_u32(smem) & 1023u) != 0u) {
+    if (threadIdx.x == 0) atomicCAS(p.status, 0u, (unsigned int)FA_ERR_CUDA);
+    return;
+  }
+  uint8_t* sQ = smem + C::kOffQ;
+  uint8_t* sKV = smem + C::kOffKV;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* q_full = bars;
+  uint64_t* q_empty = bars + 2;
+  uint64_t* kv_full = bars + 4;
+  uint64_t* kv_empty = kv_full + C::kStages;
+  uint64_t* s_full = kv_empty + C::kStages;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* o_full = p_full + 2;
+  uint64_t* drain = o_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 4 * 32);
+      mbar_init(&o_full[i], 1);
+    }
+    for (int i = 0; i < C::kStages; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+    }
+    mbar_init(drain, 1);
+    fence_barrier_init();
+  }
+  if (warp == 8) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 9 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl ctl{p.status, p.timeout_ns};
+
+  if (warp == 9) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t rc = 0;
+      uint32_t qc[2] = {0, 0};
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+        const Unit w = decode_unit(p, u);
+        for (int t = 0; ok && t < 2; ++t) {
+          if (w.n[t] == 0) continue;
+          ok = mbar_wait(&q_empty[t], (qc[t] & 1) ^ 1, ctl, kWaitQEmpty);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&q_full[t], C::kTileBytes);
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_3d(sQ + t * C::kTileBytes + c * C::kChunkBytes, &tm_q, &q_full[t], c * 64,
+                        w.q0 + kTileM * t, w.bh);
+          ++qc[t];
+        }
+        const int nmax = max(w.n[0], w.n[1]);
+        for (int j = 0; ok && j < nmax; ++j) {
+          for (int which = 0; which < 2; ++which) {
+            const uint32_t slot = rc % C::kStages;
+            ok = mbar_wait(&kv_empty[slot], ((rc / C::kStages) & 1) ^ 1, ctl, kWaitKvEmpty);
+            if (!ok) break;
+            mbar_arrive_expect_tx(&kv_full[slot], C::kTileBytes);
+            const CUtensorMap* m = which ? &tm_v : &tm_k;
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_load_3d(sKV + slot * C::kTileBytes + c * C::kChunkBytes, m, &kv_full[slot], c * 64,
+                          (w.kvb + j) * kTileN, w.bh);
+            ++rc;
+          }
+        }
+      }
+      // Let every copy this thread started land before the CTA can exit.
+      const uint32_t first = rc > (uint32_t)C::kStages ? rc - C::kStages : 0u;
+      for (uint32_t pos = first; pos < rc; ++pos)
+        mbar_wait(&kv_full[pos % C::kStages], (pos / C::kStages) & 1, ctl, kWaitDrain);
+      for (int t = 0; t < 2; ++t)
+        if (qc[t] > 0) mbar_wait(&q_full[t], (qc[t] - 1) & 1, ctl, kWaitDrain);
+    }
+  } else if (warp == 8) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t sq = smem_u32(sQ);
+      const uint32_t skv = smem_u32(sKV);
+      uint32_t rc = 0;
+      uint32_t qc[2] = {0, 0}, pc[2] = {0, 0};
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+        const Unit w = decode_unit(p, u);
+        const int nmax = max(w.n[0], w.n[1]);
+        if (nmax == 0) continue;
+        for (int t = 0; ok && t < 2; ++t) {
+          if (w.n[t] == 0) continue;
+          ok = mbar_wait(&q_full[t], qc[t] & 1, ctl, kWaitQFull);
+          ++qc[t];
+        }
+        if (!ok) break;
+        {
+          const uint32_t slot_k = rc % C::kStages;
+          ok = mbar_wait(&kv_full[slot_k], (rc / C::kStages) & 1, ctl, kWaitKvFull);
+          if (!ok) break;
+          tc_fence_after();
+          for (int t = 0; t < 2; ++t) {
+            if (w.n[t] == 0) continue;
+            issue_qk<D>(tmem + C::col_s(t), sq + t * C::kTileBytes, skv + slot_k * C::kTileBytes);
+            mma_commit(&s_full[t]);
+          }
+          mma_commit(&kv_empty[slot_k]);
+        }
+        for (int j = 0; ok && j < nmax; ++j) {
+          const uint32_t pos_v = rc + 2 * j + 1;
+          const uint32_t pos_k = pos_v + 1;
+          const uint32_t slot_v = pos_v % C::kStages;
+          const uint32_t slot_k = pos_k % C::kStages;
+          ok = mbar_wait(&kv_full[slot_v], (pos_v / C::kStages) & 1, ctl, kWaitKvFull);
+          if (!ok) break;
+          tc_fence_after();
+          bool k_ready = false;
+          for (int t = 0; t < 2; ++t) {
+            if (j >= w.n[t]) continue;
+            ok = mbar_wait(&p_full[t], pc[t] & 1, ctl, kWaitPFull);
+            ++pc[t];
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv<D>(tmem + C::col_o(t), tmem + C::col_s(t), skv + slot_v * C::kTileBytes, j > 0);
+            if (j + 1 < w.n[t]) {
+              if (!k_ready) {
+                ok = mbar_wait(&kv_full[slot_k], (pos_k / C::kStages) & 1, ctl, kWaitKvFull);
+                if (!ok) break;
+                tc_fence_after();
+                k_ready = true;
+              }
+              issue_qk<D>(tmem + C::col_s(t), sq + t * C::kTileBytes, skv + slot_k * C::kTileBytes);
+              mma_commit(&s_full[t]);
+            } else {
+              mma_commit(&o_full[t]);
+              mma_commit(&q_empty[t]);
+            }
+          }
+          if (!ok) break;
+          mma_commit(&kv_empty[slot_v]);
+          if (j + 1 < nmax) mma_commit(&kv_empty[slot_k]);
+        }
+        rc += 2 * nmax;
+      }
+      // Every MMA this thread issued completes before TMEM is released.
+      mma_commit(drain);
+      mbar_wait(drain, 0, ctl, kWaitDrain);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------- softmax
+    const int t = warp >> 2;
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+    const uint32_t tS = tmem + lane_off + C::col_s(t);
+    const uint32_t tO = tmem + lane_off + C::col_o(t);
+    const int r_in_tile = 32 * (warp & 3) + lane;
+    const float sl2 = p.scale_log2;
+    uint32_t sc = 0, oc = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+      const Unit w = decode_unit(p, u);
+      const int row0 = w.q0 + kTileM * t;
+      const int row = row0 + r_in_tile;
+      const int split = u % p.num_splits;
+      if (w.n[t] == 0) {
+        // No visible key in this split: an empty partial (O = 0, L = -inf).
+        if (p.num_splits > 1 && row < p.N) {
+          const size_t prow = ((size_t)split * p.B * p.H + w.bh) * p.N + row;
+          float4* dst = reinterpret_cast<float4*>(p.o_part + prow * D);
+          for (int c = 0; c < D / 4; ++c) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+          p.lse_part[prow] = -INFINITY;
+        }
+        continue;
+      }
+      float m_ref = -INFINITY;  // reference max of this row, log2 units
+      float l = 0.f;
+      for (int j = 0; j < w.n[t]; ++j) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t], sc & 1, ctl, kWaitSFull));
+        ++sc;
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t s[kTileN];
+#pragma unroll
+        for (int c = 0; c < kTileN / 32; ++c) tmem_ld32(tS + 32 * c, s + 32 * c);
+        tmem_ld_wait<kTileN>(s);
+        float x[kTileN];
+#pragma unroll
+        for (int c = 0; c < kTileN; ++c) x[c] = __uint_as_float(s[c]);
+        const int kv0 = (w.kvb + j) * kTileN;
+        const bool need_mask = (kv0 + kTileN > p.N) || (p.causal && kv0 + kTileN - 1 > row0);
+        if (need_mask) {
+          const int lim = p.causal ? min(p.N - 1, row) : p.N - 1;  // last visible key
+#pragma unroll
+          for (int c = 0; c < kTileN; ++c)
+            if (kv0 + c > lim) x[c] = -INFINITY;
+        }
+        float mx[4] = {x[0], x[1], x[2], x[3]};
+#pragma unroll
+        for (int c = 4; c < kTileN; c += 4) {
+          mx[0] = fmaxf(mx[0], x[c]);
+          mx[1] = fmaxf(mx[1], x[c + 1]);
+          mx[2] = fmaxf(mx[2], x[c + 2]);
+          mx[3] = fmaxf(mx[3], x[c + 3]);
+        }
+        const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
+        float f = 1.f;
+        bool rescale = false;
+        if (j == 0) {
+          m_ref = (m_tile == -INFINITY) ? 0.f : m_tile;
+        } else if (__any_sync(0xffffffffu, m_tile > m_ref + C::kRescaleThreshold)) {
+          const float m_new = fmaxf(m_ref, m_tile);
+          f = ex2_approx(m_ref - m_new);
+          l *= f;
+          m_ref = m_new;
+          rescale = true;
+        }
+        // P = exp2(S * scale * log2(e) - m_ref), 32 columns at a time, packed
+        // to bf16 over the already-read S columns.
+        const float neg = -m_ref;
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int h = 0; h < kTileN / 32; ++h) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float p0 = ex2_approx(fmaf(x[32 * h + e], sl2, neg));
+            const float p1 = ex2_approx(fmaf(x[32 * h + e + 1], sl2, neg));
+            ls[(e >> 1) & 3] += p0 + p1;
+            pk[e / 2] = pack_bf16(p0, p1);
+          }
+          tmem_st16(tS + 16 * h, pk);
+        }
+        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        if (rescale) {
+          // O~ <- exp2(m_old - m_new) O~; the previous PV MMA has completed
+          // (it was issued before this S tile's MMA) and the next one waits
+          // for the arrive below.
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + 32 * c, o);
+            tmem_ld_wait<32>(o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
+            tmem_st32(tO + 32 * c, o);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&p_full[t]);
+      }
+      if (!ok) break;
+      ok = __all_sync(0xffffffffu, mbar_wait(&o_full[t], oc & 1, ctl, kWaitOFull));
+      ++oc;
+      if (!ok) break;
+      tc_fence_after();
+      const float inv_l = 1.0f / l;
+      const float lse = (m_ref + lg2_approx(l)) * 0.69314718055994530942f;
+      if (p.num_splits == 1) {
+        const size_t grow = (size_t)w.bh * p.N + row;
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + grow * D);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + 32 * c, o);
+          tmem_ld_wait<32>(o);
+          if (row < p.N) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              uint4 v;
+              v.x = pack_bf16(__uint_as_float(o[8 * i + 0]) * inv_l, __uint_as_float(o[8 * i + 1]) * inv_l);
+              v.y = pack_bf16(__uint_as_float(o[8 * i + 2]) * inv_l, __uint_as_float(o[8 * i + 3]) * inv_l);
+              v.z = pack_bf16(__uint_as_float(o[8 * i + 4]) * inv_l, __uint_as_float(o[8 * i + 5]) * inv_l);
+              v.w = pack_bf16(__uint_as_float(o[8 * i + 6]) * inv_l, __uint_as_float(o[8 * i + 7]) * inv_l);
+              dst[c * 4 + i] = v;
+            }
+          }
+        }
+        if (row < p.N) p.lse[grow] = lse;
+      } else {
+        const size_t prow = ((size_t)split * p.B * p.H + w.bh) * p.N + row;
+        float4* dst = reinterpret_cast<float4*>(p.o_part + prow * D);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + 32 * c, o);
+          tmem_ld_wait<32>(o);
+          if (row < p.N) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[c * 8 + i] = make_float4(__uint_as_float(o[4 * i]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
+                                           __uint_as_float(o[4 * i + 2]) * inv_l,
+                                           __uint_as_float(o[4 * i + 3]) * inv_l);
+          }
+        }
+        if (row < p.N) p.lse_part[prow] = lse;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// Merge of split-KV partial results: L = log sum_s exp(L_s),
+// O = sum_s exp(L_s - L) O_s.  One warp per query row.
+template <int D>
+__global__ void __launch_bounds__(256) fa_combine_kernel(const CombineParams p) {
+  const int row = blockIdx.x * 8 + threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  if (row >= p.rows) return;
+  constexpr int kPer = D / 32;
+  float mx = -INFINITY;
+  for (int s = 0; s < p.num_splits; ++s) mx = fmaxf(mx, p.lse_part[(size_t)s * p.rows + row]);
+  float acc[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
+  float tot = 0.f;
+  for (int s = 0; s < p.num_splits; ++s) {
+    const float ls = p.lse_part[(size_t)s * p.rows + row];
+    const float wgt = (ls == -INFINITY) ? 0.f : exp2f((ls - mx) * 1.4426950408889634f);
+    tot += wgt;
+    const float* src = p.o_part + ((size_t)s * p.rows + row) * D + lane * kPer;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) acc[i] = fmaf(wgt, src[i], acc[i]);
+  }
+  const float inv = 1.0f / tot;
+  __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.o) + (size_t)row * D + lane * kPer;
+  if constexpr (kPer == 2) {
+    *reinterpret_cast<uint32_t*>(o) = pack_bf16(acc[0] * inv, acc[1] * inv);
+  } else {
+    uint2 v;
+    v.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+    v.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+    *reinterpret_cast<uint2*>(o) = v;
+  }
+  if (lane == 0) p.lse[row] = mx + logf(tot);
+}
+
+// ------------------------------------------------------------------ launch
+
+template <int D>
+static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                const FwdParams& p, int grid, cudaStream_t stream) {
+  using C = FwdCfg<D>;
+  cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  fa_fwd_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const FwdParams& p, int grid, cudaStream_t stream) {
+  return d == 64 ? launch_fwd_t<64>(tq, tk, tv, p, grid, stream) : launch_fwd_t<128>(tq, tk, tv, p, grid, stream);
+}
+
+cudaError_t launch_combine(int d, const CombineParams& p, cudaStream_t stream) {
+  const int grid = (p.rows + 7) / 8;
+  if (d == 64)
+    fa_combine_kernel<64><<<grid, 256, 0, stream>>>(p);
+  else
+    fa_combine_kernel<128><<<grid, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace fa

@@ -120,11 +120,24 @@ def make_case(
 
 
 def sample_rows(seed: int, N: int, n: int = SAMPLE_ROWS) -> np.ndarray:
-    """Seeded query rows checked per head when N is large (sorted)."""
+    """Seeded query rows checked when N is large (sorted)."""
     if N <= n:
         return np.arange(N)
     rng = np.random.default_rng(seed + 7)
     return np.sort(rng.choice(N, n, replace=False))
+
+
+def sample_rows_per_head(seed: int, B: int, H: int, N: int, n: int = SAMPLE_ROWS) -> np.ndarray:
+    """[B, H, min(N, n)] sorted query rows, drawn head after head from one
+    ``default_rng(seed + 7)`` stream (all rows when N <= n)."""
+    if N <= n:
+        return np.broadcast_to(np.arange(N), (B, H, N)).copy()
+    rng = np.random.default_rng(seed + 7)
+    out = np.empty((B, H, n), dtype=np.int64)
+    for b in range(B):
+        for h in range(H):
+            out[b, h] = np.sort(rng.choice(N, n, replace=False))
+    return out
 
 
 # Workloads: the five problem families exact attention is measured on.

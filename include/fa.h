@@ -1,0 +1,149 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) exact-attention library (libfa.so).
+ *
+ * The library computes exact scaled-dot-product attention the way
+ * FlashAttention-2 does ("FlashAttention-2: Faster Attention with Better
+ * Parallelism and Work Partitioning", abstract; "FlashAttention V2 in depth",
+ * sections 2, 5, 6 and 7): tile by tile with an online softmax, query tiles in
+ * the outer (parallel) loop and key/value tiles in the inner loop, an
+ * unnormalised accumulator divided once at the end, the row logsumexp kept
+ * for the backward pass, fully masked causal tiles skipped, and the matching
+ * dQ/dK/dV backward pass with a separate D preprocess.
+ *
+ * Conventions shared by every entry point:
+ *  - Tensors live in device memory of the current CUDA device.  Q, K, V, O,
+ *    dO, dQ, dK, dV are bf16, shape [B, H, N, d], contiguous row-major (d is
+ *    the fastest index).  LSE is fp32, shape [B, H, N], natural logarithm.
+ *  - Pointers must be non-null and 16-byte aligned.
+ *  - d must be 64 or 128.  B, H, N >= 1.  Queries and keys have the same
+ *    length N; N need not be a multiple of the tile size.
+ *  - causal != 0 applies the mask of "FlashAttention V2 in depth" section 5.1:
+ *    query row i sees key j iff j <= i (top-left aligned).
+ *  - scale multiplies Q K^T before the softmax; pass 1/sqrt(d) for the usual
+ *    attention.  It must be finite and positive.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; 0 = legacy default
+ *    stream) and never synchronise it, except fa_poll_status.
+ *  - The caller owns every buffer it passes; the library never frees or keeps
+ *    them.  Temporary device workspace (split-KV partials, the fp32 dQ
+ *    accumulator) is taken with cudaMallocAsync on `stream` and returned with
+ *    cudaFreeAsync on the same stream, so it is stream-ordered.
+ *  - Return value: FA_OK, or an fa_status code.  Argument errors are detected
+ *    on the host before anything is launched.  A device-side wait that gives
+ *    up (see fa_set_wait_timeout_ns) is reported later by fa_poll_status.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FA_ABI_VERSION 1
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size or scale      */
+  FA_ERR_UNSUPPORTED = 2, /* head dim not 64/128, or device is not sm_103    */
+  FA_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed     */
+  FA_ERR_NO_MEMORY = 4,   /* workspace allocation failed                     */
+  FA_ERR_TIMEOUT = 5      /* a device-side wait gave up (fa_poll_status)     */
+} fa_status;
+
+/*
+ * Forward pass.  "FlashAttention V2 in depth", section 6.1 (full forward
+ * algorithm) with the causal block skip of section 5.3.
+ *   q, k, v : in,  bf16 [B,H,N,d]
+ *   o       : out, bf16 [B,H,N,d], O = softmax(scale * Q K^T [+ mask]) V
+ *   lse     : out, fp32 [B,H,N],  L_i = m_i + log(l_i) = log sum_j exp(S_ij)
+ * Long sequences with few (batch, head) pairs are split along the keys
+ * automatically (sequence parallelism, FlashAttention-2 abstract point (2));
+ * see fa_fwd_ex.
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+           int causal, float scale, void* stream);
+
+/*
+ * Forward pass with an explicit number of key splits.
+ *   num_splits : 0 = automatic, 1 = no split, S > 1 = split the key range of
+ *                every query tile into S parts whose partial results (fp32 O
+ *                and LSE per part, in workspace) are merged by a second
+ *                kernel: L = log sum_s exp(L_s), O = sum_s exp(L_s - L) O_s.
+ *                S is clamped to the number of 128-key tiles.
+ * Other arguments as fa_fwd.
+ */
+int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+              int causal, float scale, int num_splits, void* stream);
+
+/*
+ * Backward pass.  "FlashAttention V2 in depth", section 7: key/value tiles in
+ * the outer loop (dK, dV accumulated by one CTA each, no atomics), dQ
+ * accumulated across CTAs with fp32 atomic adds into a workspace, P
+ * recomputed from the saved logsumexp (section 7.1), and D_i = rowsum(dO_i *
+ * O_i) from a separate preprocess kernel (section 7.3).
+ *   q, k, v : in,  bf16 [B,H,N,d] (the forward inputs)
+ *   o       : in,  bf16 [B,H,N,d] (the forward output)
+ *   lse     : in,  fp32 [B,H,N]   (the forward logsumexp)
+ *   dout    : in,  bf16 [B,H,N,d] (gradient of the loss w.r.t. O)
+ *   dq,dk,dv: out, bf16 [B,H,N,d]
+ * dq is not bitwise reproducible from run to run (atomic summation order).
+ */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+           void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale, void* stream);
+
+/*
+ * Synchronise `stream`, then return and clear the device status word of the
+ * current device: FA_OK, FA_ERR_TIMEOUT if a kernel's bounded wait gave up
+ * since the last poll, or FA_ERR_CUDA if the synchronisation failed.
+ */
+int fa_poll_status(void* stream);
+
+/*
+ * Time limit of every device-side wait (mbarrier waits between the load,
+ * MMA and softmax roles).  A wait that exceeds it records FA_ERR_TIMEOUT,
+ * and the kernel unwinds: it stops issuing work, waits (bounded) for its
+ * own copies and MMAs in flight, frees its tensor memory and returns.
+ * Default 2 s.  Returns the previous value.  Applies to later launches.
+ */
+uint64_t fa_set_wait_timeout_ns(uint64_t ns);
+
+/*
+ * Self-test of the give-up path: launches one CTA that waits on an mbarrier
+ * nothing ever arrives on, with a time limit of `timeout_ns`.  The kernel
+ * records FA_ERR_TIMEOUT and returns; fa_poll_status then reports it.
+ */
+int fa_selftest_wait_timeout(uint64_t timeout_ns, void* stream);
+
+/*
+ * Per-kernel timing for benchmarks.  While enabled, every launch of a library
+ * kernel is bracketed by two CUDA events recorded on the launch's stream.
+ * Kernel ids: FA_KERNEL_FWD (forward main kernel), FA_KERNEL_COMBINE
+ * (split-KV merge), FA_KERNEL_BWD_PRE (D preprocess), FA_KERNEL_BWD
+ * (backward main kernel), FA_KERNEL_DQ_CONVERT.
+ *   fa_timing_enable(on) : 1 starts recording (and drops old records), 0 stops.
+ *   fa_timing_read(kernel, launches, total_ms) : waits for the recorded
+ *       events of that kernel, returns how many launches were recorded and
+ *       their summed device time in milliseconds, and forgets them.
+ * Both return FA_OK, FA_ERR_INVALID_ARG (bad id / null out-pointer) or
+ * FA_ERR_CUDA.
+ */
+#define FA_KERNEL_FWD 0
+#define FA_KERNEL_COMBINE 1
+#define FA_KERNEL_BWD_PRE 2
+#define FA_KERNEL_BWD 3
+#define FA_KERNEL_DQ_CONVERT 4
+int fa_timing_enable(int on);
+int fa_timing_read(int kernel, int* launches, double* total_ms);
+
+/* Human-readable name of an fa_status code (static storage). */
+const char* fa_strerror(int status);
+
+/* FA_ABI_VERSION of the loaded library. */
+int fa_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

@@ -1,0 +1,65 @@
+"""Comparison of CUDA results with the fp64 oracle, at the stated tolerances.
+
+Tolerances (attention forward / backward on bf16 inputs):
+  O    : max |O_gpu - O_ref| <= 1e-2, element by element relaxed to one bf16
+         ulp of O_ref where |O_ref| >= 2 (a correctly rounded bf16 output can
+         sit half an ulp = 2^-9 |O| away from the fp64 value, more than 1e-2
+         once |O| > 5); and mean |O_gpu - bf16(O_ref)| <= 1e-3.
+  LSE  : |L_gpu - L_ref| <= 1e-4 * max(1, |L_ref|) (relative error, with an
+         absolute floor where L is near 0, e.g. causal row 0).
+  grads: max |g_gpu - g_ref| <= 5e-2 * max |g_ref|, per tensor.
+The oracle works in fp64 on the same bf16-rounded inputs.
+"""
+
+import numpy as np
+
+from exact_attention_92_gb300 import inputs
+
+O_MAX_ABS = 1e-2
+O_MEAN_ABS = 1e-3
+LSE_REL = 1e-4
+GRAD_REL = 5e-2
+
+
+def bf16_ulp(x):
+    """Spacing of bf16 numbers at |x| (2^(e-7) for |x| in [2^e, 2^(e+1)))."""
+    a = np.maximum(np.abs(x), np.finfo(np.float32).tiny)
+    e = np.floor(np.log2(a))
+    return np.exp2(e - 7)
+
+
+def round_bf16(x):
+    return inputs.bits_to_f64(inputs.bf16_bits(np.asarray(x, dtype=np.float32)))
+
+
+def check_o(o_gpu, o_ref, what=""):
+    o_gpu = np.asarray(o_gpu, dtype=np.float64)
+    err = np.abs(o_gpu - o_ref)
+    allowed = np.maximum(O_MAX_ABS, bf16_ulp(o_ref))
+    bad = err > allowed
+    assert not np.isnan(o_gpu).any(), f"{what}: NaN in O"
+    assert not bad.any(), (f"{what}: O max-abs error {err.max():.3e} over the bound at "
+                           f"{np.argwhere(bad)[:5].tolist()} (ref {o_ref[bad][:5]}, gpu {o_gpu[bad][:5]})")
+    mean = float(np.mean(np.abs(o_gpu - round_bf16(o_ref))))
+    assert mean <= O_MEAN_ABS, f"{what}: O mean-abs error {mean:.3e} > {O_MEAN_ABS}"
+    return float(err.max()), mean
+
+
+def check_lse(l_gpu, l_ref, what=""):
+    l_gpu = np.asarray(l_gpu, dtype=np.float64)
+    err = np.abs(l_gpu - l_ref)
+    bound = LSE_REL * np.maximum(1.0, np.abs(l_ref))
+    assert not np.isnan(l_gpu).any(), f"{what}: NaN in LSE"
+    bad = err > bound
+    assert not bad.any(), (f"{what}: LSE error {err.max():.3e} at {np.argwhere(bad)[:5].tolist()} "
+                           f"(ref {l_ref[bad][:5]}, gpu {l_gpu[bad][:5]})")
+    return float(np.max(err / np.maximum(1.0, np.abs(l_ref))))
+
+
+def check_grad(g_gpu, g_ref, name, what=""):
+    g_gpu = np.asarray(g_gpu, dtype=np.float64)
+    assert not np.isnan(g_gpu).any(), f"{what}: NaN in {name}"
+    scale = float(np.max(np.abs(g_ref)))
+    err = float(np.max(np.abs(g_gpu - g_ref)))
+    assert err <= GRAD_REL * scale, f"{what}: {name} max-abs error {err:.3e} > {GRAD_REL} x {scale:.3e}"
+    return err / scale

@@ -1,0 +1,104 @@
+"""The C ABI library without a GPU: it loads, exports every entry point
+include/fa.h declares, and rejects bad arguments on the host before any
+device work (no compute call is made here)."""
+
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+import exact_attention_92_gb300 as fa
+from exact_attention_92_gb300 import _binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return fa.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = fa.declared_symbols()
+    assert {"fa_fwd", "fa_fwd_ex", "fa_bwd", "fa_poll_status", "fa_strerror", "fa_abi_version"} <= set(declared)
+    out = subprocess.run(["nm", "-D", "--defined-only", _binding.LIB_PATH], capture_output=True, text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    missing = [s for s in declared if s not in exported]
+    assert not missing, missing
+    for s in declared:
+        assert hasattr(lib, s)
+
+
+def test_no_driver_dependency():
+    out = subprocess.run(["ldd", _binding.LIB_PATH], capture_output=True, text=True).stdout
+    assert "libcuda.so" not in out and "libcudart" not in out
+
+
+def test_version_and_strerror(lib):
+    assert fa.fa_abi_version() == 1
+    for code in range(6):
+        assert fa.fa_strerror(code).startswith("FA_")
+    assert "unknown" in fa.fa_strerror(99)
+
+
+P = ctypes.c_void_p
+
+
+def _fwd(lib, q=0x1000, k=0x2000, v=0x3000, o=0x4000, lse=0x5000, B=1, H=1, N=128, d=64, causal=0,
+         scale=0.125, splits=0):
+    return lib.fa_fwd_ex(P(q), P(k), P(v), P(o), P(lse), B, H, N, d, causal, scale, splits, None)
+
+
+def test_fwd_argument_errors(lib):
+    assert _fwd(lib, q=0) == fa.FA_ERR_INVALID_ARG          # null
+    assert _fwd(lib, k=0x2008) == fa.FA_ERR_INVALID_ARG     # not 16-byte aligned
+    assert _fwd(lib, lse=0x5004) == fa.FA_ERR_INVALID_ARG
+    assert _fwd(lib, B=0) == fa.FA_ERR_INVALID_ARG
+    assert _fwd(lib, N=0) == fa.FA_ERR_INVALID_ARG
+    assert _fwd(lib, H=-3) == fa.FA_ERR_INVALID_ARG
+    assert _fwd(lib, scale=float("nan")) == fa.FA_ERR_INVALID_ARG
+    assert _fwd(lib, scale=float("inf")) == fa.FA_ERR_INVALID_ARG
+    assert _fwd(lib, scale=-1.0) == fa.FA_ERR_INVALID_ARG
+    assert _fwd(lib, splits=-1) == fa.FA_ERR_INVALID_ARG
+    assert _fwd(lib, d=96) == fa.FA_ERR_UNSUPPORTED
+    assert _fwd(lib, d=256) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_bwd_argument_errors(lib):
+    ptrs = [P(0x1000 * (i + 1)) for i in range(9)]
+
+    def call(ptrs=ptrs, B=1, H=1, N=64, d=64, scale=0.125):
+        return lib.fa_bwd(*ptrs, B, H, N, d, 1, scale, None)
+
+    for i in range(9):
+        bad = list(ptrs)
+        bad[i] = P(0)
+        assert call(bad) == fa.FA_ERR_INVALID_ARG
+        bad[i] = P(0x1000 * (i + 1) + 2)
+        assert call(bad) == fa.FA_ERR_INVALID_ARG
+    assert call(N=0) == fa.FA_ERR_INVALID_ARG
+    assert call(d=32) == fa.FA_ERR_UNSUPPORTED
+    assert call(scale=0.0) == fa.FA_ERR_INVALID_ARG
+
+
+def test_timing_read_argument_errors(lib):
+    n = ctypes.c_int()
+    ms = ctypes.c_double()
+    assert lib.fa_timing_read(7, ctypes.byref(n), ctypes.byref(ms)) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_timing_read(0, None, ctypes.byref(ms)) == fa.FA_ERR_INVALID_ARG
+
+
+def test_python_binding_rejects_cpu_tensors(lib):
+    torch = pytest.importorskip("torch")
+    q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa.forward(q, q, q)
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(_binding, "_lib", None)
+    monkeypatch.setattr(_binding, "LIB_PATH", str(tmp_path / "libfa.so"))
+    with pytest.raises(fa.FaError):
+        _binding.load()

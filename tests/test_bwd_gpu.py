@@ -1,0 +1,73 @@
+"""Backward pass on the GPU against the fp64 oracle (through the C ABI)."""
+
+import numpy as np
+import pytest
+
+from exact_attention_92_gb300 import inputs
+from oracle import attention as att
+
+from gpu_util import case_tensors, dev, ensure_built, host, torch_cuda
+from parity import check_grad
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fa():
+    torch_cuda()
+    return ensure_built()
+
+
+def run(fa, case):
+    q, k, v, do = case_tensors(case)
+    o, lse = fa.forward(q, k, v, causal=case.causal)
+    dq, dk, dv = fa.backward(q, k, v, o, lse, do, causal=case.causal)
+    st = fa.fa_poll_status()
+    assert st == 0, fa.fa_strerror(st)
+    return host(dq), host(dk), host(dv)
+
+
+SMALL = [(1, 1, 128, 64), (1, 2, 128, 128), (1, 1, 200, 128), (2, 2, 257, 64), (1, 1, 1, 64),
+         (1, 1, 63, 128), (2, 1, 384, 128), (1, 3, 640, 64)]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: "x".join(map(str, s)))
+def test_small_shapes(fa, shape, causal):
+    B, H, N, d = shape
+    case = inputs.make_case(B, H, N, d, causal, seed=500 + N + d, with_do=True)
+    dq, dk, dv = run(fa, case)
+    rq, rk, rv = att.backward(case.f64("q"), case.f64("k"), case.f64("v"), case.f64("do"), case.scale, causal)
+    what = f"{shape} causal={causal}"
+    check_grad(dq, rq, "dQ", what)
+    check_grad(dk, rk, "dK", what)
+    check_grad(dv, rv, "dV", what)
+
+
+def test_fwd_bwd_b2_h16_n4096_d128_causal(fa):
+    """dK, dV in full on 8 seeded heads; dQ on 1024 seeded rows of every head."""
+    c = inputs.workload_cases()[5][0]
+    case = inputs.make_case(**c)
+    dq, dk, dv = run(fa, case)
+    q, k, v, do = case.f64("q"), case.f64("k"), case.f64("v"), case.f64("do")
+    rng = np.random.default_rng(case.seed + 11)
+    heads = [(int(i) // case.H, int(i) % case.H) for i in rng.choice(case.B * case.H, 8, replace=False)]
+    rq, rk, rv = att.backward(q, k, v, do, case.scale, True, heads=heads)
+    for b, h in heads:
+        check_grad(dk[b, h], rk[b, h], "dK", f"head {(b, h)}")
+        check_grad(dv[b, h], rv[b, h], "dV", f"head {(b, h)}")
+    rows = inputs.sample_rows_per_head(case.seed, case.B, case.H, case.N)
+    for b in range(case.B):
+        for h in range(case.H):
+            ref = att.backward_dq_rows_head(q[b, h], k[b, h], v[b, h], do[b, h], case.scale, True, rows[b, h])
+            check_grad(dq[b, h, rows[b, h]], ref, "dQ", f"head {(b, h)}")
+    assert np.isfinite(dq).all() and np.isfinite(dk).all() and np.isfinite(dv).all()
+
+
+def test_dq_close_between_runs(fa):
+    """dQ sums with atomics in varying order: runs agree to rounding only."""
+    case = inputs.make_case(1, 4, 512, 128, True, seed=77, with_do=True)
+    a = run(fa, case)
+    b = run(fa, case)
+    for x, y in zip(a, b):
+        assert np.max(np.abs(x - y)) <= 1e-2 * max(1e-6, np.max(np.abs(x)))

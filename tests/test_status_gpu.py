@@ -1,0 +1,67 @@
+"""Failure detection on the GPU without a fault: a bounded device wait that
+runs out records FA_ERR_TIMEOUT, the kernel returns, and the context stays
+usable."""
+
+import numpy as np
+import pytest
+
+from exact_attention_92_gb300 import inputs
+from oracle import attention as att
+
+from gpu_util import case_tensors, ensure_built, host, torch_cuda
+from parity import check_o
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fa():
+    torch_cuda()
+    return ensure_built()
+
+
+def test_wait_gives_up_and_reports(fa):
+    assert fa.fa_poll_status() == fa.FA_OK
+    fa.fa_selftest_wait_timeout(50_000_000)  # 50 ms on a barrier nothing arrives on
+    assert fa.fa_poll_status() == fa.FA_ERR_TIMEOUT
+    assert fa.fa_poll_status() == fa.FA_OK  # read clears the word
+
+
+def test_context_usable_after_timeout(fa):
+    fa.fa_selftest_wait_timeout(10_000_000)
+    assert fa.fa_poll_status() == fa.FA_ERR_TIMEOUT
+    case = inputs.make_case(1, 2, 300, 64, True, seed=9)
+    q, k, v, _ = case_tensors(case)
+    o, lse = fa.forward(q, k, v, causal=True)
+    assert fa.fa_poll_status() == fa.FA_OK
+    O, _ = att.forward(case.f64("q"), case.f64("k"), case.f64("v"), case.scale, True)
+    check_o(host(o), O, "after timeout")
+
+
+def test_bad_arguments_raise_before_launch(fa):
+    torch = torch_cuda()
+    q = torch.zeros(1, 1, 64, 96, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(fa.FaError) as e:
+        fa.forward(q, q, q)
+    assert e.value.status == fa.FA_ERR_UNSUPPORTED
+    q = torch.zeros(1, 1, 64, 64, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(fa.FaError) as e:
+        fa.forward(q, q, q, scale=float("nan"))
+    assert e.value.status == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_poll_status() == fa.FA_OK
+
+
+def test_timing_counts_launches(fa):
+    torch = torch_cuda()
+    case = inputs.make_case(1, 2, 1024, 128, True, seed=3, with_do=True)
+    q, k, v, do = case_tensors(case)
+    fa.fa_timing_enable(True)
+    o, lse = fa.forward(q, k, v, causal=True, num_splits=1)
+    fa.backward(q, k, v, o, lse, do, causal=True)
+    torch.cuda.synchronize()
+    counts = {kid: fa.fa_timing_read(kid) for kid in range(5)}
+    fa.fa_timing_enable(False)
+    assert counts[fa.FA_KERNEL_FWD][0] == 1 and counts[fa.FA_KERNEL_FWD][1] > 0
+    assert counts[fa.FA_KERNEL_COMBINE][0] == 0
+    assert counts[fa.FA_KERNEL_BWD][0] == 1 and counts[fa.FA_KERNEL_BWD_PRE][0] == 1
+    assert counts[fa.FA_KERNEL_DQ_CONVERT][0] == 1
