@@ -16,7 +16,8 @@
 //
 // Online softmax (section 6.1): the running max m and sum l live in registers
 // of the row's thread, O~ stays unnormalised in TMEM and is divided by l
-// once at the end; L = m + log l is written for the backward pass.  The
+// once at the end; L = m + log l is written for the backward pass.  P is
+// rounded to bf16 for the PV MMA and l sums those rounded weights.  The
 // exp(m_old - m_new) correction of O~ is applied only when a row's max grows
 // by more than 2^8 over the reference the row's O~ and l are kept at;
 // otherwise the old reference stays.  O~ and l always share one reference,
@@ -356,8 +357,11 @@ __global__ void __launch_bounds__(320, 1)
           for (int e = 0; e < 32; e += 2) {
             const float p0 = ex2_approx(fmaf(x[32 * h + e], sl2, neg));
             const float p1 = ex2_approx(fmaf(x[32 * h + e + 1], sl2, neg));
-            ls[(e >> 1) & 3] += p0 + p1;
-            pk[e / 2] = pack_bf16(p0, p1);
+            const uint32_t pp = pack_bf16(p0, p1);
+            // l sums the bf16-rounded weights the PV MMA uses, so O~/l is an
+            // exact weighted mean of those weights.
+            ls[(e >> 1) & 3] += __uint_as_float(pp << 16) + __uint_as_float(pp & 0xffff0000u);
+            pk[e / 2] = pp;
           }
           tmem_st16(tS + 16 * h, pk);
         }
