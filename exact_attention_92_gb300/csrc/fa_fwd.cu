@@ -17,7 +17,8 @@
 // Online softmax (section 6.1): the running max m and sum l live in registers
 // of the row's thread, O~ stays unnormalised in TMEM and is divided by l
 // once at the end; L = m + log l is written for the backward pass.  P is
-// rounded to bf16 for the PV MMA and l sums those rounded weights.  The
+// rounded to bf16 for the PV MMA; O~ is divided by the sum of those rounded
+// weights (so O is their exact weighted mean) while L uses the fp32 sum.  The
 // exp(m_old - m_new) correction of O~ is applied only when a row's max grows
 // by more than 2^8 over the reference the row's O~ and l are kept at;
 // otherwise the old reference stays.  O~ and l always share one reference,
@@ -305,7 +306,8 @@ __global__ void __launch_bounds__(320, 1)
         continue;
       }
       float m_ref = -INFINITY;  // reference max of this row, log2 units
-      float l = 0.f;
+      float l = 0.f;     // sum of the fp32 weights: L = m + log l
+      float l_bf = 0.f;  // sum of the bf16-rounded weights the PV MMA uses
       for (int j = 0; j < w.n[t]; ++j) {
         ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t], sc & 1, ctl, kWaitSFull));
         ++sc;
@@ -343,13 +345,14 @@ __global__ void __launch_bounds__(320, 1)
           const float m_new = fmaxf(m_ref, m_tile);
           f = ex2_approx(m_ref - m_new);
           l *= f;
+          l_bf *= f;
           m_ref = m_new;
           rescale = true;
         }
         // P = exp2(S * scale * log2(e) - m_ref), 32 columns at a time, packed
         // to bf16 over the already-read S columns.
         const float neg = -m_ref;
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        float ls[2] = {0.f, 0.f}, lr[2] = {0.f, 0.f};
 #pragma unroll
         for (int h = 0; h < kTileN / 32; ++h) {
           uint32_t pk[16];
@@ -358,14 +361,14 @@ __global__ void __launch_bounds__(320, 1)
             const float p0 = ex2_approx(fmaf(x[32 * h + e], sl2, neg));
             const float p1 = ex2_approx(fmaf(x[32 * h + e + 1], sl2, neg));
             const uint32_t pp = pack_bf16(p0, p1);
-            // l sums the bf16-rounded weights the PV MMA uses, so O~/l is an
-            // exact weighted mean of those weights.
-            ls[(e >> 1) & 3] += __uint_as_float(pp << 16) + __uint_as_float(pp & 0xffff0000u);
+            ls[(e >> 1) & 1] += p0 + p1;
+            lr[(e >> 1) & 1] += __uint_as_float(pp << 16) + __uint_as_float(pp & 0xffff0000u);
             pk[e / 2] = pp;
           }
           tmem_st16(tS + 16 * h, pk);
         }
-        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        l += ls[0] + ls[1];
+        l_bf += lr[0] + lr[1];
         if (rescale) {
           // O~ <- exp2(m_old - m_new) O~; the previous PV MMA has completed
           // (it was issued before this S tile's MMA) and the next one waits
@@ -389,7 +392,9 @@ __global__ void __launch_bounds__(320, 1)
       ++oc;
       if (!ok) break;
       tc_fence_after();
-      const float inv_l = 1.0f / l;
+      // O~ / l_bf is an exact weighted mean of the rounded weights; the
+      // logsumexp takes the unrounded sum.
+      const float inv_l = 1.0f / l_bf;
       const float lse = (m_ref + lg2_approx(l)) * 0.69314718055994530942f;
       if (p.num_splits == 1) {
         const size_t grow = (size_t)w.bh * p.N + row;

@@ -26,10 +26,24 @@ def run_fwd(fa, case, num_splits=0):
     return host(o), lse.cpu().numpy().astype(np.float64)
 
 
+def weights_of(case, rows=None):
+    """Oracle softmax weights and values of one output row (for the derived
+    O bound of elements above the flat bound)."""
+    q, k, v = case.f64("q"), case.f64("k"), case.f64("v")
+
+    def fn(ix):
+        b, h, r = ix
+        row = int(rows[b, h, r]) if rows is not None else int(r)
+        P = att.probabilities_head(q[b, h], k[b, h], case.scale, case.causal, rows=np.array([row]))[0]
+        return P, v[b, h]
+
+    return fn
+
+
 def check_full(fa, case, num_splits=0, what=""):
     o, lse = run_fwd(fa, case, num_splits)
     O, L = att.forward(case.f64("q"), case.f64("k"), case.f64("v"), case.scale, case.causal)
-    check_o(o, O, what)
+    check_o(o, O, what, weights_of(case))
     check_lse(lse, L, what)
     return o, lse, O, L
 
@@ -40,7 +54,7 @@ def check_sampled(fa, case, num_splits=0, what=""):
     O, L = att.forward_rows(case.f64("q"), case.f64("k"), case.f64("v"), case.scale, case.causal, rows)
     og = np.take_along_axis(o, rows[..., None], axis=2)
     lg = np.take_along_axis(lse, rows, axis=2)
-    check_o(og, O, what)
+    check_o(og, O, what, weights_of(case, rows))
     check_lse(lg, L, what)
     assert np.isfinite(o).all() and np.isfinite(lse).all(), what
     return o, lse
