@@ -10,7 +10,9 @@ also allocate the outputs.  PyTorch provides device memory and streams only.
 from ._binding import (  # noqa: F401
     FA_ERR_CUDA,
     FA_ERR_INVALID_ARG,
+    FA_BWD_NOALLOC_SCRATCH_BYTES,
     FA_ERR_NO_MEMORY,
+    FA_ERR_SCRATCH_TOO_SMALL,
     FA_ERR_TIMEOUT,
     FA_ERR_UNSUPPORTED,
     FA_OK,
@@ -19,6 +21,7 @@ from ._binding import (  # noqa: F401
     declared_symbols,
     fa_abi_version,
     fa_bwd,
+    fa_bwd_noalloc,
     fa_fwd,
     fa_fwd_ex,
     fa_poll_status,

@@ -25,6 +25,8 @@ FA_ERR_UNSUPPORTED = 2
 FA_ERR_CUDA = 3
 FA_ERR_NO_MEMORY = 4
 FA_ERR_TIMEOUT = 5
+FA_ERR_SCRATCH_TOO_SMALL = 6
+FA_BWD_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
 class FaError(RuntimeError):
@@ -46,6 +48,7 @@ _SIGNATURES = {
     "fa_fwd": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp], _i),
     "fa_fwd_ex": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp], _i),
     "fa_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp], _i),
+    "fa_bwd_noalloc": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp], _i),
     "fa_poll_status": ([_vp], _i),
     "fa_set_wait_timeout_ns": ([_u64], _u64),
     "fa_selftest_wait_timeout": ([_u64, _vp], _i),
@@ -159,6 +162,21 @@ def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, causal=False, scale=None, stream=N
     st = lib.fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
                     B, H, N, d, 1 if causal else 0, _scale(scale, d), _stream_ptr(stream, q.device))
     _check(st, "fa_bwd")
+
+
+def fa_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, causal=False, scale=None, stream=None):
+    """C fa_bwd_noalloc: fa_bwd with its workspace in the library's static
+    device scratch (no device allocation; see include/fa.h)."""
+    _check_bhnd("q", q)
+    B, H, N, d = q.shape
+    for name, t in (("k", k), ("v", v), ("o", o), ("dout", dout), ("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_bhnd(name, t, q.shape)
+    _check_lse(lse, (B, H, N))
+    lib = load()
+    st = lib.fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+                            _ptr(dv), B, H, N, d, 1 if causal else 0, _scale(scale, d),
+                            _stream_ptr(stream, q.device))
+    _check(st, "fa_bwd_noalloc")
 
 
 def fa_poll_status(stream=None):

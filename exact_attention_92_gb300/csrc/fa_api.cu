@@ -187,6 +187,23 @@ cudaError_t timed(int kernel, cudaStream_t stream, F&& launch) {
 
 }  // namespace
 
+namespace fa {
+// Accessors for entry points defined in other files of the library.
+int internal_device_setup(unsigned int** status, int* sm_count) {
+  DeviceState* s = nullptr;
+  const int e = device_state(&s);
+  if (e) return e;
+  *status = s->status;
+  *sm_count = s->sm_count;
+  return FA_OK;
+}
+int internal_validate(int B, int H, int N, int d, float scale) { return validate(B, H, N, d, scale); }
+int internal_encode_bhnd(CUtensorMap* m, const void* ptr, int BH, int N, int d) {
+  return encode_bhnd(m, ptr, BH, N, d);
+}
+unsigned long long internal_wait_timeout_ns() { return g_timeout_ns.load(); }
+}  // namespace fa
+
 extern "C" {
 
 int fa_timing_enable(int on) {
@@ -236,6 +253,8 @@ const char* fa_strerror(int status) {
     case FA_ERR_CUDA: return "FA_ERR_CUDA: CUDA runtime or launch failure";
     case FA_ERR_NO_MEMORY: return "FA_ERR_NO_MEMORY: workspace allocation failed";
     case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a device-side wait gave up";
+    case FA_ERR_SCRATCH_TOO_SMALL:
+      return "FA_ERR_SCRATCH_TOO_SMALL: problem needs more than the static scratch of fa_bwd_noalloc";
     default: return "unknown fa_status";
   }
 }

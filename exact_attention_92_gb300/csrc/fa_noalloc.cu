@@ -1,0 +1,122 @@
+// fa_bwd_noalloc: the backward pass with its workspace in a static device
+// array instead of cudaMallocAsync (see include/fa.h for who needs this).
+//
+// The array below is the only scratch this entry point uses.  Host code may
+// not use its name as an address (that is a host-side stand-in): set-up, once
+// per device with that device current, asks the runtime for its device
+// address and the launches take that pointer.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "fa_common.h"
+
+static __device__ __align__(256) unsigned char g_fa_bwd_scratch[FA_BWD_NOALLOC_SCRATCH_BYTES];
+
+namespace fa {
+int internal_device_setup(unsigned int** status, int* sm_count);
+int internal_validate(int B, int H, int N, int d, float scale);
+int internal_encode_bhnd(CUtensorMap* m, const void* ptr, int BH, int N, int d);
+unsigned long long internal_wait_timeout_ns();
+cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& tdo, const BwdParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_bwd_preprocess(int d, const void* o, const void* dout, float* dvec, float* dq_acc, int rows,
+                                  cudaStream_t stream);
+cudaError_t launch_dq_convert(int d, const float* dq_acc, void* dq, size_t elems, float scale, cudaStream_t stream);
+}  // namespace fa
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct ScratchState {
+  std::once_flag once;
+  int err = 0;
+  unsigned char* ptr = nullptr;  // device address of g_fa_bwd_scratch
+};
+ScratchState g_scratch[kMaxDevices];
+
+// Device address of the scratch array on the current device (set up once).
+int scratch_address(unsigned char** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+  ScratchState& s = g_scratch[dev];
+  std::call_once(s.once, [&s]() {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_fa_bwd_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      s.err = FA_ERR_CUDA;
+      return;
+    }
+    s.ptr = static_cast<unsigned char*>(p);
+  });
+  if (s.err) return s.err;
+  *out = s.ptr;
+  return FA_OK;
+}
+
+bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                              const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                              int causal, float scale, void* stream) {
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_INVALID_ARG;
+  int e = fa::internal_validate(B, H, N, d, scale);
+  if (e) return e;
+  const size_t rows = (size_t)B * H * N;
+  const size_t need = rows * ((size_t)d + 1) * sizeof(float);
+  if (need > (size_t)FA_BWD_NOALLOC_SCRATCH_BYTES) return FA_ERR_SCRATCH_TOO_SMALL;
+  unsigned int* status = nullptr;
+  int sm_count = 0;
+  e = fa::internal_device_setup(&status, &sm_count);
+  if (e) return e;
+  unsigned char* scratch = nullptr;
+  e = scratch_address(&scratch);
+  if (e) return e;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int BH = B * H;
+
+  CUtensorMap tq, tk, tv, tdo;
+  if (fa::internal_encode_bhnd(&tq, q, BH, N, d) || fa::internal_encode_bhnd(&tk, k, BH, N, d) ||
+      fa::internal_encode_bhnd(&tv, v, BH, N, d) || fa::internal_encode_bhnd(&tdo, dout, BH, N, d))
+    return FA_ERR_CUDA;
+
+  // Scratch layout: dQ accumulator [rows, d] fp32, then D [rows] fp32.  The
+  // preprocess kernel zeroes the accumulator rows and writes every D.
+  float* dq_acc = reinterpret_cast<float*>(scratch);
+  float* dvec = dq_acc + rows * d;
+
+  fa::BwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.B = B;
+  p.H = H;
+  p.N = N;
+  p.causal = causal ? 1 : 0;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.lse = lse;
+  p.dvec = dvec;
+  p.dq_acc = dq_acc;
+  p.dk = dk;
+  p.dv = dv;
+  p.num_kv_tiles = (N + 127) / 128;
+  p.num_units = BH * p.num_kv_tiles;
+  p.status = status;
+  p.timeout_ns = fa::internal_wait_timeout_ns();
+
+  cudaError_t ce = fa::launch_bwd_preprocess(d, o, dout, dvec, dq_acc, (int)rows, st);
+  if (ce == cudaSuccess) {
+    const int grid = p.num_units < sm_count ? p.num_units : sm_count;
+    ce = fa::launch_bwd(d, tq, tk, tv, tdo, p, grid, st);
+  }
+  if (ce == cudaSuccess) ce = fa::launch_dq_convert(d, dq_acc, dq, rows * d, scale, st);
+  return ce == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}

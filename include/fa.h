@@ -48,7 +48,8 @@ typedef enum {
   FA_ERR_UNSUPPORTED = 2, /* head dim not 64/128, or device is not sm_103    */
   FA_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed     */
   FA_ERR_NO_MEMORY = 4,   /* workspace allocation failed                     */
-  FA_ERR_TIMEOUT = 5      /* a device-side wait gave up (fa_poll_status)     */
+  FA_ERR_TIMEOUT = 5,     /* a device-side wait gave up (fa_poll_status)     */
+  FA_ERR_SCRATCH_TOO_SMALL = 6 /* fa_bwd_noalloc: problem exceeds its scratch */
 } fa_status;
 
 /*
@@ -91,6 +92,40 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
  */
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
            void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale, void* stream);
+
+/*
+ * Backward pass that allocates no device memory.  The paper has no
+ * counterpart: this is a library convenience.
+ *
+ * fa_bwd takes its fp32 workspace (the dQ accumulator and D, B*H*N*(d+1)*4
+ * bytes) from cudaMallocAsync on every call.  Some callers cannot allow
+ * that: a caller capturing a CUDA graph that must contain no memory-
+ * allocation nodes, and a caller that has handed nearly all device memory
+ * to its own pool up front (weights, KV caches) and cannot have a library
+ * take tens of megabytes in the middle of a step.  fa_bwd_noalloc runs the
+ * same three kernels as fa_bwd, with the workspace in one static device
+ * array of FA_BWD_NOALLOC_SCRATCH_BYTES, which every device that sets this
+ * entry point up keeps until the process exits.
+ *
+ *  - Arguments, layouts and ownership as fa_bwd; the caller still passes
+ *    (and owns) every input and output.
+ *  - Returns FA_ERR_SCRATCH_TOO_SMALL, before any device work, when
+ *    B*H*N*(d+1)*4 exceeds FA_BWD_NOALLOC_SCRATCH_BYTES.
+ *  - The first call on a device sets up that device (with it current): it
+ *    looks up the array's device address, and the library's status word,
+ *    once.  Make that first call before any stream capture.
+ *  - It calls no cudaMalloc/cudaMallocAsync/cudaFree and no allocating
+ *    routine of any other library.
+ *  - All calls on a device share the one array, and it keeps the last
+ *    call's contents; each call clears the part that must start at zero
+ *    (the dQ accumulator) itself.  Two calls whose kernels overlap on the GPU
+ *    (different streams, or different host threads) race on the array and
+ *    give wrong gradients: serialise them.
+ */
+#define FA_BWD_NOALLOC_SCRATCH_BYTES (64u << 20)
+int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                   const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal,
+                   float scale, void* stream);
 
 /*
  * Synchronise `stream`, then return and clear the device status word of the
