@@ -55,18 +55,28 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash():
+KERNEL_SOURCES = {
+    "fa_fwd_kernel": ["fa_fwd.cu", "sm103_primitives.cuh", "fa_common.h"],
+    "fa_combine_kernel": ["fa_fwd.cu", "sm103_primitives.cuh", "fa_common.h"],
+    "fa_bwd_kernel": ["fa_bwd.cu", "sm103_primitives.cuh", "fa_common.h"],
+    "fa_bwd_preprocess": ["fa_bwd.cu", "sm103_primitives.cuh", "fa_common.h"],
+    "fa_dq_convert": ["fa_bwd.cu", "sm103_primitives.cuh", "fa_common.h"],
+}
+
+
+def kernel_source_hash(kernel):
+    """Hash of the source files a kernel is compiled from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_attention_92_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(csrc, name), "rb") as fh:
             h.update(name.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(kernel):
-    """DRAM bytes per launch of ``kernel`` from the committed ncu summary, if
-    it was taken on the current kernel sources (else None)."""
+    """DRAM bytes per launch of ``kernel`` from the committed ncu summary,
+    if it was taken on the kernel's current sources (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as fh:
@@ -74,7 +84,7 @@ def recorded_traffic(kernel):
     except (OSError, ValueError):
         return None
     ent = rec.get(kernel)
-    if not ent or ent.get("source_hash") != kernel_source_hash():
+    if not ent or ent.get("source_hash") != kernel_source_hash(kernel):
         return None
     return ent.get("dram_bytes_per_launch")
 
