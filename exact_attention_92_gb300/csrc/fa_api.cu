@@ -16,7 +16,7 @@
 
 namespace fa {
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const FwdParams& p, int grid, cudaStream_t stream);
+                       const CUtensorMap& to, const FwdParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_combine(int d, const CombineParams& p, cudaStream_t stream);
 cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tdo, const BwdParams& p, int grid, cudaStream_t stream);
@@ -301,8 +301,9 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
   const int per_split = (nkv + S - 1) / S;
   S = (nkv + per_split - 1) / per_split;  // no empty split
 
-  CUtensorMap tq, tk, tv;
-  if (encode_bhnd(&tq, q, BH, N, d) || encode_bhnd(&tk, k, BH, N, d) || encode_bhnd(&tv, v, BH, N, d))
+  CUtensorMap tq, tk, tv, to;
+  if (encode_bhnd(&tq, q, BH, N, d) || encode_bhnd(&tk, k, BH, N, d) || encode_bhnd(&tv, v, BH, N, d) ||
+      encode_bhnd(&to, o, BH, N, d))
     return FA_ERR_CUDA;
 
   FwdParams p;
@@ -333,7 +334,7 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
     p.lse_part = p.o_part + (size_t)S * rows * d;
   }
   const int grid = p.num_units < s->sm_count ? p.num_units : s->sm_count;
-  cudaError_t ce = timed(FA_KERNEL_FWD, st, [&] { return fa::launch_fwd(d, tq, tk, tv, p, grid, st); });
+  cudaError_t ce = timed(FA_KERNEL_FWD, st, [&] { return fa::launch_fwd(d, tq, tk, tv, to, p, grid, st); });
   if (ce == cudaSuccess && S > 1) {
     fa::CombineParams c;
     c.rows = (int)rows;

@@ -8,22 +8,36 @@
 //                      persistent CTA owns one 128-key tile K_j, V_j of one
 //                      (batch, head) and walks the query tiles i that can see
 //                      it.  dK_j and dV_j accumulate in tensor memory of that
-//                      CTA alone (no atomics); the partial dQ_i of every step
-//                      is added to the fp32 accumulator with atomics.
+//                      CTA alone (no atomics); the partial dQ of every step is
+//                      added to the fp32 accumulator with atomics.
 //   fa_dq_convert      dQ = scale * accumulator, to bf16.
 //
-// Per step (query tile i), in the transposed orientation so that TMEM lanes
-// are keys:
+// Per step (query tile i of 128 rows), in the transposed orientation so that
+// TMEM lanes are keys:
 //   S^T  = K_j Q_i^T,   P^T = exp(scale S^T - L_i)   (P recovered from the
 //                       saved logsumexp, section 7.1)
 //   dP^T = V_j dO_i^T,  dS^T = P^T * (dP^T - D_i)
-//   dV_j += P^T dO_i,   dK_j += dS^T Q_i,   dQ_i += dS K_j
-// with the softmax scale applied once to dK at the end and to dQ in the
+//   dV_j += P^T dO_i,   dK_j += dS^T Q_i
+//   d = 128: dQ_i^T = K_j^T dS^T (TMEM lanes are head-dim columns, so one
+//            warp's atomic add covers 32 consecutive floats of one dQ row)
+//   d = 64:  dQ_i = dS K_j
+// The softmax scale is applied once to dK at the end and to dQ in the
 // convert kernel.
 //
-// Roles: warp 9 loads (TMA), warp 8 issues tcgen05 MMAs, warps 0-3 compute
-// P^T and dS^T (one key row per thread) and write dK/dV at the end of a unit,
-// warps 4-7 read dQ_i out of TMEM and add it to the accumulator.
+// Roles (320 threads): warp 9 loads (TMA for K, V, Q, dO; plain loads for
+// L_i and D_i into shared memory), warp 8 issues tcgen05 MMAs, warps 0-7
+// compute P^T and dS^T (a key row per lane, warps w and w+4 split the 128
+// query columns), then read their half of dQ out of TMEM, release it and
+// add it to the accumulator while the next step's S^T / dP^T run, and write
+// dK/dV at the end of a unit.
+//
+// TMEM (512 columns).  A = [0,128): S^T; P^T (bf16, two per column) goes to
+// A[0,32) for queries 0-63 and A[96,128) for queries 64-127, each written
+// over S^T columns its own warp has already read.  B = [128,256): dP^T, then
+// dS^T in B[0,32) and B[96,128).  dV and dK follow.  At d = 128 the dQ^T
+// halves take the free middle columns A[32,96) and B[32,96), so the next
+// step's S^T / dP^T wait for them to be read out; at d = 64 dQ has its own
+// 64 columns.
 #include <cuda_runtime.h>
 
 #include "sm103_primitives.cuh"
@@ -39,16 +53,12 @@ struct BwdCfg {
   static constexpr int kTileBytes = kTileM * D * 2;
   static constexpr int kStages = 2;
   static constexpr int kThreads = 320;
-  // TMEM columns.  A: S^T then P^T (bf16 in its first 64 columns).
-  // B: dP^T then dS^T.  At d = 128 the dQ tile takes the upper halves of A
-  // and B (free once P^T and dS^T are written); at d = 64 it has its own.
   static constexpr uint32_t kColA = 0;
   static constexpr uint32_t kColB = 128;
   static constexpr uint32_t kColDV = 256;
   static constexpr uint32_t kColDK = 256 + D;
-  static constexpr bool kDqAliased = (D == 128);
-  static constexpr uint32_t kColDQ0 = kDqAliased ? 64u : 384u;
-  static constexpr uint32_t kColDQ1 = kDqAliased ? 192u : 384u;
+  static constexpr bool kDqT = (D == 128);
+  static constexpr uint32_t kColDQ = kDqT ? 32u : 384u;  // d = 128: A+32 and B+32
   static constexpr uint32_t kTmemCols = 512;
   // Shared memory.
   static constexpr int kOffK = 0;
@@ -57,12 +67,15 @@ struct BwdCfg {
   static constexpr int kOffDO = kOffQ + kStages * kTileBytes;
   static constexpr int kOffDS = kOffDO + kStages * kTileBytes;
   static constexpr int kDsBytes = kTileM * kTileN * 2;
-  static constexpr int kOffLse = kOffDS + kDsBytes;      // 2 x 128 floats
-  static constexpr int kOffDvec = kOffLse + 2 * 128 * 4;  // 2 x 128 floats
-  static constexpr int kOffBar = kOffDvec + 2 * 128 * 4;
-  static constexpr int kNumBars = 2 + 2 * kStages + 1 + 1 + 2 + 2 + 1 + 2;
+  static constexpr int kOffLse = kOffDS + kDsBytes;             // kStages x 128 floats (log2 units)
+  static constexpr int kOffDvec = kOffLse + kStages * 128 * 4;  // kStages x 128 floats
+  static constexpr int kOffBar = kOffDvec + kStages * 128 * 4;
+  static constexpr int kNumBars = 2 + 3 * kStages + 1 + 1 + 1 + 2 + 2 + 1;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16;
 };
+
+// Packed-P^T / dS^T column of the 16 queries [16 kk, 16 kk + 16) in A or B.
+__device__ __forceinline__ uint32_t packed_col(int kk) { return kk < 4 ? 8u * kk : 96u + 8u * (kk - 4); }
 
 struct BwdUnit {
   int bh;
@@ -88,8 +101,6 @@ __global__ void __launch_bounds__(320, 1)
                   const BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
-  // The 128-byte swizzle anchors at 1024-byte boundaries: refuse to run (and
-  // report) if the dynamic shared memory base is not aligned.
   if ((smem_u32(smem) & 1023u) != 0u) {
     if (threadIdx.x == 0) atomicCAS(p.status, 0u, (unsigned int)FA_ERR_CUDA);
     return;
@@ -99,15 +110,15 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* kv_empty = bars + 1;
   uint64_t* qdo_full = bars + 2;
   uint64_t* qdo_empty = qdo_full + C::kStages;
-  uint64_t* s_full = qdo_empty + C::kStages;
+  uint64_t* stat_full = qdo_empty + C::kStages;  // L_i, D_i of a stage written
+  uint64_t* s_full = stat_full + C::kStages;
   uint64_t* p_ready = s_full + 1;
   uint64_t* dq_full = p_ready + 1;
-  uint64_t* dq_empty = dq_full + 1;
-  uint64_t* dkv_full = dq_empty + 1;
+  uint64_t* dq_empty = dq_full + 1;  // [2]: the two dQ^T halves read out (d = 64: [0] only)
+  uint64_t* dkv_full = dq_empty + 2;
   uint64_t* dkv_empty = dkv_full + 1;
   uint64_t* drain = dkv_empty + 1;
-  uint64_t* stat_ready = drain + 1;  // [2]: L_i / D_i of a step staged in smem
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stat_ready + 2);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   float* sLse = reinterpret_cast<float*>(smem + C::kOffLse);
   float* sDv = reinterpret_cast<float*>(smem + C::kOffDvec);
 
@@ -120,16 +131,18 @@ __global__ void __launch_bounds__(320, 1)
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&qdo_full[s], 1);
       mbar_init(&qdo_empty[s], 1);
+      mbar_init(&stat_full[s], 32);
     }
     mbar_init(s_full, 1);
-    mbar_init(p_ready, 128);
+    mbar_init(p_ready, 256);
     mbar_init(dq_full, 1);
-    mbar_init(dq_empty, 128);
+    // d = 128: one barrier per dQ^T half (the 4 warps reading it); d = 64:
+    // all 8 warps release the one dQ tile.
+    mbar_init(&dq_empty[0], C::kDqT ? 128 : 256);
+    mbar_init(&dq_empty[1], 128);
     mbar_init(dkv_full, 1);
-    mbar_init(dkv_empty, 128);
+    mbar_init(dkv_empty, 256);
     mbar_init(drain, 1);
-    mbar_init(&stat_ready[0], 128);
-    mbar_init(&stat_ready[1], 128);
     fence_barrier_init();
   }
   if (warp == 8) {
@@ -150,34 +163,54 @@ __global__ void __launch_bounds__(320, 1)
 
   if (warp == 9) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      uint32_t kc = 0, qc = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-        const BwdUnit w = decode_bwd(p, u);
-        ok = mbar_wait(kv_empty, (kc & 1) ^ 1, ctl, kWaitBwdLoad);
-        if (!ok) break;
+    uint32_t kc = 0, qc = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+      const BwdUnit w = decode_bwd(p, u);
+      const size_t head = (size_t)w.bh * p.N;
+      ok = __all_sync(0xffffffffu, mbar_wait(kv_empty, (kc & 1) ^ 1, ctl, kWaitBwdLoad));
+      if (!ok) break;
+      if (lane == 0) {
         mbar_arrive_expect_tx(kv_full, 2 * C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c) {
           tma_load_3d(smem + C::kOffK + c * C::kChunkBytes, &tm_k, kv_full, c * 64, w.j * kTileN, w.bh);
           tma_load_3d(smem + C::kOffV + c * C::kChunkBytes, &tm_v, kv_full, c * 64, w.j * kTileN, w.bh);
         }
-        ++kc;
-        for (int ii = 0; ok && ii < w.nq; ++ii) {
-          const uint32_t st = qc % C::kStages;
-          ok = mbar_wait(&qdo_empty[st], ((qc / C::kStages) & 1) ^ 1, ctl, kWaitBwdLoad);
-          if (!ok) break;
+      }
+      ++kc;
+      for (int ii = 0; ok && ii < w.nq; ++ii) {
+        const uint32_t st = qc % C::kStages;
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(&qdo_empty[st], ((qc / C::kStages) & 1) ^ 1, ctl, kWaitBwdLoad));
+        if (!ok) break;
+        const int row = (w.i0 + ii) * kTileM;
+        if (lane == 0) {
           mbar_arrive_expect_tx(&qdo_full[st], 2 * C::kTileBytes);
-          const int row = (w.i0 + ii) * kTileM;
           for (int c = 0; c < C::kChunks; ++c) {
             tma_load_3d(smem + C::kOffQ + st * C::kTileBytes + c * C::kChunkBytes, &tm_q, &qdo_full[st], c * 64,
                         row, w.bh);
             tma_load_3d(smem + C::kOffDO + st * C::kTileBytes + c * C::kChunkBytes, &tm_do, &qdo_full[st],
                         c * 64, row, w.bh);
           }
-          ++qc;
         }
+        // L_i (log2 units) and D_i of the tile's 128 queries; rows past N get
+        // L = +inf so their weights vanish.
+        float4 l4, d4;
+        float* lp = &l4.x;
+        float* dp = &d4.x;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int qr = row + 4 * lane + e;
+          lp[e] = qr < p.N ? p.lse[head + qr] * 1.4426950408889634f : INFINITY;
+          dp[e] = qr < p.N ? p.dvec[head + qr] : 0.f;
+        }
+        reinterpret_cast<float4*>(sLse + st * 128)[lane] = l4;
+        reinterpret_cast<float4*>(sDv + st * 128)[lane] = d4;
+        mbar_arrive(&stat_full[st]);
+        ++qc;
       }
+    }
+    if (lane == 0) {
       if (kc > 0) mbar_wait(kv_full, (kc - 1) & 1, ctl, kWaitDrain);
       const uint32_t first = qc > (uint32_t)C::kStages ? qc - C::kStages : 0u;
       for (uint32_t pos = first; pos < qc; ++pos)
@@ -187,9 +220,9 @@ __global__ void __launch_bounds__(320, 1)
   } else if (warp == 8) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t id_s = idesc_bf16(kTileM, kTileM, false, false);   // S^T, dP^T
-      constexpr uint32_t id_kv = idesc_bf16(kTileM, D, false, true);        // dV, dK
-      constexpr uint32_t id_dq = idesc_bf16(kTileM, 64, true, true);        // dQ (per 64 columns)
+      constexpr uint32_t id_s = idesc_bf16(kTileM, kTileM, false, false);  // S^T, dP^T
+      constexpr uint32_t id_kv = idesc_bf16(kTileM, D, false, true);       // dV, dK
+      constexpr uint32_t id_dq = idesc_bf16(kTileM, 64, true, true);       // dQ^T halves / dQ
       const uint32_t sk = smem_u32(smem + C::kOffK);
       const uint32_t sv = smem_u32(smem + C::kOffV);
       const uint32_t sds = smem_u32(smem + C::kOffDS);
@@ -207,9 +240,9 @@ __global__ void __launch_bounds__(320, 1)
           if (!ok) break;
           const uint32_t sq = smem_u32(smem + C::kOffQ + st * C::kTileBytes);
           const uint32_t sdo = smem_u32(smem + C::kOffDO + st * C::kTileBytes);
-          if (C::kDqAliased && dqc > 0) {
-            // S^T and dP^T overwrite the columns the previous dQ tile sits in.
-            ok = mbar_wait(dq_empty, (dqc - 1) & 1, ctl, kWaitBwdMma);
+          if (C::kDqT && dqc > 0) {
+            // S^T overwrites the columns of the previous dQ^T's first half.
+            ok = mbar_wait(&dq_empty[0], (dqc - 1) & 1, ctl, kWaitBwdMma);
             if (!ok) break;
           }
           tc_fence_after();
@@ -218,6 +251,11 @@ __global__ void __launch_bounds__(320, 1)
             const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
             mma_ss(tmem + C::kColA, sdesc_sw128(sk + off, 16, 1024), sdesc_sw128(sq + off, 16, 1024), id_s,
                    kk > 0 ? 1u : 0u);
+          }
+          if (C::kDqT && dqc > 0) {
+            ok = mbar_wait(&dq_empty[1], (dqc - 1) & 1, ctl, kWaitBwdMma);
+            if (!ok) break;
+            tc_fence_after();
           }
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
@@ -234,31 +272,40 @@ __global__ void __launch_bounds__(320, 1)
             ok = mbar_wait(dkv_empty, (uc - 1) & 1, ctl, kWaitBwdMma);
             if (!ok) break;
           }
-          if (!C::kDqAliased && dqc > 0) {
-            ok = mbar_wait(dq_empty, (dqc - 1) & 1, ctl, kWaitBwdMma);
+          if (!C::kDqT && dqc > 0) {
+            ok = mbar_wait(&dq_empty[0], (dqc - 1) & 1, ctl, kWaitBwdMma);
             if (!ok) break;
           }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < kTileM / 16; ++kk) {
             const uint32_t acc = (ii > 0 || kk > 0) ? 1u : 0u;
-            mma_ts(tmem + C::kColDV, tmem + C::kColA + kk * 8, sdesc_sw128(sdo + kk * 2048, C::kChunkBytes, 1024),
-                   id_kv, acc);
+            mma_ts(tmem + C::kColDV, tmem + C::kColA + packed_col(kk),
+                   sdesc_sw128(sdo + kk * 2048, C::kChunkBytes, 1024), id_kv, acc);
           }
 #pragma unroll
           for (int kk = 0; kk < kTileM / 16; ++kk) {
             const uint32_t acc = (ii > 0 || kk > 0) ? 1u : 0u;
-            mma_ts(tmem + C::kColDK, tmem + C::kColB + kk * 8, sdesc_sw128(sq + kk * 2048, C::kChunkBytes, 1024),
-                   id_kv, acc);
+            mma_ts(tmem + C::kColDK, tmem + C::kColB + packed_col(kk),
+                   sdesc_sw128(sq + kk * 2048, C::kChunkBytes, 1024), id_kv, acc);
           }
+          if constexpr (C::kDqT) {
+            // dQ^T[:, 64h : 64h+64] = K^T dS^T[:, 64h : 64h+64]: A = K^T (K
+            // tile read MN-major), B = the 64-query block h of dS^T.
 #pragma unroll
-          for (int kk = 0; kk < kTileN / 16; ++kk) {
-            const uint64_t a = sdesc_sw128(sds + kk * 2048, C::kChunkBytes, 1024);
-            mma_ss(tmem + C::kColDQ0, a, sdesc_sw128(sk + kk * 2048, C::kChunkBytes, 1024), id_dq,
-                   kk > 0 ? 1u : 0u);
-            if (D == 128)
-              mma_ss(tmem + C::kColDQ1, a, sdesc_sw128(sk + C::kChunkBytes + kk * 2048, C::kChunkBytes, 1024),
-                     id_dq, kk > 0 ? 1u : 0u);
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int kk = 0; kk < kTileN / 16; ++kk)
+                mma_ss(tmem + (h ? C::kColB : C::kColA) + C::kColDQ,
+                       sdesc_sw128(sk + kk * 2048, C::kChunkBytes, 1024),
+                       sdesc_sw128(sds + h * C::kChunkBytes + kk * 2048, C::kChunkBytes, 1024), id_dq,
+                       kk > 0 ? 1u : 0u);
+          } else {
+            // dQ = dS K: A = dS (the dS^T tile read MN-major), B = K.
+#pragma unroll
+            for (int kk = 0; kk < kTileN / 16; ++kk)
+              mma_ss(tmem + C::kColDQ, sdesc_sw128(sds + kk * 2048, C::kChunkBytes, 1024),
+                     sdesc_sw128(sk + kk * 2048, C::kChunkBytes, 1024), id_dq, kk > 0 ? 1u : 0u);
           }
           mma_commit(dq_full);
           ++dqc;
@@ -274,43 +321,38 @@ __global__ void __launch_bounds__(320, 1)
       mbar_wait(drain, 0, ctl, kWaitDrain);
     }
     __syncwarp();
-  } else if (warp < 4) {
-    // -------------------------------------------- P^T, dS^T and dK/dV output
-    const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
-    const int r = 32 * warp + lane;  // key row within the tile
+  } else if (warp < 8) {
+    // ------------------------------ P^T, dS^T, dQ read-out and dK/dV output
+    const int g = warp & 3;    // TMEM lane quarter
+    const int hc = warp >> 2;  // query-column half
+    const uint32_t lane_off = (uint32_t)(32 * g) << 16;
+    const int r = 32 * g + lane;  // key row within the tile
     const float sl2 = p.scale_log2;
     uint8_t* sds = smem + C::kOffDS;
-    uint32_t sc = 0, uc = 0, step = 0;
+    uint32_t sc = 0, uc = 0, qc = 0, dc = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
       const BwdUnit w = decode_bwd(p, u);
       const int kr = w.j * kTileN + r;  // key index
       const size_t head = (size_t)w.bh * p.N;
-      for (int ii = 0; ii < w.nq; ++ii, ++step) {
+      for (int ii = 0; ii < w.nq; ++ii, ++qc) {
         const int q0 = (w.i0 + ii) * kTileM;
-        {
-          // L_i (log2 units) and D_i of the tile's 128 queries; rows past N
-          // get L = +inf so their weights vanish.
-          const int qr = q0 + r;
-          float* bl = sLse + (step & 1) * 128;
-          float* bd = sDv + (step & 1) * 128;
-          bl[r] = qr < p.N ? p.lse[head + qr] * 1.4426950408889634f : INFINITY;
-          bd[r] = qr < p.N ? p.dvec[head + qr] : 0.f;
-          // Buffer (step & 1) is reused every other step; all 128 threads
-          // arrive once per step, so its k-th use completes phase k.
-          mbar_arrive(&stat_ready[step & 1]);
-          ok = __all_sync(0xffffffffu, mbar_wait(&stat_ready[step & 1], (step >> 1) & 1, ctl, kWaitBwdSoftmax));
-          if (!ok) break;
-        }
-        const float* bl = sLse + (step & 1) * 128;
-        const float* bd = sDv + (step & 1) * 128;
+        const uint32_t st = qc % C::kStages;
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(&stat_full[st], (qc / C::kStages) & 1, ctl, kWaitBwdSoftmax));
+        if (!ok) break;
         ok = __all_sync(0xffffffffu, mbar_wait(s_full, sc & 1, ctl, kWaitBwdSoftmax));
         ++sc;
         if (!ok) break;
         tc_fence_after();
+        const float* bl = sLse + st * 128;
+        const float* bd = sDv + st * 128;
         const bool mask = (kr >= p.N) || (p.causal && kr > q0);
 #pragma unroll 1
-        for (int c = 0; c < kTileM / 32; ++c) {
+        for (int cc = 0; cc < 2; ++cc) {
+          // Half 0 walks query chunks 0, 1; half 1 walks 3, 2, so each packed
+          // store lands on S^T / dP^T columns this warp has already read.
+          const int c = hc ? 3 - cc : cc;
           uint32_t s[32], dp[32];
           tmem_ld32(tmem + lane_off + C::kColA + 32 * c, s);
           tmem_ld32(tmem + lane_off + C::kColB + 32 * c, dp);
@@ -318,21 +360,28 @@ __global__ void __launch_bounds__(320, 1)
           tmem_ld_wait<32>(dp);
           uint32_t pp[16], dd[16];
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            float pr[2], dr[2];
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const float4 l4 = reinterpret_cast<const float4*>(bl + 32 * c)[e4];
+            const float4 d4 = reinterpret_cast<const float4*>(bd + 32 * c)[e4];
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+            const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+            float pr[4], dr[4];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int col = 32 * c + e + h;
-              float pv = ex2_approx(fmaf(__uint_as_float(s[e + h]), sl2, -bl[col]));
+            for (int e = 0; e < 4; ++e) {
+              const int col = 32 * c + 4 * e4 + e;
+              float pv = ex2_approx(fmaf(__uint_as_float(s[4 * e4 + e]), sl2, -lv[e]));
               if (mask && (kr >= p.N || (p.causal && kr > q0 + col))) pv = 0.f;
-              pr[h] = pv;
-              dr[h] = pv * (__uint_as_float(dp[e + h]) - bd[col]);
+              pr[e] = pv;
+              dr[e] = pv * (__uint_as_float(dp[4 * e4 + e]) - dv[e]);
             }
-            pp[e / 2] = pack_bf16(pr[0], pr[1]);
-            dd[e / 2] = pack_bf16(dr[0], dr[1]);
+            pp[2 * e4] = pack_bf16(pr[0], pr[1]);
+            pp[2 * e4 + 1] = pack_bf16(pr[2], pr[3]);
+            dd[2 * e4] = pack_bf16(dr[0], dr[1]);
+            dd[2 * e4 + 1] = pack_bf16(dr[2], dr[3]);
           }
-          tmem_st16(tmem + lane_off + C::kColA + 16 * c, pp);
-          tmem_st16(tmem + lane_off + C::kColB + 16 * c, dd);
+          const uint32_t dst = c < 2 ? 16u * c : 96u + 16u * (c - 2);
+          tmem_st16(tmem + lane_off + C::kColA + dst, pp);
+          tmem_st16(tmem + lane_off + C::kColB + dst, dd);
           // dS^T row r, query columns [32c, 32c+32): 64 bytes of the
           // 128-byte-swizzled [key row][query] tile the dQ MMA reads.
           uint8_t* rowp = sds + (c / 2) * C::kChunkBytes + r * 128;
@@ -347,9 +396,47 @@ __global__ void __launch_bounds__(320, 1)
         tc_fence_before();
         fence_proxy_async_smem();
         mbar_arrive(p_ready);
+        // dQ of this step: read this warp's share out of TMEM, release it,
+        // then add it to the fp32 accumulator.
+        ok = __all_sync(0xffffffffu, mbar_wait(dq_full, dc & 1, ctl, kWaitBwdDq));
+        ++dc;
+        if (!ok) break;
+        tc_fence_after();
+        if constexpr (C::kDqT) {
+          // Lane = head-dim column dd, 64 query rows of half hc.
+          const int dd = 32 * g + lane;
+          uint32_t v[64];
+          const uint32_t base = tmem + lane_off + (hc ? C::kColB : C::kColA) + C::kColDQ;
+          tmem_ld32(base, v);
+          tmem_ld32(base + 32, v + 32);
+          tmem_ld_wait<64>(v);
+          tc_fence_before();
+          mbar_arrive(&dq_empty[hc]);
+          float* dst = p.dq_acc + (head + q0 + 64 * hc) * D + dd;
+          const int nrow = min(64, p.N - q0 - 64 * hc);
+#pragma unroll
+          for (int qq = 0; qq < 64; ++qq)
+            if (qq < nrow) atomicAdd(dst + (size_t)qq * D, __uint_as_float(v[qq]));
+        } else {
+          // Lane = query row; head-dim columns [32 hc, 32 hc + 32).
+          const int qr = q0 + r;
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_off + C::kColDQ + 32 * hc, v);
+          tmem_ld_wait<32>(v);
+          tc_fence_before();
+          mbar_arrive(&dq_empty[0]);
+          if (qr < p.N) {
+            float4* dst = reinterpret_cast<float4*>(p.dq_acc + (head + qr) * D + 32 * hc);
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              atomicAdd(dst + c, make_float4(__uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
+                                             __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3])));
+          }
+        }
       }
       if (!ok) break;
-      // dK_j = scale * sum dS^T Q and dV_j = sum P^T dO of this unit.
+      // dK_j = scale * sum dS^T Q and dV_j = sum P^T dO of this unit; this
+      // warp writes head-dim columns [D/2 hc, D/2 hc + D/2).
       ok = __all_sync(0xffffffffu, mbar_wait(dkv_full, uc & 1, ctl, kWaitBwdSoftmax));
       ++uc;
       if (!ok) break;
@@ -357,7 +444,7 @@ __global__ void __launch_bounds__(320, 1)
       __nv_bfloat16* dvp = reinterpret_cast<__nv_bfloat16*>(p.dv) + (head + kr) * D;
       __nv_bfloat16* dkp = reinterpret_cast<__nv_bfloat16*>(p.dk) + (head + kr) * D;
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = hc * (D / 64); c < (hc + 1) * (D / 64); ++c) {
         uint32_t a[32], b[32];
         tmem_ld32(tmem + lane_off + C::kColDV + 32 * c, a);
         tmem_ld32(tmem + lane_off + C::kColDK + 32 * c, b);
@@ -382,40 +469,6 @@ __global__ void __launch_bounds__(320, 1)
       }
       tc_fence_before();
       mbar_arrive(dkv_empty);
-    }
-  } else {
-    // ---------------------------------------------- dQ_i out of TMEM, atomics
-    const int wq = warp - 4;
-    const uint32_t lane_off = (uint32_t)(32 * wq) << 16;
-    const int r = 32 * wq + lane;  // query row within the tile
-    uint32_t dc = 0;
-    bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-      const BwdUnit w = decode_bwd(p, u);
-      const size_t head = (size_t)w.bh * p.N;
-      for (int ii = 0; ii < w.nq; ++ii) {
-        ok = __all_sync(0xffffffffu, mbar_wait(dq_full, dc & 1, ctl, kWaitBwdDq));
-        ++dc;
-        if (!ok) break;
-        tc_fence_after();
-        uint32_t g[D];
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          const uint32_t col = (c < 2) ? C::kColDQ0 + 32 * c : C::kColDQ1 + 32 * (c - 2);
-          tmem_ld32(tmem + lane_off + col, g + 32 * c);
-        }
-        tmem_ld_wait<D>(g);
-        tc_fence_before();
-        mbar_arrive(dq_empty);
-        const int qr = (w.i0 + ii) * kTileM + r;
-        if (qr < p.N) {
-          float4* dst = reinterpret_cast<float4*>(p.dq_acc + (head + qr) * D);
-#pragma unroll
-          for (int c = 0; c < D / 4; ++c)
-            atomicAdd(dst + c, make_float4(__uint_as_float(g[4 * c]), __uint_as_float(g[4 * c + 1]),
-                                           __uint_as_float(g[4 * c + 2]), __uint_as_float(g[4 * c + 3])));
-        }
-      }
     }
   }
 

@@ -6,6 +6,8 @@
 // query tiles Q0, Q1 that stay in shared memory (loaded once, section 2.3)
 // and share one stream of 128-key K/V tiles (the inner loop).  Roles:
 //   warp 9     TMA producer: Q tiles, then K_j, V_j into a ring of slots.
+//              A Q buffer is refilled once the softmax warps have stored
+//              that tile's O through it (O is staged there for a TMA store).
 //   warp 8     MMA issuer (one thread): S_t = Q_t K_j^T and O_t += P_t V_j
 //              with tcgen05 into tensor memory (TMEM).
 //   warps 0-3  softmax of query tile 0, warps 4-7 of tile 1: each thread owns
@@ -48,7 +50,7 @@ struct FwdCfg {
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = 2 * kTileBytes;
   static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
-  static constexpr int kNumBars = 2 + 2 + 2 * kStages + 2 + 2 + 2 + 1;
+  static constexpr int kNumBars = 2 + 2 + 2 * kStages + 2 + 2 + 2 + 1 + 2;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16;
   static constexpr float kRescaleThreshold = 8.0f;     // log2 units
 };
@@ -88,33 +90,36 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
   return w;
 }
 
+// S = Q K^T: 16-wide K-steps walk 32 bytes inside a 128-byte swizzle row
+// (four per 64-column block), then the next 64-column block.  Descriptors
+// come as precomputed halves; a K-step only adds to the start address.
 template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint32_t q_addr, uint32_t k_addr) {
+__device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint32_t q_lo, uint32_t k_lo, uint32_t hi) {
   using C = FwdCfg<D>;
   constexpr uint32_t idesc = idesc_bf16(kTileM, kTileN, false, false);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
-    mma_ss(tmem_s, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024), idesc,
-           kk > 0 ? 1u : 0u);
+    const uint32_t off = ((kk / 4) * C::kChunkBytes + (kk % 4) * 32) >> 4;
+    mma_ss_lh(tmem_s, q_lo + off, hi, k_lo + off, hi, idesc, kk > 0 ? 1u : 0u);
   }
 }
 
+// O += P V: P from TMEM (8 columns per 16 keys), V read MN-major, 16 key rows
+// (2048 bytes) per K-step.
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_addr, bool accumulate) {
-  using C = FwdCfg<D>;
+__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_lo, uint32_t hi,
+                                         bool accumulate) {
   constexpr uint32_t idesc = idesc_bf16(kTileM, D, false, true);
 #pragma unroll
-  for (int kk = 0; kk < kTileN / 16; ++kk) {
-    mma_ts(tmem_o, tmem_p + kk * 8, sdesc_sw128(v_addr + kk * 16 * 128, C::kChunkBytes, 1024), idesc,
-           (accumulate || kk > 0) ? 1u : 0u);
-  }
+  for (int kk = 0; kk < kTileN / 16; ++kk)
+    mma_ts_lh(tmem_o, tmem_p + kk * 8, v_lo + ((kk * 2048) >> 4), hi, idesc, (accumulate || kk > 0) ? 1u : 0u);
 }
 
 template <int D>
 __global__ void __launch_bounds__(320, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                  const FwdParams p) {
   using C = FwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   // The 128-byte swizzle anchors at 1024-byte boundaries: refuse to run (and
@@ -134,7 +139,8 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* p_full = s_full + 2;
   uint64_t* o_full = p_full + 2;
   uint64_t* drain = o_full + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* o_staged = drain + 1;  // [2]: a tile's O rows written to its staging buffer
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_staged + 2);
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -146,6 +152,7 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 4 * 32);
       mbar_init(&o_full[i], 1);
+      mbar_init(&o_staged[i], 128);
     }
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&kv_full[i], 1);
@@ -162,6 +169,7 @@ __global__ void __launch_bounds__(320, 1)
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_o);
   }
   tc_fence_before();
   __syncthreads();
@@ -212,8 +220,13 @@ __global__ void __launch_bounds__(320, 1)
   } else if (warp == 8) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t sq = smem_u32(sQ);
-      const uint32_t skv = smem_u32(sKV);
+      // Descriptor low halves: buffer i of a kind is (i * tile bytes) / 16
+      // past the first; V differs from K only in its leading byte offset.
+      constexpr uint32_t hi = sdesc_hi(1024);
+      constexpr uint32_t kTileStep = C::kTileBytes >> 4;
+      const uint32_t q_lo0 = sdesc_lo(smem_u32(sQ), 16);
+      const uint32_t k_lo0 = sdesc_lo(smem_u32(sKV), 16);
+      const uint32_t v_lo0 = sdesc_lo(smem_u32(sKV), C::kChunkBytes);
       uint32_t rc = 0;
       uint32_t qc[2] = {0, 0}, pc[2] = {0, 0};
       bool ok = true;
@@ -234,7 +247,7 @@ __global__ void __launch_bounds__(320, 1)
           tc_fence_after();
           for (int t = 0; t < 2; ++t) {
             if (w.n[t] == 0) continue;
-            issue_qk<D>(tmem + C::col_s(t), sq + t * C::kTileBytes, skv + slot_k * C::kTileBytes);
+            issue_qk<D>(tmem + C::col_s(t), q_lo0 + t * kTileStep, k_lo0 + slot_k * kTileStep, hi);
             mma_commit(&s_full[t]);
           }
           mma_commit(&kv_empty[slot_k]);
@@ -254,7 +267,7 @@ __global__ void __launch_bounds__(320, 1)
             ++pc[t];
             if (!ok) break;
             tc_fence_after();
-            issue_pv<D>(tmem + C::col_o(t), tmem + C::col_s(t), skv + slot_v * C::kTileBytes, j > 0);
+            issue_pv<D>(tmem + C::col_o(t), tmem + C::col_s(t), v_lo0 + slot_v * kTileStep, hi, j > 0);
             if (j + 1 < w.n[t]) {
               if (!k_ready) {
                 ok = mbar_wait(&kv_full[slot_k], (pos_k / C::kStages) & 1, ctl, kWaitKvFull);
@@ -262,11 +275,12 @@ __global__ void __launch_bounds__(320, 1)
                 tc_fence_after();
                 k_ready = true;
               }
-              issue_qk<D>(tmem + C::col_s(t), sq + t * C::kTileBytes, skv + slot_k * C::kTileBytes);
+              issue_qk<D>(tmem + C::col_s(t), q_lo0 + t * kTileStep, k_lo0 + slot_k * kTileStep, hi);
               mma_commit(&s_full[t]);
             } else {
+              // Q_t is released by the softmax warps once O_t, staged in
+              // Q_t's buffer, has been stored.
               mma_commit(&o_full[t]);
-              mma_commit(&q_empty[t]);
             }
           }
           if (!ok) break;
@@ -288,7 +302,7 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t tO = tmem + lane_off + C::col_o(t);
     const int r_in_tile = 32 * (warp & 3) + lane;
     const float sl2 = p.scale_log2;
-    uint32_t sc = 0, oc = 0;
+    uint32_t sc = 0, oc = 0, stc = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
       const Unit w = decode_unit(p, u);
@@ -328,15 +342,15 @@ __global__ void __launch_bounds__(320, 1)
           for (int c = 0; c < kTileN; ++c)
             if (kv0 + c > lim) x[c] = -INFINITY;
         }
-        float mx[4] = {x[0], x[1], x[2], x[3]};
+        float mx0 = x[0], mx1 = x[1], mx2 = x[2], mx3 = x[3];
 #pragma unroll
-        for (int c = 4; c < kTileN; c += 4) {
-          mx[0] = fmaxf(mx[0], x[c]);
-          mx[1] = fmaxf(mx[1], x[c + 1]);
-          mx[2] = fmaxf(mx[2], x[c + 2]);
-          mx[3] = fmaxf(mx[3], x[c + 3]);
+        for (int c = 4; c < kTileN; c += 8) {
+          mx0 = fmax3(mx0, x[c], x[c + 1]);
+          mx1 = fmax3(mx1, x[c + 2], x[c + 3]);
+          mx2 = fmax3(mx2, x[c + 4], x[c + 5]);
+          mx3 = fmax3(mx3, x[c + 6], x[c + 7]);
         }
-        const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
+        const float m_tile = fmax3(fmaxf(mx0, mx1), mx2, mx3) * sl2;
         float f = 1.f;
         bool rescale = false;
         if (j == 0) {
@@ -350,25 +364,34 @@ __global__ void __launch_bounds__(320, 1)
           rescale = true;
         }
         // P = exp2(S * scale * log2(e) - m_ref), 32 columns at a time, packed
-        // to bf16 over the already-read S columns.
-        const float neg = -m_ref;
-        float ls[2] = {0.f, 0.f}, lr[2] = {0.f, 0.f};
+        // to bf16 over the already-read S columns; pairs of columns share the
+        // packed fp32x2 FMA and adds.
+        const float2 sl2v = make_float2(sl2, sl2);
+        const float2 negv = make_float2(-m_ref, -m_ref);
+        float2 ls0 = make_float2(0.f, 0.f), ls1 = ls0, lr0 = ls0, lr1 = ls0;
 #pragma unroll
         for (int h = 0; h < kTileN / 32; ++h) {
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
-            const float p0 = ex2_approx(fmaf(x[32 * h + e], sl2, neg));
-            const float p1 = ex2_approx(fmaf(x[32 * h + e + 1], sl2, neg));
+            const float2 a = __ffma2_rn(make_float2(x[32 * h + e], x[32 * h + e + 1]), sl2v, negv);
+            const float p0 = ex2_approx(a.x);
+            const float p1 = ex2_approx(a.y);
             const uint32_t pp = pack_bf16(p0, p1);
-            ls[(e >> 1) & 1] += p0 + p1;
-            lr[(e >> 1) & 1] += __uint_as_float(pp << 16) + __uint_as_float(pp & 0xffff0000u);
+            const float2 pr = make_float2(__uint_as_float(pp << 16), __uint_as_float(pp & 0xffff0000u));
+            if ((e >> 1) & 1) {
+              ls1 = __fadd2_rn(ls1, make_float2(p0, p1));
+              lr1 = __fadd2_rn(lr1, pr);
+            } else {
+              ls0 = __fadd2_rn(ls0, make_float2(p0, p1));
+              lr0 = __fadd2_rn(lr0, pr);
+            }
             pk[e / 2] = pp;
           }
           tmem_st16(tS + 16 * h, pk);
         }
-        l += ls[0] + ls[1];
-        l_bf += lr[0] + lr[1];
+        l += (ls0.x + ls0.y) + (ls1.x + ls1.y);
+        l_bf += (lr0.x + lr0.y) + (lr1.x + lr1.y);
         if (rescale) {
           // O~ <- exp2(m_old - m_new) O~; the previous PV MMA has completed
           // (it was issued before this S tile's MMA) and the next one waits
@@ -379,7 +402,12 @@ __global__ void __launch_bounds__(320, 1)
             tmem_ld32(tO + 32 * c, o);
             tmem_ld_wait<32>(o);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
+            for (int i = 0; i < 32; i += 2) {
+              const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])),
+                                          make_float2(f, f));
+              o[i] = __float_as_uint(v.x);
+              o[i + 1] = __float_as_uint(v.y);
+            }
             tmem_st32(tO + 32 * c, o);
           }
         }
@@ -397,26 +425,48 @@ __global__ void __launch_bounds__(320, 1)
       const float inv_l = 1.0f / l_bf;
       const float lse = (m_ref + lg2_approx(l)) * 0.69314718055994530942f;
       if (p.num_splits == 1) {
-        const size_t grow = (size_t)w.bh * p.N + row;
-        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + grow * D);
+        // O rows -> Q_t's buffer (no longer read: every S_t MMA finished
+        // before O_t did) in the 128-byte-swizzled layout of the tensor map,
+        // then one TMA store per 64 columns; rows past N are clipped by the
+        // copy.
+        uint8_t* stg = sQ + t * C::kTileBytes;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
           tmem_ld32(tO + 32 * c, o);
           tmem_ld_wait<32>(o);
-          if (row < p.N) {
+          uint8_t* rowp = stg + (c / 2) * C::kChunkBytes + r_in_tile * 128;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              uint4 v;
-              v.x = pack_bf16(__uint_as_float(o[8 * i + 0]) * inv_l, __uint_as_float(o[8 * i + 1]) * inv_l);
-              v.y = pack_bf16(__uint_as_float(o[8 * i + 2]) * inv_l, __uint_as_float(o[8 * i + 3]) * inv_l);
-              v.z = pack_bf16(__uint_as_float(o[8 * i + 4]) * inv_l, __uint_as_float(o[8 * i + 5]) * inv_l);
-              v.w = pack_bf16(__uint_as_float(o[8 * i + 6]) * inv_l, __uint_as_float(o[8 * i + 7]) * inv_l);
-              dst[c * 4 + i] = v;
-            }
+          for (int i = 0; i < 4; ++i) {
+            const float2 il = make_float2(inv_l, inv_l);
+            const float2 a = __fmul2_rn(make_float2(__uint_as_float(o[8 * i + 0]), __uint_as_float(o[8 * i + 1])), il);
+            const float2 b = __fmul2_rn(make_float2(__uint_as_float(o[8 * i + 2]), __uint_as_float(o[8 * i + 3])), il);
+            const float2 e = __fmul2_rn(make_float2(__uint_as_float(o[8 * i + 4]), __uint_as_float(o[8 * i + 5])), il);
+            const float2 g = __fmul2_rn(make_float2(__uint_as_float(o[8 * i + 6]), __uint_as_float(o[8 * i + 7])), il);
+            const int unit = (c % 2) * 4 + i;
+            *reinterpret_cast<uint4*>(rowp + ((unit ^ (r_in_tile & 7)) << 4)) =
+                make_uint4(pack_bf16(a.x, a.y), pack_bf16(b.x, b.y), pack_bf16(e.x, e.y), pack_bf16(g.x, g.y));
           }
         }
-        if (row < p.N) p.lse[grow] = lse;
+        fence_proxy_async_smem();
+        mbar_arrive(&o_staged[t]);
+        if (row < p.N) p.lse[(size_t)w.bh * p.N + row] = lse;
+        if ((warp & 3) == 0) {
+          bool sent = true;
+          if (lane == 0) {
+            sent = mbar_wait(&o_staged[t], stc & 1, ctl, kWaitOFull);
+            if (sent) {
+              for (int c = 0; c < C::kChunks; ++c)
+                tma_store_3d(&tm_o, stg + c * C::kChunkBytes, c * 64, row0, w.bh);
+              bulk_commit();
+              // The buffer takes the next unit's Q_t once the store has read it.
+              bulk_wait_read_all();
+              mbar_arrive(&q_empty[t]);
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, sent, 0);
+        }
+        ++stc;
       } else {
         const size_t prow = ((size_t)split * p.B * p.H + w.bh) * p.N + row;
         float4* dst = reinterpret_cast<float4*>(p.o_part + prow * D);
@@ -434,8 +484,13 @@ __global__ void __launch_bounds__(320, 1)
           }
         }
         if (row < p.N) p.lse_part[prow] = lse;
+        // Q_t's buffer is free: every S_t MMA completed before O_t did.
+        if ((warp & 3) == 0 && lane == 0) mbar_arrive(&q_empty[t]);
       }
     }
+    // Every O store this warpgroup issued has landed before the CTA exits.
+    if ((warp & 3) == 0 && lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -485,17 +540,18 @@ __global__ void __launch_bounds__(256) fa_combine_kernel(const CombineParams p) 
 
 template <int D>
 static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                                const FwdParams& p, int grid, cudaStream_t stream) {
+                                const CUtensorMap& to, const FwdParams& p, int grid, cudaStream_t stream) {
   using C = FwdCfg<D>;
   cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  fa_fwd_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
+  fa_fwd_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, to, p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const FwdParams& p, int grid, cudaStream_t stream) {
-  return d == 64 ? launch_fwd_t<64>(tq, tk, tv, p, grid, stream) : launch_fwd_t<128>(tq, tk, tv, p, grid, stream);
+                       const CUtensorMap& to, const FwdParams& p, int grid, cudaStream_t stream) {
+  return d == 64 ? launch_fwd_t<64>(tq, tk, tv, to, p, grid, stream)
+                 : launch_fwd_t<128>(tq, tk, tv, to, p, grid, stream);
 }
 
 cudaError_t launch_combine(int d, const CombineParams& p, cudaStream_t stream) {
