@@ -18,9 +18,11 @@
 //                       saved logsumexp, section 7.1)
 //   dP^T = V_j dO_i^T,  dS^T = P^T * (dP^T - D_i)
 //   dV_j += P^T dO_i,   dK_j += dS^T Q_i
-//   d = 128: dQ_i^T = K_j^T dS^T (TMEM lanes are head-dim columns, so one
-//            warp's atomic add covers 32 consecutive floats of one dQ row)
-//   d = 64:  dQ_i = dS K_j
+//   d = 128: dQ_i^T = K_j^T dS^T; the softmax warps write it row-major into
+//            the step's Q/dO stage buffer (free once dQ is complete) and the
+//            producer adds each 64-row half (32 contiguous KB of the
+//            accumulator) with one bulk reduce-add, then refills the stage
+//   d = 64:  dQ_i = dS K_j, added with per-thread vector atomics
 // The softmax scale is applied once to dK at the end and to dQ in the
 // convert kernel.
 //
@@ -28,8 +30,8 @@
 // L_i and D_i into shared memory), warp 8 issues tcgen05 MMAs, warps 0-7
 // compute P^T and dS^T (a key row per lane, warps w and w+4 split the 128
 // query columns), then read their half of dQ out of TMEM, release it and
-// add it to the accumulator while the next step's S^T / dP^T run, and write
-// dK/dV at the end of a unit.
+// stage it for the reduction while the next step's S^T / dP^T run, and
+// write dK/dV at the end of a unit.
 //
 // TMEM (512 columns).  A = [0,128): S^T; P^T (bf16, two per column) goes to
 // A[0,32) for queries 0-63 and A[96,128) for queries 64-127, each written
@@ -70,7 +72,7 @@ struct BwdCfg {
   static constexpr int kOffLse = kOffDS + kDsBytes;             // kStages x 128 floats (log2 units)
   static constexpr int kOffDvec = kOffLse + kStages * 128 * 4;  // kStages x 128 floats
   static constexpr int kOffBar = kOffDvec + kStages * 128 * 4;
-  static constexpr int kNumBars = 2 + 3 * kStages + 1 + 1 + 1 + 2 + 2 + 1;
+  static constexpr int kNumBars = 2 + 3 * kStages + 1 + 1 + 1 + 2 + 2 + 1 + 2 * kStages;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16;
 };
 
@@ -118,7 +120,11 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* dkv_full = dq_empty + 2;
   uint64_t* dkv_empty = dkv_full + 1;
   uint64_t* drain = dkv_empty + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  // [stage][half]: a dQ^T half written into that stage's buffer (d = 128).
+  // One pair per stage: a stage is refilled only after its last use was
+  // reduced, so these never run more than one phase ahead of the producer.
+  uint64_t* dq_staged = drain + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dq_staged + 2 * C::kStages);
   float* sLse = reinterpret_cast<float*>(smem + C::kOffLse);
   float* sDv = reinterpret_cast<float*>(smem + C::kOffDvec);
 
@@ -143,6 +149,7 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(dkv_full, 1);
     mbar_init(dkv_empty, 256);
     mbar_init(drain, 1);
+    for (int i = 0; i < 2 * C::kStages; ++i) mbar_init(&dq_staged[i], 128);
     fence_barrier_init();
   }
   if (warp == 8) {
@@ -164,7 +171,33 @@ __global__ void __launch_bounds__(320, 1)
   if (warp == 9) {
     // ------------------------------------------------------------ producer
     uint32_t kc = 0, qc = 0;
+    // Rows (bh * N + q0) and valid row count of the steps in each stage, for
+    // the dQ reduction of d = 128.
+    size_t st_row[C::kStages];
+    int st_nrow[C::kStages];
     bool ok = true;
+    // d = 128: add step `k`'s staged dQ (two 64-row halves in the Q and dO
+    // buffers of stage k % kStages) to the accumulator, and wait until the
+    // copies have read the buffers.
+    auto reduce_step = [&](uint32_t k) -> bool {
+      const uint32_t s = k % C::kStages;
+      const uint32_t par = (k / C::kStages) & 1;
+      bool r = __all_sync(0xffffffffu, mbar_wait(&dq_staged[2 * s], par, ctl, kWaitBwdLoad)) &&
+               __all_sync(0xffffffffu, mbar_wait(&dq_staged[2 * s + 1], par, ctl, kWaitBwdLoad));
+      if (r && lane == 0) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int n = min(64, st_nrow[s] - 64 * h);
+          if (n > 0)
+            bulk_reduce_add_f32(p.dq_acc + (st_row[s] + 64 * h) * D,
+                                smem + (h ? C::kOffDO : C::kOffQ) + s * C::kTileBytes, (uint32_t)n * D * 4);
+        }
+        bulk_commit();
+        bulk_wait_read_all();
+      }
+      __syncwarp();
+      return r;
+    };
     for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
       const BwdUnit w = decode_bwd(p, u);
       const size_t head = (size_t)w.bh * p.N;
@@ -180,10 +213,18 @@ __global__ void __launch_bounds__(320, 1)
       ++kc;
       for (int ii = 0; ok && ii < w.nq; ++ii) {
         const uint32_t st = qc % C::kStages;
-        ok = __all_sync(0xffffffffu,
-                        mbar_wait(&qdo_empty[st], ((qc / C::kStages) & 1) ^ 1, ctl, kWaitBwdLoad));
+        if constexpr (C::kDqT) {
+          // The stage's previous step has finished with Q/dO and its dQ is
+          // staged there: reduce it, then refill.
+          if (qc >= (uint32_t)C::kStages) ok = reduce_step(qc - C::kStages);
+        } else {
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait(&qdo_empty[st], ((qc / C::kStages) & 1) ^ 1, ctl, kWaitBwdLoad));
+        }
         if (!ok) break;
         const int row = (w.i0 + ii) * kTileM;
+        st_row[st] = head + row;
+        st_nrow[st] = p.N - row;
         if (lane == 0) {
           mbar_arrive_expect_tx(&qdo_full[st], 2 * C::kTileBytes);
           for (int c = 0; c < C::kChunks; ++c) {
@@ -210,7 +251,13 @@ __global__ void __launch_bounds__(320, 1)
         ++qc;
       }
     }
+    if constexpr (C::kDqT) {
+      // The last steps' dQ.
+      const uint32_t first = qc > (uint32_t)C::kStages ? qc - C::kStages : 0u;
+      for (uint32_t k = first; ok && k < qc; ++k) ok = reduce_step(k);
+    }
     if (lane == 0) {
+      bulk_wait_all();  // every reduction has landed
       if (kc > 0) mbar_wait(kv_full, (kc - 1) & 1, ctl, kWaitDrain);
       const uint32_t first = qc > (uint32_t)C::kStages ? qc - C::kStages : 0u;
       for (uint32_t pos = first; pos < qc; ++pos)
@@ -309,7 +356,7 @@ __global__ void __launch_bounds__(320, 1)
           }
           mma_commit(dq_full);
           ++dqc;
-          mma_commit(&qdo_empty[st]);
+          if (!C::kDqT) mma_commit(&qdo_empty[st]);
           ++qc;
         }
         if (!ok) break;
@@ -412,11 +459,13 @@ __global__ void __launch_bounds__(320, 1)
           tmem_ld_wait<64>(v);
           tc_fence_before();
           mbar_arrive(&dq_empty[hc]);
-          float* dst = p.dq_acc + (head + q0 + 64 * hc) * D + dd;
-          const int nrow = min(64, p.N - q0 - 64 * hc);
+          // Row-major [query][head dim] into the stage's Q (half 0) or dO
+          // (half 1) buffer: 32 lanes write one 128-byte run per query.
+          float* buf = reinterpret_cast<float*>(smem + (hc ? C::kOffDO : C::kOffQ) + st * C::kTileBytes);
 #pragma unroll
-          for (int qq = 0; qq < 64; ++qq)
-            if (qq < nrow) atomicAdd(dst + (size_t)qq * D, __uint_as_float(v[qq]));
+          for (int qq = 0; qq < 64; ++qq) buf[qq * D + dd] = __uint_as_float(v[qq]);
+          fence_proxy_async_smem();
+          mbar_arrive(&dq_staged[2 * st + hc]);
         } else {
           // Lane = query row; head-dim columns [32 hc, 32 hc + 32).
           const int qr = q0 + r;

@@ -302,6 +302,14 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, const void* s
       "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
+// dst[i] += src[i] for `bytes` bytes of fp32 (contiguous; 16-byte aligned,
+// size a multiple of 16), element-wise atomic with respect to other
+// reductions into the same memory.
+__device__ __forceinline__ void bulk_reduce_add_f32(float* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(dst),
+               "r"(smem_u32(src)), "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until the shared memory of every committed bulk store has been read.
 __device__ __forceinline__ void bulk_wait_read_all() {
