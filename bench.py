@@ -404,12 +404,15 @@ def fwd_targets(fa, device, peaks, args):
 
     from exact_attention_92_gb300 import inputs
 
-    cases = [
-        ("GPT layer B=8 H=32 N=4096 d=128 causal, Q,K ~ N(0,3^2)", dict(B=8, H=32, N=4096, d=128, causal=True), 3.0),
-        ("B=2 H=16 N=8192 d=128 non-causal", dict(B=2, H=16, N=8192, d=128, causal=False), 1.0),
-        ("B=2 H=16 N=8192 d=128 causal", dict(B=2, H=16, N=8192, d=128, causal=True), 1.0),
-        ("B=1 H=1 N=65536 d=128 causal, split-KV", dict(B=1, H=1, N=65536, d=128, causal=True), 1.0),
-    ]
+    cases = [("GPT layer B=8 H=32 N=4096 d=128 causal, Q,K ~ N(0,3^2)", dict(B=8, H=32, N=4096, d=128, causal=True),
+              3.0)]
+    # The 16K-token sweep at d=128 (hidden 2048), N >= 4K.
+    for N in (4096, 8192, 16384):
+        for causal in (False, True):
+            cases.append((f"B={16384 // N} H=16 N={N} d=128 {'causal' if causal else 'non-causal'}",
+                          dict(B=16384 // N, H=16, N=N, d=128, causal=causal), 1.0))
+    cases.append(("B=1 H=1 N=65536 d=128 causal, split-KV", dict(B=1, H=1, N=65536, d=128, causal=True), 1.0))
+    cases.append(("B=1 H=1 N=65536 d=128 non-causal, split-KV", dict(B=1, H=1, N=65536, d=128, causal=False), 1.0))
     out = []
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream(device)

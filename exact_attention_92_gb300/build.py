@@ -11,6 +11,7 @@ from __future__ import annotations
 
 import concurrent.futures
 import os
+import re
 import shutil
 import subprocess
 import sys
@@ -43,13 +44,32 @@ def _deps():
     return max(os.path.getmtime(f) for f in files)
 
 
+# Kernels that read tensor memory with tcgen05.ld: the destination registers
+# of such a load are only valid after tcgen05.wait::ld, so a register spill
+# between the two would store garbage.  The build refuses any spill in them.
+NO_SPILL_KERNELS = ("fa_fwd_kernel", "fa_bwd_kernel")
+
+
+def check_spills(ptxas_log: str) -> None:
+    entry = None
+    for line in ptxas_log.splitlines():
+        m = re.search(r"Compiling entry function '([^']+)'", line)
+        if m:
+            entry = m.group(1)
+            continue
+        m = re.search(r"(\d+) bytes spill stores, (\d+) bytes spill loads", line)
+        if m and entry and any(k in entry for k in NO_SPILL_KERNELS):
+            if int(m.group(1)) or int(m.group(2)):
+                raise RuntimeError(f"register spills in {entry}: {line.strip()}")
+
+
 def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False) -> str:
     """Compile and link libfa.so if any source is newer than it; return its path."""
     if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps() and not ptxas_verbose:
         return LIB
     os.makedirs(BUILD, exist_ok=True)
     cc = nvcc()
-    extra = ["-Xptxas", "-v"] if ptxas_verbose else []
+    extra = ["-Xptxas", "-v"]
 
     def compile_one(src):
         obj = os.path.join(BUILD, src.replace(".cu", ".o"))
@@ -61,6 +81,8 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
 
     with concurrent.futures.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         results = list(ex.map(compile_one, SOURCES))
+    for _, log in results:
+        check_spills(log)
     if verbose or ptxas_verbose:
         for _, log in results:
             if log.strip():

@@ -198,7 +198,9 @@ __global__ void __launch_bounds__(320, 1)
       __syncwarp();
       return r;
     };
-    for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+    for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units; ++rnd) {
+      const int u = snake_unit(rnd);
+      if (u >= p.num_units) continue;
       const BwdUnit w = decode_bwd(p, u);
       const size_t head = (size_t)w.bh * p.N;
       ok = __all_sync(0xffffffffu, mbar_wait(kv_empty, (kc & 1) ^ 1, ctl, kWaitBwdLoad));
@@ -275,7 +277,9 @@ __global__ void __launch_bounds__(320, 1)
       const uint32_t sds = smem_u32(smem + C::kOffDS);
       uint32_t kc = 0, qc = 0, pc = 0, dqc = 0, uc = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+      for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units; ++rnd) {
+        const int u = snake_unit(rnd);
+        if (u >= p.num_units) continue;
         const BwdUnit w = decode_bwd(p, u);
         ok = mbar_wait(kv_full, kc & 1, ctl, kWaitBwdMma);
         ++kc;
@@ -378,7 +382,9 @@ __global__ void __launch_bounds__(320, 1)
     uint8_t* sds = smem + C::kOffDS;
     uint32_t sc = 0, uc = 0, qc = 0, dc = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+    for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units; ++rnd) {
+      const int u = snake_unit(rnd);
+      if (u >= p.num_units) continue;
       const BwdUnit w = decode_bwd(p, u);
       const int kr = w.j * kTileN + r;  // key index
       const size_t head = (size_t)w.bh * p.N;
@@ -395,36 +401,50 @@ __global__ void __launch_bounds__(320, 1)
         const float* bl = sLse + st * 128;
         const float* bd = sDv + st * 128;
         const bool mask = (kr >= p.N) || (p.causal && kr > q0);
+        // Half 0 handles query chunks 0, 1; half 1 handles 3, 2 (in that
+        // order), so each packed store lands on S^T / dP^T columns this warp
+        // has already read.  Two loads (64 registers) per chunk: a load's
+        // registers must not be live across spills before its wait.
 #pragma unroll 1
         for (int cc = 0; cc < 2; ++cc) {
-          // Half 0 walks query chunks 0, 1; half 1 walks 3, 2, so each packed
-          // store lands on S^T / dP^T columns this warp has already read.
           const int c = hc ? 3 - cc : cc;
-          uint32_t s[32], dp[32];
-          tmem_ld32(tmem + lane_off + C::kColA + 32 * c, s);
-          tmem_ld32(tmem + lane_off + C::kColB + 32 * c, dp);
-          tmem_ld_wait<32>(s);
-          tmem_ld_wait<32>(dp);
+          uint32_t s[1][32], dpv[1][32];
+          tmem_ld32(tmem + lane_off + C::kColA + 32 * c, s[0]);
+          tmem_ld32(tmem + lane_off + C::kColB + 32 * c, dpv[0]);
+          tmem_ld_wait<32>(s[0]);
+          tmem_ld_wait<32>(dpv[0]);
+          const int ci = 0;
           uint32_t pp[16], dd[16];
 #pragma unroll
           for (int e4 = 0; e4 < 8; ++e4) {
             const float4 l4 = reinterpret_cast<const float4*>(bl + 32 * c)[e4];
             const float4 d4 = reinterpret_cast<const float4*>(bd + 32 * c)[e4];
-            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-            const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
-            float pr[4], dr[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int col = 32 * c + 4 * e4 + e;
-              float pv = ex2_approx(fmaf(__uint_as_float(s[4 * e4 + e]), sl2, -lv[e]));
-              if (mask && (kr >= p.N || (p.causal && kr > q0 + col))) pv = 0.f;
-              pr[e] = pv;
-              dr[e] = pv * (__uint_as_float(dp[4 * e4 + e]) - dv[e]);
+            // P^T = exp2(S^T * scale * log2(e) - L), two columns per packed op.
+            const float2 a01 = __ffma2_rn(make_float2(__uint_as_float(s[ci][4 * e4]), __uint_as_float(s[ci][4 * e4 + 1])),
+                                          make_float2(sl2, sl2), make_float2(-l4.x, -l4.y));
+            const float2 a23 = __ffma2_rn(make_float2(__uint_as_float(s[ci][4 * e4 + 2]), __uint_as_float(s[ci][4 * e4 + 3])),
+                                          make_float2(sl2, sl2), make_float2(-l4.z, -l4.w));
+            float2 p01 = make_float2(ex2_approx(a01.x), ex2_approx(a01.y));
+            float2 p23 = make_float2(ex2_approx(a23.x), ex2_approx(a23.y));
+            if (mask) {
+              const int col = q0 + 32 * c + 4 * e4;
+              const bool dead = kr >= p.N;
+              if (dead || (p.causal && kr > col)) p01.x = 0.f;
+              if (dead || (p.causal && kr > col + 1)) p01.y = 0.f;
+              if (dead || (p.causal && kr > col + 2)) p23.x = 0.f;
+              if (dead || (p.causal && kr > col + 3)) p23.y = 0.f;
             }
-            pp[2 * e4] = pack_bf16(pr[0], pr[1]);
-            pp[2 * e4 + 1] = pack_bf16(pr[2], pr[3]);
-            dd[2 * e4] = pack_bf16(dr[0], dr[1]);
-            dd[2 * e4 + 1] = pack_bf16(dr[2], dr[3]);
+            // dS^T = P^T * (dP^T - D)
+            const float2 g01 = __fadd2_rn(make_float2(__uint_as_float(dpv[ci][4 * e4]), __uint_as_float(dpv[ci][4 * e4 + 1])),
+                                          make_float2(-d4.x, -d4.y));
+            const float2 g23 = __fadd2_rn(make_float2(__uint_as_float(dpv[ci][4 * e4 + 2]), __uint_as_float(dpv[ci][4 * e4 + 3])),
+                                          make_float2(-d4.z, -d4.w));
+            const float2 ds01 = __fmul2_rn(p01, g01);
+            const float2 ds23 = __fmul2_rn(p23, g23);
+            pp[2 * e4] = pack_bf16(p01.x, p01.y);
+            pp[2 * e4 + 1] = pack_bf16(p23.x, p23.y);
+            dd[2 * e4] = pack_bf16(ds01.x, ds01.y);
+            dd[2 * e4 + 1] = pack_bf16(ds23.x, ds23.y);
           }
           const uint32_t dst = c < 2 ? 16u * c : 96u + 16u * (c - 2);
           tmem_st16(tmem + lane_off + C::kColA + dst, pp);

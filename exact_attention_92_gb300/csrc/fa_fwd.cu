@@ -60,6 +60,7 @@ struct Unit {
   int q0;     // first query row of the 256-row block
   int kvb;    // first key tile of this split
   int n[2];   // key tiles processed by query tile 0 / 1 (0 = none)
+  int split;
 };
 
 __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
@@ -76,6 +77,7 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
   const int lo = split * p.kv_tiles_per_split;
   const int hi = min(nkv, lo + p.kv_tiles_per_split);
   w.kvb = lo;
+  w.split = split;
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     const int row0 = w.q0 + kTileM * t;
@@ -183,7 +185,9 @@ __global__ void __launch_bounds__(320, 1)
       uint32_t rc = 0;
       uint32_t qc[2] = {0, 0};
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+      for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units; ++rnd) {
+        const int u = snake_unit(rnd);
+        if (u >= p.num_units) continue;
         const Unit w = decode_unit(p, u);
         for (int t = 0; ok && t < 2; ++t) {
           if (w.n[t] == 0) continue;
@@ -230,7 +234,9 @@ __global__ void __launch_bounds__(320, 1)
       uint32_t rc = 0;
       uint32_t qc[2] = {0, 0}, pc[2] = {0, 0};
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+      for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units; ++rnd) {
+        const int u = snake_unit(rnd);
+        if (u >= p.num_units) continue;
         const Unit w = decode_unit(p, u);
         const int nmax = max(w.n[0], w.n[1]);
         if (nmax == 0) continue;
@@ -304,11 +310,13 @@ __global__ void __launch_bounds__(320, 1)
     const float sl2 = p.scale_log2;
     uint32_t sc = 0, oc = 0, stc = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+    for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units; ++rnd) {
+      const int u = snake_unit(rnd);
+      if (u >= p.num_units) continue;
       const Unit w = decode_unit(p, u);
       const int row0 = w.q0 + kTileM * t;
       const int row = row0 + r_in_tile;
-      const int split = u % p.num_splits;
+      const int split = w.split;
       if (w.n[t] == 0) {
         // No visible key in this split: an empty partial (O = 0, L = -inf).
         if (p.num_splits > 1 && row < p.N) {

@@ -27,6 +27,15 @@ __device__ __forceinline__ uint32_t warp_id() {
   return __shfl_sync(0xffffffffu, threadIdx.x / 32, 0);
 }
 
+// Persistent-grid schedule: round r hands units [r G, (r+1) G) to the G CTAs,
+// in reverse CTA order on odd rounds.  Over a list sorted by decreasing work
+// this evens out each CTA's total (a CTA that gets a heavy unit in one round
+// gets a light one in the next).  Every role of a CTA walks the same units.
+__device__ __forceinline__ int snake_unit(int r) {
+  const int G = gridDim.x, c = blockIdx.x;
+  return r * G + ((r & 1) ? (G - 1 - c) : c);
+}
+
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
