@@ -96,6 +96,45 @@ __device__ __forceinline__ BwdUnit decode_bwd(const BwdParams& p, int u) {
   return w;
 }
 
+// P^T and dS^T of 32 query columns of one key row: p = exp2(s * sl2 - L),
+// ds = p * (dP - D), packed to bf16 pairs.  MASK zeroes the weights the
+// causal mask hides (kr > query) and those of a key row past N; it is a
+// template argument so the unmasked instance has no branch at all and the
+// compiler can interleave its independent chains.
+template <bool MASK>
+__device__ __forceinline__ void bwd_chunk(const uint32_t* s, const uint32_t* dpv, const float* bl, const float* bd,
+                                          float sl2, int kr, int q_first, bool dead, bool causal, uint32_t* pp,
+                                          uint32_t* dd) {
+#pragma unroll
+  for (int e4 = 0; e4 < 8; ++e4) {
+    const float4 l4 = reinterpret_cast<const float4*>(bl)[e4];
+    const float4 d4 = reinterpret_cast<const float4*>(bd)[e4];
+    const float2 a01 = __ffma2_rn(make_float2(__uint_as_float(s[4 * e4]), __uint_as_float(s[4 * e4 + 1])),
+                                  make_float2(sl2, sl2), make_float2(-l4.x, -l4.y));
+    const float2 a23 = __ffma2_rn(make_float2(__uint_as_float(s[4 * e4 + 2]), __uint_as_float(s[4 * e4 + 3])),
+                                  make_float2(sl2, sl2), make_float2(-l4.z, -l4.w));
+    float2 p01 = make_float2(ex2_approx(a01.x), ex2_approx(a01.y));
+    float2 p23 = make_float2(ex2_approx(a23.x), ex2_approx(a23.y));
+    if (MASK) {
+      const int col = q_first + 4 * e4;
+      p01.x = (dead || (causal && kr > col)) ? 0.f : p01.x;
+      p01.y = (dead || (causal && kr > col + 1)) ? 0.f : p01.y;
+      p23.x = (dead || (causal && kr > col + 2)) ? 0.f : p23.x;
+      p23.y = (dead || (causal && kr > col + 3)) ? 0.f : p23.y;
+    }
+    const float2 g01 = __fadd2_rn(make_float2(__uint_as_float(dpv[4 * e4]), __uint_as_float(dpv[4 * e4 + 1])),
+                                  make_float2(-d4.x, -d4.y));
+    const float2 g23 = __fadd2_rn(make_float2(__uint_as_float(dpv[4 * e4 + 2]), __uint_as_float(dpv[4 * e4 + 3])),
+                                  make_float2(-d4.z, -d4.w));
+    const float2 ds01 = __fmul2_rn(p01, g01);
+    const float2 ds23 = __fmul2_rn(p23, g23);
+    pp[2 * e4] = pack_bf16(p01.x, p01.y);
+    pp[2 * e4 + 1] = pack_bf16(p23.x, p23.y);
+    dd[2 * e4] = pack_bf16(ds01.x, ds01.y);
+    dd[2 * e4 + 1] = pack_bf16(ds23.x, ds23.y);
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(320, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -413,39 +452,12 @@ __global__ void __launch_bounds__(320, 1)
           tmem_ld32(tmem + lane_off + C::kColB + 32 * c, dpv[0]);
           tmem_ld_wait<32>(s[0]);
           tmem_ld_wait<32>(dpv[0]);
-          const int ci = 0;
           uint32_t pp[16], dd[16];
-#pragma unroll
-          for (int e4 = 0; e4 < 8; ++e4) {
-            const float4 l4 = reinterpret_cast<const float4*>(bl + 32 * c)[e4];
-            const float4 d4 = reinterpret_cast<const float4*>(bd + 32 * c)[e4];
-            // P^T = exp2(S^T * scale * log2(e) - L), two columns per packed op.
-            const float2 a01 = __ffma2_rn(make_float2(__uint_as_float(s[ci][4 * e4]), __uint_as_float(s[ci][4 * e4 + 1])),
-                                          make_float2(sl2, sl2), make_float2(-l4.x, -l4.y));
-            const float2 a23 = __ffma2_rn(make_float2(__uint_as_float(s[ci][4 * e4 + 2]), __uint_as_float(s[ci][4 * e4 + 3])),
-                                          make_float2(sl2, sl2), make_float2(-l4.z, -l4.w));
-            float2 p01 = make_float2(ex2_approx(a01.x), ex2_approx(a01.y));
-            float2 p23 = make_float2(ex2_approx(a23.x), ex2_approx(a23.y));
-            if (mask) {
-              const int col = q0 + 32 * c + 4 * e4;
-              const bool dead = kr >= p.N;
-              if (dead || (p.causal && kr > col)) p01.x = 0.f;
-              if (dead || (p.causal && kr > col + 1)) p01.y = 0.f;
-              if (dead || (p.causal && kr > col + 2)) p23.x = 0.f;
-              if (dead || (p.causal && kr > col + 3)) p23.y = 0.f;
-            }
-            // dS^T = P^T * (dP^T - D)
-            const float2 g01 = __fadd2_rn(make_float2(__uint_as_float(dpv[ci][4 * e4]), __uint_as_float(dpv[ci][4 * e4 + 1])),
-                                          make_float2(-d4.x, -d4.y));
-            const float2 g23 = __fadd2_rn(make_float2(__uint_as_float(dpv[ci][4 * e4 + 2]), __uint_as_float(dpv[ci][4 * e4 + 3])),
-                                          make_float2(-d4.z, -d4.w));
-            const float2 ds01 = __fmul2_rn(p01, g01);
-            const float2 ds23 = __fmul2_rn(p23, g23);
-            pp[2 * e4] = pack_bf16(p01.x, p01.y);
-            pp[2 * e4 + 1] = pack_bf16(p23.x, p23.y);
-            dd[2 * e4] = pack_bf16(ds01.x, ds01.y);
-            dd[2 * e4 + 1] = pack_bf16(ds23.x, ds23.y);
-          }
+          if (mask)
+            bwd_chunk<true>(s[0], dpv[0], bl + 32 * c, bd + 32 * c, sl2, kr, q0 + 32 * c, kr >= p.N, p.causal != 0,
+                            pp, dd);
+          else
+            bwd_chunk<false>(s[0], dpv[0], bl + 32 * c, bd + 32 * c, sl2, kr, q0 + 32 * c, false, false, pp, dd);
           const uint32_t dst = c < 2 ? 16u * c : 96u + 16u * (c - 2);
           tmem_st16(tmem + lane_off + C::kColA + dst, pp);
           tmem_st16(tmem + lane_off + C::kColB + dst, dd);
