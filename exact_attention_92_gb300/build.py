@@ -50,6 +50,13 @@ def _deps():
 NO_SPILL_KERNELS = ("fa_fwd_kernel", "fa_bwd_kernel")
 
 
+# Kernels that move registers between warpgroups with setmaxnreg, and the
+# per-thread count they must be launched with.  The split's shares are
+# static_asserted against this count in the source; if ptxas gave the entry
+# fewer registers, the warpgroup that asks for more would wait forever.
+REG_SPLIT_KERNELS = {"fa_fwd_kernel": 168}
+
+
 def check_spills(ptxas_log: str) -> None:
     entry = None
     for line in ptxas_log.splitlines():
@@ -61,6 +68,11 @@ def check_spills(ptxas_log: str) -> None:
         if m and entry and any(k in entry for k in NO_SPILL_KERNELS):
             if int(m.group(1)) or int(m.group(2)):
                 raise RuntimeError(f"register spills in {entry}: {line.strip()}")
+        m = re.search(r"Used (\d+) registers", line)
+        if m and entry:
+            for k, regs in REG_SPLIT_KERNELS.items():
+                if k in entry and int(m.group(1)) != regs:
+                    raise RuntimeError(f"{entry} starts with {m.group(1)} registers, its register split needs {regs}")
 
 
 def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False) -> str:

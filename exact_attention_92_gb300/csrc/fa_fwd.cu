@@ -19,8 +19,7 @@
 // Online softmax (section 6.1): the running max m and sum l live in registers
 // of the row's thread, O~ stays unnormalised in TMEM and is divided by l
 // once at the end; L = m + log l is written for the backward pass.  P is
-// rounded to bf16 for the PV MMA; O~ is divided by the sum of those rounded
-// weights (so O is their exact weighted mean) while L uses the fp32 sum.  The
+// rounded to bf16 for the PV MMA; l sums the fp32 weights.  The
 // exp(m_old - m_new) correction of O~ is applied only when a row's max grows
 // by more than 2^8 over the reference the row's O~ and l are kept at;
 // otherwise the old reference stays.  O~ and l always share one reference,
@@ -43,7 +42,9 @@ struct FwdCfg {
   static constexpr int kChunkBytes = kTileM * 128;     // one 128-row x 64-column block
   static constexpr int kTileBytes = kTileM * D * 2;    // one 128 x D bf16 tile
   static constexpr int kStages = (D == 128) ? 4 : 8;   // K/V ring slots
-  static constexpr int kThreads = 320;
+  // Three warpgroups: 0-1 softmax (one 128-row Q tile each), 2 the MMA
+  // issuer (warp 8), the TMA producer (warp 9) and two idle warps.
+  static constexpr int kThreads = 384;
   __host__ __device__ static constexpr uint32_t col_s(int t) { return 128u * t; }
   __host__ __device__ static constexpr uint32_t col_o(int t) { return 256u + (uint32_t)D * t; }
   static constexpr uint32_t kTmemCols = 512;
@@ -53,6 +54,16 @@ struct FwdCfg {
   static constexpr int kNumBars = 2 + 2 + 2 * kStages + 2 + 2 + 2 + 1 + 2;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16;
   static constexpr float kRescaleThreshold = 8.0f;     // log2 units
+  // Register split (setmaxnreg).  At 384 threads and one CTA per SM each
+  // thread starts with 168 registers (three warps per SM sub-partition share
+  // its 16384); warpgroup 2 hands registers back so the softmax warpgroups,
+  // which hold a whole 128-column S row, get 216.  The shares must not exceed
+  // what the CTA was launched with, or the increase waits forever.
+  static constexpr int kRegsAtLaunch = 168;
+  static constexpr int kRegsCtl = 72;
+  static constexpr int kRegsMath = 216;
+  static_assert(128 * kRegsCtl + 256 * kRegsMath <= kThreads * kRegsAtLaunch, "register split exceeds the launch");
+  static_assert(kRegsCtl % 8 == 0 && kRegsMath % 8 == 0, "setmaxnreg counts are multiples of 8");
 };
 
 struct Unit {
@@ -118,7 +129,7 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint3
 }
 
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                   const FwdParams p) {
@@ -178,8 +189,8 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtl ctl{p.status, p.timeout_ns};
-
   if (warp == 9) {
+    reg_dealloc<C::kRegsCtl>();
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t rc = 0;
@@ -222,6 +233,7 @@ __global__ void __launch_bounds__(320, 1)
         if (qc[t] > 0) mbar_wait(&q_full[t], (qc[t] - 1) & 1, ctl, kWaitDrain);
     }
   } else if (warp == 8) {
+    reg_dealloc<C::kRegsCtl>();
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
       // Descriptor low halves: buffer i of a kind is (i * tile bytes) / 16
@@ -300,7 +312,8 @@ __global__ void __launch_bounds__(320, 1)
       mbar_wait(drain, 0, ctl, kWaitDrain);
     }
     __syncwarp();
-  } else {
+  } else if (warp < 8) {
+    reg_alloc<C::kRegsMath>();
     // ------------------------------------------------------------- softmax
     const int t = warp >> 2;
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
@@ -328,8 +341,7 @@ __global__ void __launch_bounds__(320, 1)
         continue;
       }
       float m_ref = -INFINITY;  // reference max of this row, log2 units
-      float l = 0.f;     // sum of the fp32 weights: L = m + log l
-      float l_bf = 0.f;  // sum of the bf16-rounded weights the PV MMA uses
+      float l = 0.f;  // sum of the fp32 weights
       for (int j = 0; j < w.n[t]; ++j) {
         ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t], sc & 1, ctl, kWaitSFull));
         ++sc;
@@ -367,7 +379,6 @@ __global__ void __launch_bounds__(320, 1)
           const float m_new = fmaxf(m_ref, m_tile);
           f = ex2_approx(m_ref - m_new);
           l *= f;
-          l_bf *= f;
           m_ref = m_new;
           rescale = true;
         }
@@ -376,7 +387,7 @@ __global__ void __launch_bounds__(320, 1)
         // packed fp32x2 FMA and adds.
         const float2 sl2v = make_float2(sl2, sl2);
         const float2 negv = make_float2(-m_ref, -m_ref);
-        float2 ls0 = make_float2(0.f, 0.f), ls1 = ls0, lr0 = ls0, lr1 = ls0;
+        float2 ls0 = make_float2(0.f, 0.f), ls1 = ls0;
 #pragma unroll
         for (int h = 0; h < kTileN / 32; ++h) {
           uint32_t pk[16];
@@ -385,21 +396,15 @@ __global__ void __launch_bounds__(320, 1)
             const float2 a = __ffma2_rn(make_float2(x[32 * h + e], x[32 * h + e + 1]), sl2v, negv);
             const float p0 = ex2_approx(a.x);
             const float p1 = ex2_approx(a.y);
-            const uint32_t pp = pack_bf16(p0, p1);
-            const float2 pr = make_float2(__uint_as_float(pp << 16), __uint_as_float(pp & 0xffff0000u));
-            if ((e >> 1) & 1) {
+            if ((e >> 1) & 1)
               ls1 = __fadd2_rn(ls1, make_float2(p0, p1));
-              lr1 = __fadd2_rn(lr1, pr);
-            } else {
+            else
               ls0 = __fadd2_rn(ls0, make_float2(p0, p1));
-              lr0 = __fadd2_rn(lr0, pr);
-            }
-            pk[e / 2] = pp;
+            pk[e / 2] = pack_bf16(p0, p1);
           }
           tmem_st16(tS + 16 * h, pk);
         }
         l += (ls0.x + ls0.y) + (ls1.x + ls1.y);
-        l_bf += (lr0.x + lr0.y) + (lr1.x + lr1.y);
         if (rescale) {
           // O~ <- exp2(m_old - m_new) O~; the previous PV MMA has completed
           // (it was issued before this S tile's MMA) and the next one waits
@@ -428,9 +433,7 @@ __global__ void __launch_bounds__(320, 1)
       ++oc;
       if (!ok) break;
       tc_fence_after();
-      // O~ / l_bf is an exact weighted mean of the rounded weights; the
-      // logsumexp takes the unrounded sum.
-      const float inv_l = 1.0f / l_bf;
+      const float inv_l = 1.0f / l;
       const float lse = (m_ref + lg2_approx(l)) * 0.69314718055994530942f;
       if (p.num_splits == 1) {
         // O rows -> Q_t's buffer (no longer read: every S_t MMA finished
@@ -499,6 +502,8 @@ __global__ void __launch_bounds__(320, 1)
     // Every O store this warpgroup issued has landed before the CTA exits.
     if ((warp & 3) == 0 && lane == 0) bulk_wait_all();
     __syncwarp();
+  } else {
+    reg_dealloc<C::kRegsCtl>();
   }
 
   tc_fence_before();

@@ -12,6 +12,14 @@
 namespace fa {
 namespace dev {
 
+// Per-warpgroup register budget (setmaxnreg): every warp of a warpgroup
+// executes the same one.  inc blocks until other warpgroups' dec have freed
+// enough of the registers the CTA was launched with.
+template <int N>
+__device__ __forceinline__ void reg_alloc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
+template <int N>
+__device__ __forceinline__ void reg_dealloc() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -77,7 +85,9 @@ struct WaitCtl {
   unsigned long long timeout_ns;
 };
 
-static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, WaitCtl ctl, uint32_t where) {
+// Inlined rather than called: a kernel that splits registers with setmaxnreg
+// cannot call one function from warpgroups with different budgets.
+static __device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, WaitCtl ctl, uint32_t where) {
   const uint64_t t0 = globaltimer_ns();
   while (true) {
 #pragma unroll 1
