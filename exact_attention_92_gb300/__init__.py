@@ -38,4 +38,4 @@ FA_KERNEL_FWD = 0
 FA_KERNEL_COMBINE = 1
 FA_KERNEL_BWD_PRE = 2
 FA_KERNEL_BWD = 3
-FA_KERNEL_DQ_CONVERT = 4
+FA_KERNEL_BWD_DQ = 4

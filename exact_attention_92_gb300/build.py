@@ -47,14 +47,14 @@ def _deps():
 # Kernels that read tensor memory with tcgen05.ld: the destination registers
 # of such a load are only valid after tcgen05.wait::ld, so a register spill
 # between the two would store garbage.  The build refuses any spill in them.
-NO_SPILL_KERNELS = ("fa_fwd_kernel", "fa_bwd_kernel")
+NO_SPILL_KERNELS = ("fa_fwd_kernel", "fa_bwd_dkdv_kernel", "fa_bwd_dq_kernel")
 
 
 # Kernels that move registers between warpgroups with setmaxnreg, and the
 # per-thread count they must be launched with.  The split's shares are
 # static_asserted against this count in the source; if ptxas gave the entry
 # fewer registers, the warpgroup that asks for more would wait forever.
-REG_SPLIT_KERNELS = {"fa_fwd_kernel": 168}
+REG_SPLIT_KERNELS = {"fa_fwd_kernel": 168, "fa_bwd_dkdv_kernel": 168, "fa_bwd_dq_kernel": 168}
 
 
 def check_spills(ptxas_log: str) -> None:

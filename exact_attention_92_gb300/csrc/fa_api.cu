@@ -18,11 +18,12 @@ namespace fa {
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& to, const FwdParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_combine(int d, const CombineParams& p, cudaStream_t stream);
-cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const BwdParams& p, int grid, cudaStream_t stream);
-cudaError_t launch_bwd_preprocess(int d, const void* o, const void* dout, float* dvec, float* dq_acc, int rows,
+cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const BwdParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_bwd_dq(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const CUtensorMap& tdo, const BwdParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_bwd_preprocess(int d, const void* o, const void* dout, float* dvec, int rows,
                                   cudaStream_t stream);
-cudaError_t launch_dq_convert(int d, const float* dq_acc, void* dq, size_t elems, float scale, cudaStream_t stream);
 cudaError_t launch_selftest_wait(unsigned int* status, unsigned long long timeout_ns, cudaStream_t stream);
 }  // namespace fa
 
@@ -219,7 +220,7 @@ int fa_timing_enable(int on) {
 }
 
 int fa_timing_read(int kernel, int* launches, double* total_ms) {
-  if (!launches || !total_ms || kernel < 0 || kernel > FA_KERNEL_DQ_CONVERT) return FA_ERR_INVALID_ARG;
+  if (!launches || !total_ms || kernel < 0 || kernel > FA_KERNEL_BWD_DQ) return FA_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> g(g_tmu);
   int n = 0;
   double ms = 0.0;
@@ -373,15 +374,14 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
       encode_bhnd(&tdo, dout, BH, N, d))
     return FA_ERR_CUDA;
 
-  // Workspace: fp32 dQ accumulator [rows, d] and D [rows].
+  // Workspace: D [rows].
   void* ws = nullptr;
-  const size_t bytes = rows * ((size_t)d + 1) * sizeof(float);
+  const size_t bytes = rows * sizeof(float);
   if (cudaMallocAsync(&ws, bytes, st) != cudaSuccess) {
     cudaGetLastError();
     return FA_ERR_NO_MEMORY;
   }
-  float* dq_acc = static_cast<float*>(ws);
-  float* dvec = dq_acc + rows * d;
+  float* dvec = static_cast<float*>(ws);
 
   fa::BwdParams p;
   std::memset(&p, 0, sizeof(p));
@@ -393,22 +393,21 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
   p.scale_log2 = scale * 1.4426950408889634f;
   p.lse = lse;
   p.dvec = dvec;
-  p.dq_acc = dq_acc;
+  p.dq = dq;
   p.dk = dk;
   p.dv = dv;
-  p.num_kv_tiles = (N + 127) / 128;
-  p.num_units = BH * p.num_kv_tiles;
+  p.num_tiles = (N + 127) / 128;
+  p.num_units = BH * p.num_tiles;
   p.status = s->status;
   p.timeout_ns = g_timeout_ns.load();
 
-  cudaError_t ce = timed(FA_KERNEL_BWD_PRE, st,
-                         [&] { return fa::launch_bwd_preprocess(d, o, dout, dvec, dq_acc, (int)rows, st); });
-  if (ce == cudaSuccess) {
-    const int grid = p.num_units < s->sm_count ? p.num_units : s->sm_count;
-    ce = timed(FA_KERNEL_BWD, st, [&] { return fa::launch_bwd(d, tq, tk, tv, tdo, p, grid, st); });
-  }
+  const int grid = p.num_units < s->sm_count ? p.num_units : s->sm_count;
+  cudaError_t ce =
+      timed(FA_KERNEL_BWD_PRE, st, [&] { return fa::launch_bwd_preprocess(d, o, dout, dvec, (int)rows, st); });
   if (ce == cudaSuccess)
-    ce = timed(FA_KERNEL_DQ_CONVERT, st, [&] { return fa::launch_dq_convert(d, dq_acc, dq, rows * d, scale, st); });
+    ce = timed(FA_KERNEL_BWD, st, [&] { return fa::launch_bwd_dkdv(d, tq, tk, tv, tdo, p, grid, st); });
+  if (ce == cudaSuccess)
+    ce = timed(FA_KERNEL_BWD_DQ, st, [&] { return fa::launch_bwd_dq(d, tq, tk, tv, tdo, p, grid, st); });
   cudaFreeAsync(ws, st);
   return ce == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }

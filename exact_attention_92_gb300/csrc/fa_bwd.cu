@@ -1,45 +1,39 @@
 // Backward pass of exact attention on sm_103a ("FlashAttention V2 in depth",
 // section 7).
 //
-//   fa_bwd_preprocess  D_i = rowsum(dO_i * O_i) (section 7.3, a separate
-//                      kernel run once) and zeroing of the fp32 dQ
-//                      accumulator.
-//   fa_bwd_kernel      key/value tiles in the outer loop (section 7.2): a
-//                      persistent CTA owns one 128-key tile K_j, V_j of one
-//                      (batch, head) and walks the query tiles i that can see
-//                      it.  dK_j and dV_j accumulate in tensor memory of that
-//                      CTA alone (no atomics); the partial dQ of every step is
-//                      added to the fp32 accumulator with atomics.
-//   fa_dq_convert      dQ = scale * accumulator, to bf16.
+//   fa_bwd_preprocess   D_i = rowsum(dO_i * O_i) (section 7.3), once.
+//   fa_bwd_dkdv_kernel  key/value tiles in the outer loop (section 7.2): a
+//                       persistent CTA owns one 128-key tile K_j, V_j of one
+//                       (batch, head) and walks the query tiles i that can
+//                       see it; dK_j and dV_j accumulate in tensor memory.
+//   fa_bwd_dq_kernel    query tiles in the outer loop: a CTA owns one
+//                       128-query tile Q_i, dO_i and walks the key tiles j it
+//                       can see; dQ_i accumulates in tensor memory and is
+//                       written once, as bf16.
 //
-// Per step (query tile i of 128 rows), in the transposed orientation so that
-// TMEM lanes are keys:
-//   S^T  = K_j Q_i^T,   P^T = exp(scale S^T - L_i)   (P recovered from the
-//                       saved logsumexp, section 7.1)
-//   dP^T = V_j dO_i^T,  dS^T = P^T * (dP^T - D_i)
-//   dV_j += P^T dO_i,   dK_j += dS^T Q_i
-//   d = 128: dQ_i^T = K_j^T dS^T; the softmax warps write it row-major into
-//            the step's Q/dO stage buffer (free once dQ is complete) and the
-//            producer adds each 64-row half (32 contiguous KB of the
-//            accumulator) with one bulk reduce-add, then refills the stage
-//   d = 64:  dQ_i = dS K_j, added with per-thread vector atomics
-// The softmax scale is applied once to dK at the end and to dQ in the
-// convert kernel.
+// Both kernels recompute P from the saved logsumexp (section 7.1) and
+// dS = P * (dP - D).  Splitting dQ from dK/dV costs the S and dP products a
+// second time but removes the fp32 atomic accumulation of dQ over key tiles,
+// whose reductions into L2 bound the single-kernel form on this GPU (about
+// 24 bytes per clock per SM when every SM reduces).  The products per
+// (key tile, query tile) pair are
+//   dK/dV kernel (TMEM lanes are keys):
+//     S^T = K Q^T,  dP^T = V dO^T,  dV += P^T dO,  dK += dS^T Q
+//   dQ kernel (TMEM lanes are queries):
+//     S = Q K^T,    dP = dO V^T,    dQ += dS K
+// The softmax scale is applied once to dK and dQ when they are written.
 //
-// Roles (320 threads): warp 9 loads (TMA for K, V, Q, dO; plain loads for
-// L_i and D_i into shared memory), warp 8 issues tcgen05 MMAs, warps 0-7
-// compute P^T and dS^T (a key row per lane, warps w and w+4 split the 128
-// query columns), then read their half of dQ out of TMEM, release it and
-// stage it for the reduction while the next step's S^T / dP^T run, and
-// write dK/dV at the end of a unit.
+// Roles (384 threads, three warpgroups, registers split with setmaxnreg as
+// in the forward kernel): warp 9 loads (TMA), warp 8 issues tcgen05 MMAs,
+// warps 10-11 idle, warps 0-7 do the element-wise work (a TMEM lane per
+// thread; warps w and w+4 split the 128 columns of a tile) and write the
+// results.
 //
-// TMEM (512 columns).  A = [0,128): S^T; P^T (bf16, two per column) goes to
-// A[0,32) for queries 0-63 and A[96,128) for queries 64-127, each written
-// over S^T columns its own warp has already read.  B = [128,256): dP^T, then
-// dS^T in B[0,32) and B[96,128).  dV and dK follow.  At d = 128 the dQ^T
-// halves take the free middle columns A[32,96) and B[32,96), so the next
-// step's S^T / dP^T wait for them to be read out; at d = 64 dQ has its own
-// 64 columns.
+// Pipelining.  The element-wise warps read a tile of S into registers and
+// compute P from it while the tensor core runs other products; they read dP
+// when it lands, and P^T / dS^T (dK/dV kernel) or dS (dQ kernel) go back to
+// TMEM as bf16 pairs over columns the same warp has already read, where the
+// next products take them as the TMEM operand.
 #include <cuda_runtime.h>
 
 #include "sm103_primitives.cuh"
@@ -48,99 +42,137 @@ namespace fa {
 
 using namespace dev;
 
+// Register split shared by both kernels: 168 per thread at launch (three
+// warps per SM sub-partition); warpgroup 2 keeps kRegsCtl, the element-wise
+// warpgroups get kRegsMath.
+struct BwdRegs {
+  static constexpr int kRegsAtLaunch = 168;
+  static constexpr int kRegsCtl = 72;
+  static constexpr int kRegsMath = 216;
+  static_assert(128 * kRegsCtl + 256 * kRegsMath <= 384 * kRegsAtLaunch, "register split exceeds the launch");
+};
+
+// ---------------------------------------------------------------- dK / dV
+
 template <int D>
-struct BwdCfg {
+struct DkdvCfg {
   static constexpr int kChunks = D / 64;
   static constexpr int kChunkBytes = kTileM * 128;
   static constexpr int kTileBytes = kTileM * D * 2;
-  static constexpr int kStages = 2;
-  static constexpr int kThreads = 320;
-  static constexpr uint32_t kColA = 0;
-  static constexpr uint32_t kColB = 128;
+  static constexpr int kQStages = 3;  // the next step's S^T needs Q early
+  static constexpr int kDoStages = 2;
+  static constexpr int kThreads = 384;
+  static constexpr uint32_t kColS = 0;    // S^T
+  static constexpr uint32_t kColB = 128;  // dP^T, then P^T | dS^T packed
   static constexpr uint32_t kColDV = 256;
   static constexpr uint32_t kColDK = 256 + D;
-  static constexpr bool kDqT = (D == 128);
-  static constexpr uint32_t kColDQ = kDqT ? 32u : 384u;  // d = 128: A+32 and B+32
   static constexpr uint32_t kTmemCols = 512;
-  // Shared memory.
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kTileBytes;
   static constexpr int kOffQ = 2 * kTileBytes;
-  static constexpr int kOffDO = kOffQ + kStages * kTileBytes;
-  static constexpr int kOffDS = kOffDO + kStages * kTileBytes;
-  static constexpr int kDsBytes = kTileM * kTileN * 2;
-  static constexpr int kOffLse = kOffDS + kDsBytes;             // kStages x 128 floats (log2 units)
-  static constexpr int kOffDvec = kOffLse + kStages * 128 * 4;  // kStages x 128 floats
-  static constexpr int kOffBar = kOffDvec + kStages * 128 * 4;
-  static constexpr int kNumBars = 2 + 3 * kStages + 1 + 1 + 1 + 2 + 2 + 1 + 2 * kStages;
+  static constexpr int kOffDO = kOffQ + kQStages * kTileBytes;
+  static constexpr int kOffLse = kOffDO + kDoStages * kTileBytes;  // kQStages x 128 floats (log2 units)
+  static constexpr int kOffDvec = kOffLse + kQStages * 128 * 4;    // kDoStages x 128 floats
+  static constexpr int kOffBar = kOffDvec + kDoStages * 128 * 4;
+  static constexpr int kNumBars = 2 + 2 * kQStages + 2 * kDoStages + 7;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16;
+  static_assert(kSmemBytes <= 232448, "shared memory");
 };
 
-// Packed-P^T / dS^T column of the 16 queries [16 kk, 16 kk + 16) in A or B.
-__device__ __forceinline__ uint32_t packed_col(int kk) { return kk < 4 ? 8u * kk : 96u + 8u * (kk - 4); }
+// Packed column of the 16 columns [16 kk, 16 kk + 16) of a bf16 tile written
+// by the element-wise warps: warp half h holds columns [64 h, 64 h + 64) as
+// bf16 pairs in [64 h, 64 h + 32) of its region (second = true: in
+// [64 h + 32, 64 h + 64)).
+__device__ __forceinline__ uint32_t packed_col(int kk, bool second) {
+  return 64u * (kk >> 2) + (second ? 32u : 0u) + 8u * (kk & 3);
+}
 
 struct BwdUnit {
   int bh;
-  int j;       // key tile
-  int i0, nq;  // first query tile and number of query tiles
+  int t;      // the tile this CTA owns (key tile / query tile)
+  int first;  // first tile of the other operand
+  int count;  // number of tiles of the other operand
 };
 
-__device__ __forceinline__ BwdUnit decode_bwd(const BwdParams& p, int u) {
+// dK/dV units: with the causal mask, low key tiles see the most query tiles,
+// so they come first.
+__device__ __forceinline__ BwdUnit decode_dkdv(const BwdParams& p, int u) {
   BwdUnit w;
   const int BH = p.B * p.H;
   w.bh = u % BH;
-  w.j = u / BH;  // with the causal mask, low key tiles have the most work
-  const int nq = p.num_kv_tiles;
-  w.i0 = p.causal ? w.j : 0;
-  w.nq = nq - w.i0;
+  w.t = u / BH;
+  w.first = p.causal ? w.t : 0;
+  w.count = p.num_tiles - w.first;
   return w;
 }
 
-// P^T and dS^T of 32 query columns of one key row: p = exp2(s * sl2 - L),
-// ds = p * (dP - D), packed to bf16 pairs.  MASK zeroes the weights the
-// causal mask hides (kr > query) and those of a key row past N; it is a
-// template argument so the unmasked instance has no branch at all and the
-// compiler can interleave its independent chains.
+// dQ units: with the causal mask, high query tiles see the most key tiles.
+__device__ __forceinline__ BwdUnit decode_dq(const BwdParams& p, int u) {
+  BwdUnit w;
+  const int BH = p.B * p.H;
+  w.bh = u % BH;
+  w.t = p.causal ? p.num_tiles - 1 - u / BH : u / BH;
+  w.first = 0;
+  w.count = p.causal ? w.t + 1 : p.num_tiles;
+  return w;
+}
+
+// P^T of 64 query columns [q_first, q_first + 64) of key row kr, in place:
+// p = exp2(s * sl2 - L_q) with L per column.  MASK zeroes the weights the
+// causal mask hides (key > query) and those of a key row past N.
 template <bool MASK>
-__device__ __forceinline__ void bwd_chunk(const uint32_t* s, const uint32_t* dpv, const float* bl, const float* bd,
-                                          float sl2, int kr, int q_first, bool dead, bool causal, uint32_t* pp,
-                                          uint32_t* dd) {
+__device__ __forceinline__ void p64_colL(uint32_t* s, const float* bl, float sl2, int kr, int q_first, bool dead,
+                                         bool causal) {
 #pragma unroll
-  for (int e4 = 0; e4 < 8; ++e4) {
+  for (int e4 = 0; e4 < 16; ++e4) {
     const float4 l4 = reinterpret_cast<const float4*>(bl)[e4];
-    const float4 d4 = reinterpret_cast<const float4*>(bd)[e4];
     const float2 a01 = __ffma2_rn(make_float2(__uint_as_float(s[4 * e4]), __uint_as_float(s[4 * e4 + 1])),
                                   make_float2(sl2, sl2), make_float2(-l4.x, -l4.y));
     const float2 a23 = __ffma2_rn(make_float2(__uint_as_float(s[4 * e4 + 2]), __uint_as_float(s[4 * e4 + 3])),
                                   make_float2(sl2, sl2), make_float2(-l4.z, -l4.w));
-    float2 p01 = make_float2(ex2_approx(a01.x), ex2_approx(a01.y));
-    float2 p23 = make_float2(ex2_approx(a23.x), ex2_approx(a23.y));
+    float p0 = ex2_approx(a01.x), p1 = ex2_approx(a01.y), p2 = ex2_approx(a23.x), p3 = ex2_approx(a23.y);
     if (MASK) {
       const int col = q_first + 4 * e4;
-      p01.x = (dead || (causal && kr > col)) ? 0.f : p01.x;
-      p01.y = (dead || (causal && kr > col + 1)) ? 0.f : p01.y;
-      p23.x = (dead || (causal && kr > col + 2)) ? 0.f : p23.x;
-      p23.y = (dead || (causal && kr > col + 3)) ? 0.f : p23.y;
+      p0 = (dead || (causal && kr > col)) ? 0.f : p0;
+      p1 = (dead || (causal && kr > col + 1)) ? 0.f : p1;
+      p2 = (dead || (causal && kr > col + 2)) ? 0.f : p2;
+      p3 = (dead || (causal && kr > col + 3)) ? 0.f : p3;
     }
-    const float2 g01 = __fadd2_rn(make_float2(__uint_as_float(dpv[4 * e4]), __uint_as_float(dpv[4 * e4 + 1])),
-                                  make_float2(-d4.x, -d4.y));
-    const float2 g23 = __fadd2_rn(make_float2(__uint_as_float(dpv[4 * e4 + 2]), __uint_as_float(dpv[4 * e4 + 3])),
-                                  make_float2(-d4.z, -d4.w));
-    const float2 ds01 = __fmul2_rn(p01, g01);
-    const float2 ds23 = __fmul2_rn(p23, g23);
-    pp[2 * e4] = pack_bf16(p01.x, p01.y);
-    pp[2 * e4 + 1] = pack_bf16(p23.x, p23.y);
-    dd[2 * e4] = pack_bf16(ds01.x, ds01.y);
-    dd[2 * e4 + 1] = pack_bf16(ds23.x, ds23.y);
+    s[4 * e4] = __float_as_uint(p0);
+    s[4 * e4 + 1] = __float_as_uint(p1);
+    s[4 * e4 + 2] = __float_as_uint(p2);
+    s[4 * e4 + 3] = __float_as_uint(p3);
+  }
+}
+
+// P of 64 key columns [k_first, k_first + 64) of query row q, in place:
+// p = exp2(s * sl2 - L) with one L for the row.  MASK zeroes keys past N and,
+// with the causal mask, keys after the query.
+template <bool MASK>
+__device__ __forceinline__ void p64_rowL(uint32_t* s, float L, float sl2, int q, int k_first, int N, bool causal) {
+  const float2 sv = make_float2(sl2, sl2);
+  const float2 lv = make_float2(-L, -L);
+#pragma unroll
+  for (int e = 0; e < 64; e += 2) {
+    const float2 a = __ffma2_rn(make_float2(__uint_as_float(s[e]), __uint_as_float(s[e + 1])), sv, lv);
+    float p0 = ex2_approx(a.x), p1 = ex2_approx(a.y);
+    if (MASK) {
+      const int k = k_first + e;
+      p0 = (k >= N || (causal && k > q)) ? 0.f : p0;
+      p1 = (k + 1 >= N || (causal && k + 1 > q)) ? 0.f : p1;
+    }
+    s[e] = __float_as_uint(p0);
+    s[e + 1] = __float_as_uint(p1);
   }
 }
 
 template <int D>
-__global__ void __launch_bounds__(320, 1)
-    fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                  const BwdParams p) {
-  using C = BwdCfg<D>;
+__global__ void __launch_bounds__(384, 1)
+    fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                       const BwdParams p) {
+  using C = DkdvCfg<D>;
+  using R = BwdRegs;
   extern __shared__ __align__(1024) uint8_t smem[];
   if ((smem_u32(smem) & 1023u) != 0u) {
     if (threadIdx.x == 0) atomicCAS(p.status, 0u, (unsigned int)FA_ERR_CUDA);
@@ -149,21 +181,18 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* kv_full = bars;
   uint64_t* kv_empty = bars + 1;
-  uint64_t* qdo_full = bars + 2;
-  uint64_t* qdo_empty = qdo_full + C::kStages;
-  uint64_t* stat_full = qdo_empty + C::kStages;  // L_i, D_i of a stage written
-  uint64_t* s_full = stat_full + C::kStages;
-  uint64_t* p_ready = s_full + 1;
-  uint64_t* dq_full = p_ready + 1;
-  uint64_t* dq_empty = dq_full + 1;  // [2]: the two dQ^T halves read out (d = 64: [0] only)
-  uint64_t* dkv_full = dq_empty + 2;
+  uint64_t* q_full = bars + 2;  // [kQStages]: Q tile and its L values
+  uint64_t* q_empty = q_full + C::kQStages;
+  uint64_t* do_full = q_empty + C::kQStages;  // [kDoStages]: dO tile and its D values
+  uint64_t* do_empty = do_full + C::kDoStages;
+  uint64_t* s_full = do_empty + C::kDoStages;  // S^T in TMEM
+  uint64_t* s_free = s_full + 1;               // S^T read by all element-wise warps
+  uint64_t* dp_full = s_free + 1;              // dP^T in TMEM
+  uint64_t* p_ready = dp_full + 1;             // P^T, dS^T packed in TMEM
+  uint64_t* dkv_full = p_ready + 1;
   uint64_t* dkv_empty = dkv_full + 1;
   uint64_t* drain = dkv_empty + 1;
-  // [stage][half]: a dQ^T half written into that stage's buffer (d = 128).
-  // One pair per stage: a stage is refilled only after its last use was
-  // reduced, so these never run more than one phase ahead of the producer.
-  uint64_t* dq_staged = drain + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dq_staged + 2 * C::kStages);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   float* sLse = reinterpret_cast<float*>(smem + C::kOffLse);
   float* sDv = reinterpret_cast<float*>(smem + C::kOffDvec);
 
@@ -173,22 +202,21 @@ __global__ void __launch_bounds__(320, 1)
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
     mbar_init(kv_empty, 1);
-    for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(&qdo_full[s], 1);
-      mbar_init(&qdo_empty[s], 1);
-      mbar_init(&stat_full[s], 32);
+    for (int s = 0; s < C::kQStages; ++s) {
+      mbar_init(&q_full[s], 1);
+      mbar_init(&q_empty[s], 1);
+    }
+    for (int s = 0; s < C::kDoStages; ++s) {
+      mbar_init(&do_full[s], 1);
+      mbar_init(&do_empty[s], 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(p_ready, 256);
-    mbar_init(dq_full, 1);
-    // d = 128: one barrier per dQ^T half (the 4 warps reading it); d = 64:
-    // all 8 warps release the one dQ tile.
-    mbar_init(&dq_empty[0], C::kDqT ? 128 : 256);
-    mbar_init(&dq_empty[1], 128);
+    mbar_init(s_free, 8);
+    mbar_init(dp_full, 1);
+    mbar_init(p_ready, 8);
     mbar_init(dkv_full, 1);
-    mbar_init(dkv_empty, 256);
+    mbar_init(dkv_empty, 8);
     mbar_init(drain, 1);
-    for (int i = 0; i < 2 * C::kStages; ++i) mbar_init(&dq_staged[i], 128);
     fence_barrier_init();
   }
   if (warp == 8) {
@@ -209,151 +237,143 @@ __global__ void __launch_bounds__(320, 1)
 
   if (warp == 9) {
     // ------------------------------------------------------------ producer
+    reg_dealloc<R::kRegsCtl>();
     uint32_t kc = 0, qc = 0;
-    // Rows (bh * N + q0) and valid row count of the steps in each stage, for
-    // the dQ reduction of d = 128.
-    size_t st_row[C::kStages];
-    int st_nrow[C::kStages];
     bool ok = true;
-    // d = 128: add step `k`'s staged dQ (two 64-row halves in the Q and dO
-    // buffers of stage k % kStages) to the accumulator, and wait until the
-    // copies have read the buffers.
-    auto reduce_step = [&](uint32_t k) -> bool {
-      const uint32_t s = k % C::kStages;
-      const uint32_t par = (k / C::kStages) & 1;
-      bool r = __all_sync(0xffffffffu, mbar_wait(&dq_staged[2 * s], par, ctl, kWaitBwdLoad)) &&
-               __all_sync(0xffffffffu, mbar_wait(&dq_staged[2 * s + 1], par, ctl, kWaitBwdLoad));
-      if (r && lane == 0) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int n = min(64, st_nrow[s] - 64 * h);
-          if (n > 0)
-            bulk_reduce_add_f32(p.dq_acc + (st_row[s] + 64 * h) * D,
-                                smem + (h ? C::kOffDO : C::kOffQ) + s * C::kTileBytes, (uint32_t)n * D * 4);
-        }
-        bulk_commit();
-        bulk_wait_read_all();
-      }
-      __syncwarp();
-      return r;
-    };
     for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units; ++rnd) {
       const int u = snake_unit(rnd);
       if (u >= p.num_units) continue;
-      const BwdUnit w = decode_bwd(p, u);
+      const BwdUnit w = decode_dkdv(p, u);
       const size_t head = (size_t)w.bh * p.N;
       ok = __all_sync(0xffffffffu, mbar_wait(kv_empty, (kc & 1) ^ 1, ctl, kWaitBwdLoad));
       if (!ok) break;
       if (lane == 0) {
         mbar_arrive_expect_tx(kv_full, 2 * C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c) {
-          tma_load_3d(smem + C::kOffK + c * C::kChunkBytes, &tm_k, kv_full, c * 64, w.j * kTileN, w.bh);
-          tma_load_3d(smem + C::kOffV + c * C::kChunkBytes, &tm_v, kv_full, c * 64, w.j * kTileN, w.bh);
+          tma_load_3d(smem + C::kOffK + c * C::kChunkBytes, &tm_k, kv_full, c * 64, w.t * kTileN, w.bh);
+          tma_load_3d(smem + C::kOffV + c * C::kChunkBytes, &tm_v, kv_full, c * 64, w.t * kTileN, w.bh);
         }
       }
       ++kc;
-      for (int ii = 0; ok && ii < w.nq; ++ii) {
-        const uint32_t st = qc % C::kStages;
-        if constexpr (C::kDqT) {
-          // The stage's previous step has finished with Q/dO and its dQ is
-          // staged there: reduce it, then refill.
-          if (qc >= (uint32_t)C::kStages) ok = reduce_step(qc - C::kStages);
-        } else {
-          ok = __all_sync(0xffffffffu,
-                          mbar_wait(&qdo_empty[st], ((qc / C::kStages) & 1) ^ 1, ctl, kWaitBwdLoad));
-        }
+      for (int ii = 0; ok && ii < w.count; ++ii, ++qc) {
+        const int row = (w.first + ii) * kTileM;
+        // Q_i with L_i (log2 units; rows past N get +inf so their weights
+        // vanish).  The values are written before the arrive that completes
+        // the stage together with the copy.
+        const uint32_t sq = qc % C::kQStages;
+        ok = __all_sync(0xffffffffu, mbar_wait(&q_empty[sq], ((qc / C::kQStages) & 1) ^ 1, ctl, kWaitBwdLoad));
         if (!ok) break;
-        const int row = (w.i0 + ii) * kTileM;
-        st_row[st] = head + row;
-        st_nrow[st] = p.N - row;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&qdo_full[st], 2 * C::kTileBytes);
-          for (int c = 0; c < C::kChunks; ++c) {
-            tma_load_3d(smem + C::kOffQ + st * C::kTileBytes + c * C::kChunkBytes, &tm_q, &qdo_full[st], c * 64,
-                        row, w.bh);
-            tma_load_3d(smem + C::kOffDO + st * C::kTileBytes + c * C::kChunkBytes, &tm_do, &qdo_full[st],
-                        c * 64, row, w.bh);
-          }
-        }
-        // L_i (log2 units) and D_i of the tile's 128 queries; rows past N get
-        // L = +inf so their weights vanish.
-        float4 l4, d4;
-        float* lp = &l4.x;
-        float* dp = &d4.x;
+        {
+          float4 l4;
+          float* lp = &l4.x;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int qr = row + 4 * lane + e;
-          lp[e] = qr < p.N ? p.lse[head + qr] * 1.4426950408889634f : INFINITY;
-          dp[e] = qr < p.N ? p.dvec[head + qr] : 0.f;
+          for (int e = 0; e < 4; ++e) {
+            const int qr = row + 4 * lane + e;
+            lp[e] = qr < p.N ? p.lse[head + qr] * 1.4426950408889634f : INFINITY;
+          }
+          reinterpret_cast<float4*>(sLse + sq * 128)[lane] = l4;
         }
-        reinterpret_cast<float4*>(sLse + st * 128)[lane] = l4;
-        reinterpret_cast<float4*>(sDv + st * 128)[lane] = d4;
-        mbar_arrive(&stat_full[st]);
-        ++qc;
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&q_full[sq], C::kTileBytes);
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_3d(smem + C::kOffQ + sq * C::kTileBytes + c * C::kChunkBytes, &tm_q, &q_full[sq], c * 64,
+                        row, w.bh);
+        }
+        // dO_i with D_i.
+        const uint32_t sd = qc % C::kDoStages;
+        ok = __all_sync(0xffffffffu, mbar_wait(&do_empty[sd], ((qc / C::kDoStages) & 1) ^ 1, ctl, kWaitBwdLoad));
+        if (!ok) break;
+        {
+          float4 d4;
+          float* dp = &d4.x;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int qr = row + 4 * lane + e;
+            dp[e] = qr < p.N ? p.dvec[head + qr] : 0.f;
+          }
+          reinterpret_cast<float4*>(sDv + sd * 128)[lane] = d4;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&do_full[sd], C::kTileBytes);
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_3d(smem + C::kOffDO + sd * C::kTileBytes + c * C::kChunkBytes, &tm_do, &do_full[sd],
+                        c * 64, row, w.bh);
+        }
       }
     }
-    if constexpr (C::kDqT) {
-      // The last steps' dQ.
-      const uint32_t first = qc > (uint32_t)C::kStages ? qc - C::kStages : 0u;
-      for (uint32_t k = first; ok && k < qc; ++k) ok = reduce_step(k);
-    }
     if (lane == 0) {
-      bulk_wait_all();  // every reduction has landed
+      // Every copy this warp issued has landed before the CTA exits.
       if (kc > 0) mbar_wait(kv_full, (kc - 1) & 1, ctl, kWaitDrain);
-      const uint32_t first = qc > (uint32_t)C::kStages ? qc - C::kStages : 0u;
-      for (uint32_t pos = first; pos < qc; ++pos)
-        mbar_wait(&qdo_full[pos % C::kStages], (pos / C::kStages) & 1, ctl, kWaitDrain);
+      for (uint32_t pos = qc > (uint32_t)C::kQStages ? qc - C::kQStages : 0u; pos < qc; ++pos)
+        mbar_wait(&q_full[pos % C::kQStages], (pos / C::kQStages) & 1, ctl, kWaitDrain);
+      for (uint32_t pos = qc > (uint32_t)C::kDoStages ? qc - C::kDoStages : 0u; pos < qc; ++pos)
+        mbar_wait(&do_full[pos % C::kDoStages], (pos / C::kDoStages) & 1, ctl, kWaitDrain);
     }
     __syncwarp();
   } else if (warp == 8) {
     // ---------------------------------------------------------- MMA issuer
+    reg_dealloc<R::kRegsCtl>();
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16(kTileM, kTileM, false, false);  // S^T, dP^T
       constexpr uint32_t id_kv = idesc_bf16(kTileM, D, false, true);       // dV, dK
-      constexpr uint32_t id_dq = idesc_bf16(kTileM, 64, true, true);       // dQ^T halves / dQ
       const uint32_t sk = smem_u32(smem + C::kOffK);
       const uint32_t sv = smem_u32(smem + C::kOffV);
-      const uint32_t sds = smem_u32(smem + C::kOffDS);
-      uint32_t kc = 0, qc = 0, pc = 0, dqc = 0, uc = 0;
+      uint32_t kc = 0, qc = 0, sn = 0, pc = 0, uc = 0;
       bool ok = true;
+      // S^T of the step at position `pos` into S, once the previous S^T has
+      // been read out.
+      auto issue_s = [&](uint32_t pos) -> bool {
+        const uint32_t sq = pos % C::kQStages;
+        if (!mbar_wait(&q_full[sq], (pos / C::kQStages) & 1, ctl, kWaitBwdMma)) return false;
+        if (sn > 0 && !mbar_wait(s_free, (sn - 1) & 1, ctl, kWaitBwdMma)) return false;
+        tc_fence_after();
+        const uint32_t sq_addr = smem_u32(smem + C::kOffQ + sq * C::kTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
+          mma_ss(tmem + C::kColS, sdesc_sw128(sk + off, 16, 1024), sdesc_sw128(sq_addr + off, 16, 1024), id_s,
+                 kk > 0 ? 1u : 0u);
+        }
+        mma_commit(s_full);
+        ++sn;
+        return true;
+      };
       for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units; ++rnd) {
         const int u = snake_unit(rnd);
         if (u >= p.num_units) continue;
-        const BwdUnit w = decode_bwd(p, u);
+        const BwdUnit w = decode_dkdv(p, u);
         ok = mbar_wait(kv_full, kc & 1, ctl, kWaitBwdMma);
         ++kc;
         if (!ok) break;
         tc_fence_after();
-        for (int ii = 0; ii < w.nq; ++ii) {
-          const uint32_t st = qc % C::kStages;
-          ok = mbar_wait(&qdo_full[st], (qc / C::kStages) & 1, ctl, kWaitBwdMma);
+        ok = issue_s(qc);
+        for (int ii = 0; ok && ii < w.count; ++ii, ++qc) {
+          const uint32_t sq = qc % C::kQStages;
+          const uint32_t sd = qc % C::kDoStages;
+          const uint32_t sq_addr = smem_u32(smem + C::kOffQ + sq * C::kTileBytes);
+          const uint32_t sdo = smem_u32(smem + C::kOffDO + sd * C::kTileBytes);
+          // dP^T into B; the previous step's P^T / dS^T there were consumed
+          // by products issued earlier (the tensor pipe runs in issue order).
+          ok = mbar_wait(&do_full[sd], (qc / C::kDoStages) & 1, ctl, kWaitBwdMma);
           if (!ok) break;
-          const uint32_t sq = smem_u32(smem + C::kOffQ + st * C::kTileBytes);
-          const uint32_t sdo = smem_u32(smem + C::kOffDO + st * C::kTileBytes);
-          if (C::kDqT && dqc > 0) {
-            // S^T overwrites the columns of the previous dQ^T's first half.
-            ok = mbar_wait(&dq_empty[0], (dqc - 1) & 1, ctl, kWaitBwdMma);
-            if (!ok) break;
-          }
           tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
-            mma_ss(tmem + C::kColA, sdesc_sw128(sk + off, 16, 1024), sdesc_sw128(sq + off, 16, 1024), id_s,
-                   kk > 0 ? 1u : 0u);
-          }
-          if (C::kDqT && dqc > 0) {
-            ok = mbar_wait(&dq_empty[1], (dqc - 1) & 1, ctl, kWaitBwdMma);
-            if (!ok) break;
-            tc_fence_after();
-          }
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
             mma_ss(tmem + C::kColB, sdesc_sw128(sv + off, 16, 1024), sdesc_sw128(sdo + off, 16, 1024), id_s,
                    kk > 0 ? 1u : 0u);
           }
-          mma_commit(s_full);
+          mma_commit(dp_full);
+          // K_j and V_j are read by S^T and dP^T only: after the unit's last
+          // dP^T they can take the next unit's tiles.
+          if (ii + 1 == w.count) mma_commit(kv_empty);
+          // The next step's S^T, while the element-wise warps work on this one.
+          if (ii + 1 < w.count) {
+            ok = issue_s(qc + 1);
+            if (!ok) break;
+          }
           ok = mbar_wait(p_ready, pc & 1, ctl, kWaitBwdMma);
           ++pc;
           if (!ok) break;
@@ -362,49 +382,23 @@ __global__ void __launch_bounds__(320, 1)
             ok = mbar_wait(dkv_empty, (uc - 1) & 1, ctl, kWaitBwdMma);
             if (!ok) break;
           }
-          if (!C::kDqT && dqc > 0) {
-            ok = mbar_wait(&dq_empty[0], (dqc - 1) & 1, ctl, kWaitBwdMma);
-            if (!ok) break;
-          }
           tc_fence_after();
+          // dK += dS^T Q_i (A = dS^T from TMEM, B = Q_i read MN-major), then
+          // Q_i's stage is free.
 #pragma unroll
-          for (int kk = 0; kk < kTileM / 16; ++kk) {
-            const uint32_t acc = (ii > 0 || kk > 0) ? 1u : 0u;
-            mma_ts(tmem + C::kColDV, tmem + C::kColA + packed_col(kk),
-                   sdesc_sw128(sdo + kk * 2048, C::kChunkBytes, 1024), id_kv, acc);
-          }
+          for (int kk = 0; kk < kTileM / 16; ++kk)
+            mma_ts(tmem + C::kColDK, tmem + C::kColB + packed_col(kk, true),
+                   sdesc_sw128(sq_addr + kk * 2048, C::kChunkBytes, 1024), id_kv, (ii > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&q_empty[sq]);
+          // dV += P^T dO_i.
 #pragma unroll
-          for (int kk = 0; kk < kTileM / 16; ++kk) {
-            const uint32_t acc = (ii > 0 || kk > 0) ? 1u : 0u;
-            mma_ts(tmem + C::kColDK, tmem + C::kColB + packed_col(kk),
-                   sdesc_sw128(sq + kk * 2048, C::kChunkBytes, 1024), id_kv, acc);
-          }
-          if constexpr (C::kDqT) {
-            // dQ^T[:, 64h : 64h+64] = K^T dS^T[:, 64h : 64h+64]: A = K^T (K
-            // tile read MN-major), B = the 64-query block h of dS^T.
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-              for (int kk = 0; kk < kTileN / 16; ++kk)
-                mma_ss(tmem + (h ? C::kColB : C::kColA) + C::kColDQ,
-                       sdesc_sw128(sk + kk * 2048, C::kChunkBytes, 1024),
-                       sdesc_sw128(sds + h * C::kChunkBytes + kk * 2048, C::kChunkBytes, 1024), id_dq,
-                       kk > 0 ? 1u : 0u);
-          } else {
-            // dQ = dS K: A = dS (the dS^T tile read MN-major), B = K.
-#pragma unroll
-            for (int kk = 0; kk < kTileN / 16; ++kk)
-              mma_ss(tmem + C::kColDQ, sdesc_sw128(sds + kk * 2048, C::kChunkBytes, 1024),
-                     sdesc_sw128(sk + kk * 2048, C::kChunkBytes, 1024), id_dq, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(dq_full);
-          ++dqc;
-          if (!C::kDqT) mma_commit(&qdo_empty[st]);
-          ++qc;
+          for (int kk = 0; kk < kTileM / 16; ++kk)
+            mma_ts(tmem + C::kColDV, tmem + C::kColB + packed_col(kk, false),
+                   sdesc_sw128(sdo + kk * 2048, C::kChunkBytes, 1024), id_kv, (ii > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&do_empty[sd]);
         }
         if (!ok) break;
         mma_commit(dkv_full);
-        mma_commit(kv_empty);
         ++uc;
       }
       mma_commit(drain);
@@ -412,107 +406,92 @@ __global__ void __launch_bounds__(320, 1)
     }
     __syncwarp();
   } else if (warp < 8) {
-    // ------------------------------ P^T, dS^T, dQ read-out and dK/dV output
+    // ------------------------------------------ P^T, dS^T and dK/dV output
+    reg_alloc<R::kRegsMath>();
     const int g = warp & 3;    // TMEM lane quarter
     const int hc = warp >> 2;  // query-column half
     const uint32_t lane_off = (uint32_t)(32 * g) << 16;
+    const uint32_t tS = tmem + lane_off + C::kColS + 64 * hc;
+    const uint32_t tB = tmem + lane_off + C::kColB + 64 * hc;
     const int r = 32 * g + lane;  // key row within the tile
     const float sl2 = p.scale_log2;
-    uint8_t* sds = smem + C::kOffDS;
     uint32_t sc = 0, uc = 0, qc = 0, dc = 0;
     bool ok = true;
+    uint32_t pv[64];  // P^T of the current step (fp32 bits), 64 query columns
+    uint32_t pk[32];  // the same, packed to bf16 pairs for the dV product
+    // Wait for S^T of the step at position `pos`, read this warp's 64
+    // columns, release them and compute P^T.
+    auto load_p = [&](uint32_t pos, int q0, int kr) -> bool {
+      const uint32_t sq = pos % C::kQStages;
+      if (!__all_sync(0xffffffffu, mbar_wait(&q_full[sq], (pos / C::kQStages) & 1, ctl, kWaitBwdSoftmax)))
+        return false;
+      if (!__all_sync(0xffffffffu, mbar_wait(s_full, sc & 1, ctl, kWaitBwdSoftmax))) return false;
+      ++sc;
+      tc_fence_after();
+      tmem_ld32(tS, pv);
+      tmem_ld32(tS + 32, pv + 32);
+      tmem_ld_wait<64>(pv);
+      tc_fence_before();
+      mbar_arrive_warp(s_free);
+      const float* bl = sLse + sq * 128 + 64 * hc;
+      const int qf = q0 + 64 * hc;
+      if ((kr >= p.N) || (p.causal && kr > qf))
+        p64_colL<true>(pv, bl, sl2, kr, qf, kr >= p.N, p.causal != 0);
+      else
+        p64_colL<false>(pv, bl, sl2, kr, qf, false, false);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(__uint_as_float(pv[2 * e]), __uint_as_float(pv[2 * e + 1]));
+      return true;
+    };
     for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units; ++rnd) {
       const int u = snake_unit(rnd);
       if (u >= p.num_units) continue;
-      const BwdUnit w = decode_bwd(p, u);
-      const int kr = w.j * kTileN + r;  // key index
+      const BwdUnit w = decode_dkdv(p, u);
+      const int kr = w.t * kTileN + r;  // key index
       const size_t head = (size_t)w.bh * p.N;
-      for (int ii = 0; ii < w.nq; ++ii, ++qc) {
-        const int q0 = (w.i0 + ii) * kTileM;
-        const uint32_t st = qc % C::kStages;
-        ok = __all_sync(0xffffffffu,
-                        mbar_wait(&stat_full[st], (qc / C::kStages) & 1, ctl, kWaitBwdSoftmax));
-        if (!ok) break;
-        ok = __all_sync(0xffffffffu, mbar_wait(s_full, sc & 1, ctl, kWaitBwdSoftmax));
-        ++sc;
-        if (!ok) break;
-        tc_fence_after();
-        const float* bl = sLse + st * 128;
-        const float* bd = sDv + st * 128;
-        const bool mask = (kr >= p.N) || (p.causal && kr > q0);
-        // Half 0 handles query chunks 0, 1; half 1 handles 3, 2 (in that
-        // order), so each packed store lands on S^T / dP^T columns this warp
-        // has already read.  Two loads (64 registers) per chunk: a load's
-        // registers must not be live across spills before its wait.
-#pragma unroll 1
-        for (int cc = 0; cc < 2; ++cc) {
-          const int c = hc ? 3 - cc : cc;
-          uint32_t s[1][32], dpv[1][32];
-          tmem_ld32(tmem + lane_off + C::kColA + 32 * c, s[0]);
-          tmem_ld32(tmem + lane_off + C::kColB + 32 * c, dpv[0]);
-          tmem_ld_wait<32>(s[0]);
-          tmem_ld_wait<32>(dpv[0]);
-          uint32_t pp[16], dd[16];
-          if (mask)
-            bwd_chunk<true>(s[0], dpv[0], bl + 32 * c, bd + 32 * c, sl2, kr, q0 + 32 * c, kr >= p.N, p.causal != 0,
-                            pp, dd);
-          else
-            bwd_chunk<false>(s[0], dpv[0], bl + 32 * c, bd + 32 * c, sl2, kr, q0 + 32 * c, false, false, pp, dd);
-          const uint32_t dst = c < 2 ? 16u * c : 96u + 16u * (c - 2);
-          tmem_st16(tmem + lane_off + C::kColA + dst, pp);
-          tmem_st16(tmem + lane_off + C::kColB + dst, dd);
-          // dS^T row r, query columns [32c, 32c+32): 64 bytes of the
-          // 128-byte-swizzled [key row][query] tile the dQ MMA reads.
-          uint8_t* rowp = sds + (c / 2) * C::kChunkBytes + r * 128;
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const int unit = (c % 2) * 4 + q4;
-            *reinterpret_cast<uint4*>(rowp + ((unit ^ (r & 7)) << 4)) =
-                make_uint4(dd[4 * q4], dd[4 * q4 + 1], dd[4 * q4 + 2], dd[4 * q4 + 3]);
-          }
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        fence_proxy_async_smem();
-        mbar_arrive(p_ready);
-        // dQ of this step: read this warp's share out of TMEM, release it,
-        // then add it to the fp32 accumulator.
-        ok = __all_sync(0xffffffffu, mbar_wait(dq_full, dc & 1, ctl, kWaitBwdDq));
+      ok = load_p(qc, w.first * kTileM, kr);
+      for (int ii = 0; ok && ii < w.count; ++ii, ++qc) {
+        const int q0 = (w.first + ii) * kTileM;
+        const uint32_t sd = qc % C::kDoStages;
+        // dS^T = P^T * (dP^T - D); P^T and dS^T packed over this warp's dP^T
+        // columns.
+        ok = __all_sync(0xffffffffu, mbar_wait(&do_full[sd], (qc / C::kDoStages) & 1, ctl, kWaitBwdSoftmax));
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(dp_full, dc & 1, ctl, kWaitBwdSoftmax));
         ++dc;
         if (!ok) break;
         tc_fence_after();
-        if constexpr (C::kDqT) {
-          // Lane = head-dim column dd, 64 query rows of half hc.
-          const int dd = 32 * g + lane;
-          uint32_t v[64];
-          const uint32_t base = tmem + lane_off + (hc ? C::kColB : C::kColA) + C::kColDQ;
-          tmem_ld32(base, v);
-          tmem_ld32(base + 32, v + 32);
-          tmem_ld_wait<64>(v);
-          tc_fence_before();
-          mbar_arrive(&dq_empty[hc]);
-          // Row-major [query][head dim] into the stage's Q (half 0) or dO
-          // (half 1) buffer: 32 lanes write one 128-byte run per query.
-          float* buf = reinterpret_cast<float*>(smem + (hc ? C::kOffDO : C::kOffQ) + st * C::kTileBytes);
+        {
+          uint32_t dpv[64];
+          tmem_ld32(tB, dpv);
+          tmem_ld32(tB + 32, dpv + 32);
+          tmem_ld_wait<64>(dpv);
+          const float* bd = sDv + sd * 128 + 64 * hc;
+          uint32_t dk[32];
 #pragma unroll
-          for (int qq = 0; qq < 64; ++qq) buf[qq * D + dd] = __uint_as_float(v[qq]);
-          fence_proxy_async_smem();
-          mbar_arrive(&dq_staged[2 * st + hc]);
-        } else {
-          // Lane = query row; head-dim columns [32 hc, 32 hc + 32).
-          const int qr = q0 + r;
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_off + C::kColDQ + 32 * hc, v);
-          tmem_ld_wait<32>(v);
-          tc_fence_before();
-          mbar_arrive(&dq_empty[0]);
-          if (qr < p.N) {
-            float4* dst = reinterpret_cast<float4*>(p.dq_acc + (head + qr) * D + 32 * hc);
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-              atomicAdd(dst + c, make_float4(__uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
-                                             __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3])));
+          for (int e4 = 0; e4 < 16; ++e4) {
+            const float4 d4 = reinterpret_cast<const float4*>(bd)[e4];
+            const float2 p01 = make_float2(__uint_as_float(pv[4 * e4]), __uint_as_float(pv[4 * e4 + 1]));
+            const float2 p23 = make_float2(__uint_as_float(pv[4 * e4 + 2]), __uint_as_float(pv[4 * e4 + 3]));
+            const float2 g01 = __fadd2_rn(
+                make_float2(__uint_as_float(dpv[4 * e4]), __uint_as_float(dpv[4 * e4 + 1])), make_float2(-d4.x, -d4.y));
+            const float2 g23 = __fadd2_rn(
+                make_float2(__uint_as_float(dpv[4 * e4 + 2]), __uint_as_float(dpv[4 * e4 + 3])),
+                make_float2(-d4.z, -d4.w));
+            const float2 ds01 = __fmul2_rn(p01, g01);
+            const float2 ds23 = __fmul2_rn(p23, g23);
+            dk[2 * e4] = pack_bf16(ds01.x, ds01.y);
+            dk[2 * e4 + 1] = pack_bf16(ds23.x, ds23.y);
           }
+          tmem_st32(tB, pk);
+          tmem_st32(tB + 32, dk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive_warp(p_ready);
+        // The next step's P^T while the tensor core runs dK and dV.
+        if (ii + 1 < w.count) {
+          ok = load_p(qc + 1, q0 + kTileM, kr);
+          if (!ok) break;
         }
       }
       if (!ok) break;
@@ -549,8 +528,10 @@ __global__ void __launch_bounds__(320, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(dkv_empty);
+      mbar_arrive_warp(dkv_empty);
     }
+  } else {
+    reg_dealloc<R::kRegsCtl>();
   }
 
   tc_fence_before();
@@ -561,12 +542,341 @@ __global__ void __launch_bounds__(320, 1)
   }
 }
 
-// D_i = sum_c dO_ic * O_ic; also zeroes row i of the dQ accumulator.
+// --------------------------------------------------------------------- dQ
+
+template <int D>
+struct DqCfg {
+  static constexpr int kChunks = D / 64;
+  static constexpr int kChunkBytes = kTileM * 128;
+  static constexpr int kTileBytes = kTileM * D * 2;
+  static constexpr int kKStages = 3;  // S two steps ahead needs K early
+  static constexpr int kVStages = 2;
+  static constexpr int kThreads = 384;
+  static constexpr uint32_t kColS0 = 0;    // S of even steps, then their dS packed
+  static constexpr uint32_t kColS1 = 128;  // S of odd steps, then their dS packed
+  static constexpr uint32_t kColDP = 256;  // dP
+  static constexpr uint32_t kColDQ = 384;  // dQ accumulator (D columns)
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffDO = kTileBytes;
+  static constexpr int kOffK = 2 * kTileBytes;
+  static constexpr int kOffV = kOffK + kKStages * kTileBytes;
+  static constexpr int kOffBar = kOffV + kVStages * kTileBytes;
+  static constexpr int kNumBars = 2 + 2 * kKStages + 2 * kVStages + 8;
+  static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16;
+  static_assert(kSmemBytes <= 232448, "shared memory");
+};
+
+template <int D>
+__global__ void __launch_bounds__(384, 1)
+    fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                     const BwdParams p) {
+  using C = DqCfg<D>;
+  using R = BwdRegs;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if ((smem_u32(smem) & 1023u) != 0u) {
+    if (threadIdx.x == 0) atomicCAS(p.status, 0u, (unsigned int)FA_ERR_CUDA);
+    return;
+  }
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* qdo_full = bars;
+  uint64_t* qdo_empty = bars + 1;
+  uint64_t* k_full = bars + 2;  // [kKStages]
+  uint64_t* k_empty = k_full + C::kKStages;
+  uint64_t* v_full = k_empty + C::kKStages;  // [kVStages]
+  uint64_t* v_empty = v_full + C::kVStages;
+  uint64_t* s_full = v_empty + C::kVStages;  // [2]: S of even / odd steps in TMEM
+  uint64_t* dp_full = s_full + 2;            // dP in TMEM
+  uint64_t* dp_free = dp_full + 1;           // dP read by all element-wise warps
+  uint64_t* p_ready = dp_free + 1;           // dS packed in TMEM
+  uint64_t* dq_full = p_ready + 1;           // the unit's dQ complete
+  uint64_t* dq_empty = dq_full + 1;          // ... and read out
+  uint64_t* drain = dq_empty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    mbar_init(qdo_full, 1);
+    mbar_init(qdo_empty, 1);
+    for (int s = 0; s < C::kKStages; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < C::kVStages; ++s) {
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+    }
+    mbar_init(&s_full[0], 1);
+    mbar_init(&s_full[1], 1);
+    mbar_init(dp_full, 1);
+    mbar_init(dp_free, 8);
+    mbar_init(p_ready, 8);
+    mbar_init(dq_full, 1);
+    mbar_init(dq_empty, 8);
+    mbar_init(drain, 1);
+    fence_barrier_init();
+  }
+  if (warp == 8) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 9 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_do);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl ctl{p.status, p.timeout_ns};
+
+  if (warp == 9) {
+    // ------------------------------------------------------------ producer
+    reg_dealloc<R::kRegsCtl>();
+    if (lane == 0) {
+      uint32_t uc = 0, kc = 0;
+      bool ok = true;
+      for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units; ++rnd) {
+        const int u = snake_unit(rnd);
+        if (u >= p.num_units) continue;
+        const BwdUnit w = decode_dq(p, u);
+        ok = mbar_wait(qdo_empty, (uc & 1) ^ 1, ctl, kWaitBwdLoad);
+        if (!ok) break;
+        mbar_arrive_expect_tx(qdo_full, 2 * C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c) {
+          tma_load_3d(smem + C::kOffQ + c * C::kChunkBytes, &tm_q, qdo_full, c * 64, w.t * kTileM, w.bh);
+          tma_load_3d(smem + C::kOffDO + c * C::kChunkBytes, &tm_do, qdo_full, c * 64, w.t * kTileM, w.bh);
+        }
+        ++uc;
+        for (int jj = 0; ok && jj < w.count; ++jj, ++kc) {
+          const int key0 = (w.first + jj) * kTileN;
+          const uint32_t sk = kc % C::kKStages;
+          ok = mbar_wait(&k_empty[sk], ((kc / C::kKStages) & 1) ^ 1, ctl, kWaitBwdLoad);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&k_full[sk], C::kTileBytes);
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_3d(smem + C::kOffK + sk * C::kTileBytes + c * C::kChunkBytes, &tm_k, &k_full[sk], c * 64, key0,
+                        w.bh);
+          const uint32_t sv = kc % C::kVStages;
+          ok = mbar_wait(&v_empty[sv], ((kc / C::kVStages) & 1) ^ 1, ctl, kWaitBwdLoad);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&v_full[sv], C::kTileBytes);
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_3d(smem + C::kOffV + sv * C::kTileBytes + c * C::kChunkBytes, &tm_v, &v_full[sv], c * 64, key0,
+                        w.bh);
+        }
+      }
+      // Every copy this thread issued has landed before the CTA exits.
+      if (uc > 0) mbar_wait(qdo_full, (uc - 1) & 1, ctl, kWaitDrain);
+      for (uint32_t pos = kc > (uint32_t)C::kKStages ? kc - C::kKStages : 0u; pos < kc; ++pos)
+        mbar_wait(&k_full[pos % C::kKStages], (pos / C::kKStages) & 1, ctl, kWaitDrain);
+      for (uint32_t pos = kc > (uint32_t)C::kVStages ? kc - C::kVStages : 0u; pos < kc; ++pos)
+        mbar_wait(&v_full[pos % C::kVStages], (pos / C::kVStages) & 1, ctl, kWaitDrain);
+    }
+    __syncwarp();
+  } else if (warp == 8) {
+    // ---------------------------------------------------------- MMA issuer
+    reg_dealloc<R::kRegsCtl>();
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16(kTileM, kTileN, false, false);  // S, dP
+      constexpr uint32_t id_dq = idesc_bf16(kTileM, D, false, true);       // dQ += dS K
+      const uint32_t sq = smem_u32(smem + C::kOffQ);
+      const uint32_t sdo = smem_u32(smem + C::kOffDO);
+      uint32_t uc = 0, kc = 0, dn = 0, pc = 0;
+      bool ok = true;
+      // S of the step at position `pos` into S buffer (pos & 1).  The buffer
+      // last held the dS of step pos - 2, read by a dQ product issued
+      // earlier; its S was read before that dS was written.
+      auto issue_s = [&](uint32_t pos) -> bool {
+        const uint32_t sk = pos % C::kKStages;
+        if (!mbar_wait(&k_full[sk], (pos / C::kKStages) & 1, ctl, kWaitBwdMma)) return false;
+        tc_fence_after();
+        const uint32_t sk_addr = smem_u32(smem + C::kOffK + sk * C::kTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
+          mma_ss(tmem + ((pos & 1) ? C::kColS1 : C::kColS0), sdesc_sw128(sq + off, 16, 1024),
+                 sdesc_sw128(sk_addr + off, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&s_full[pos & 1]);
+        return true;
+      };
+      // dP of the step at position `pos`, once the previous dP was read out.
+      // Q_i and dO_i are read by S and dP only: after the unit's last dP
+      // (`last`) they can take the next unit's tiles.
+      auto issue_dp = [&](uint32_t pos, bool last) -> bool {
+        const uint32_t sv = pos % C::kVStages;
+        if (!mbar_wait(&v_full[sv], (pos / C::kVStages) & 1, ctl, kWaitBwdMma)) return false;
+        if (dn > 0 && !mbar_wait(dp_free, (dn - 1) & 1, ctl, kWaitBwdMma)) return false;
+        tc_fence_after();
+        const uint32_t sv_addr = smem_u32(smem + C::kOffV + sv * C::kTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
+          mma_ss(tmem + C::kColDP, sdesc_sw128(sdo + off, 16, 1024), sdesc_sw128(sv_addr + off, 16, 1024), id_s,
+                 kk > 0 ? 1u : 0u);
+        }
+        mma_commit(dp_full);
+        mma_commit(&v_empty[sv]);
+        if (last) mma_commit(qdo_empty);
+        ++dn;
+        return true;
+      };
+      for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units; ++rnd) {
+        const int u = snake_unit(rnd);
+        if (u >= p.num_units) continue;
+        const BwdUnit w = decode_dq(p, u);
+        ok = mbar_wait(qdo_full, uc & 1, ctl, kWaitBwdMma);
+        if (!ok) break;
+        tc_fence_after();
+        ok = issue_s(kc);
+        if (ok && w.count > 1) ok = issue_s(kc + 1);
+        if (ok) ok = issue_dp(kc, w.count == 1);
+        for (int jj = 0; ok && jj < w.count; ++jj, ++kc) {
+          // The next step's dP as soon as this one has been read out.
+          if (jj + 1 < w.count) {
+            ok = issue_dp(kc + 1, jj + 2 == w.count);
+            if (!ok) break;
+          }
+          ok = mbar_wait(p_ready, pc & 1, ctl, kWaitBwdMma);
+          ++pc;
+          if (!ok) break;
+          if (jj == 0 && uc > 0) {
+            // The previous unit's dQ has been read out of TMEM.
+            ok = mbar_wait(dq_empty, (uc - 1) & 1, ctl, kWaitBwdMma);
+            if (!ok) break;
+          }
+          tc_fence_after();
+          // dQ += dS K_j: A = dS (bf16 pairs in the step's S buffer), B = K_j
+          // read MN-major (N = head dim, K = keys).
+          const uint32_t sk = kc % C::kKStages;
+          const uint32_t sk_addr = smem_u32(smem + C::kOffK + sk * C::kTileBytes);
+          const uint32_t ds_col = (kc & 1) ? C::kColS1 : C::kColS0;
+#pragma unroll
+          for (int kk = 0; kk < kTileN / 16; ++kk)
+            mma_ts(tmem + C::kColDQ, tmem + ds_col + packed_col(kk, false),
+                   sdesc_sw128(sk_addr + kk * 2048, C::kChunkBytes, 1024), id_dq, (jj > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&k_empty[sk]);
+          // S two steps ahead, into the buffer this dQ product reads from.
+          if (jj + 2 < w.count) {
+            ok = issue_s(kc + 2);
+            if (!ok) break;
+          }
+        }
+        if (!ok) break;
+        mma_commit(dq_full);
+        ++uc;
+      }
+      mma_commit(drain);
+      mbar_wait(drain, 0, ctl, kWaitDrain);
+    }
+    __syncwarp();
+  } else if (warp < 8) {
+    // --------------------------------------------------- P, dS and dQ output
+    reg_alloc<R::kRegsMath>();
+    const int g = warp & 3;    // TMEM lane quarter: queries [32 g, 32 g + 32)
+    const int hc = warp >> 2;  // key-column half
+    const uint32_t lane_off = (uint32_t)(32 * g) << 16;
+    const float sl2 = p.scale_log2;
+    uint32_t uc = 0, kc = 0, dc = 0;
+    bool ok = true;
+    for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units; ++rnd) {
+      const int u = snake_unit(rnd);
+      if (u >= p.num_units) continue;
+      const BwdUnit w = decode_dq(p, u);
+      const size_t head = (size_t)w.bh * p.N;
+      const int q = w.t * kTileM + 32 * g + lane;  // query row
+      const float L = q < p.N ? p.lse[head + q] * 1.4426950408889634f : INFINITY;
+      const float Dq = q < p.N ? p.dvec[head + q] : 0.f;
+      const int q_lo = w.t * kTileM + 32 * g;  // first query of this warp
+      for (int jj = 0; ok && jj < w.count; ++jj, ++kc) {
+        const uint32_t tS = tmem + lane_off + ((kc & 1) ? C::kColS1 : C::kColS0) + 64 * hc;
+        const int k_first = (w.first + jj) * kTileN + 64 * hc;
+        ok = __all_sync(0xffffffffu, mbar_wait(&s_full[kc & 1], (kc >> 1) & 1, ctl, kWaitBwdSoftmax));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t pv[64];
+        tmem_ld32(tS, pv);
+        tmem_ld32(tS + 32, pv + 32);
+        tmem_ld_wait<64>(pv);
+        if (k_first + 63 >= p.N || (p.causal && k_first + 63 > q_lo))
+          p64_rowL<true>(pv, L, sl2, q, k_first, p.N, p.causal != 0);
+        else
+          p64_rowL<false>(pv, L, sl2, q, k_first, p.N, false);
+        ok = __all_sync(0xffffffffu, mbar_wait(dp_full, dc & 1, ctl, kWaitBwdSoftmax));
+        ++dc;
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t dk[32];
+        {
+          uint32_t dpv[64];
+          tmem_ld32(tmem + lane_off + C::kColDP + 64 * hc, dpv);
+          tmem_ld32(tmem + lane_off + C::kColDP + 64 * hc + 32, dpv + 32);
+          tmem_ld_wait<64>(dpv);
+          tc_fence_before();
+          mbar_arrive_warp(dp_free);
+          const float2 dv2 = make_float2(-Dq, -Dq);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float2 g2 =
+                __fadd2_rn(make_float2(__uint_as_float(dpv[2 * e]), __uint_as_float(dpv[2 * e + 1])), dv2);
+            const float2 ds =
+                __fmul2_rn(make_float2(__uint_as_float(pv[2 * e]), __uint_as_float(pv[2 * e + 1])), g2);
+            dk[e] = pack_bf16(ds.x, ds.y);
+          }
+        }
+        // dS as bf16 pairs over this warp's S columns (already read).
+        tmem_st32(tS, dk);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive_warp(p_ready);
+      }
+      if (!ok) break;
+      // dQ_i = scale * sum dS K of this unit: lane = query row, this warp
+      // writes head-dim columns [D/2 hc, D/2 hc + D/2).
+      ok = __all_sync(0xffffffffu, mbar_wait(dq_full, uc & 1, ctl, kWaitBwdDq));
+      ++uc;
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t v[D / 2];
+      tmem_ld32(tmem + lane_off + C::kColDQ + (D / 2) * hc, v);
+      if constexpr (D == 128) tmem_ld32(tmem + lane_off + C::kColDQ + (D / 2) * hc + 32, v + 32);
+      tmem_ld_wait<D / 2>(v);
+      tc_fence_before();
+      mbar_arrive_warp(dq_empty);
+      if (q < p.N) {
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.dq) + (head + q) * D + (D / 2) * hc);
+        const float sc = p.scale;
+#pragma unroll
+        for (int i = 0; i < D / 16; ++i)
+          dst[i] = make_uint4(pack_bf16(__uint_as_float(v[8 * i + 0]) * sc, __uint_as_float(v[8 * i + 1]) * sc),
+                              pack_bf16(__uint_as_float(v[8 * i + 2]) * sc, __uint_as_float(v[8 * i + 3]) * sc),
+                              pack_bf16(__uint_as_float(v[8 * i + 4]) * sc, __uint_as_float(v[8 * i + 5]) * sc),
+                              pack_bf16(__uint_as_float(v[8 * i + 6]) * sc, __uint_as_float(v[8 * i + 7]) * sc));
+      }
+    }
+  } else {
+    reg_dealloc<R::kRegsCtl>();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// D_i = sum_c dO_ic * O_ic, one warp per row.
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_preprocess(const __nv_bfloat16* __restrict__ o,
                                                          const __nv_bfloat16* __restrict__ dout,
-                                                         float* __restrict__ dvec, float* __restrict__ dq_acc,
-                                                         int rows) {
+                                                         float* __restrict__ dvec, int rows) {
   const int row = blockIdx.x * 8 + threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   if (row >= rows) return;
@@ -579,20 +889,6 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess(const __nv_bfloat16* __
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (lane == 0) dvec[row] = acc;
-  float* z = dq_acc + (size_t)row * D + lane * kPer;
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) z[i] = 0.f;
-}
-
-__global__ void __launch_bounds__(256) fa_dq_convert(const float4* __restrict__ acc, uint2* __restrict__ out,
-                                                     size_t n4, float scale) {
-  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
-    const float4 v = acc[i];
-    uint2 r;
-    r.x = pack_bf16(v.x * scale, v.y * scale);
-    r.y = pack_bf16(v.z * scale, v.w * scale);
-    out[i] = r;
-  }
 }
 
 // A wait on an mbarrier that nothing arrives on: exercises the give-up path.
@@ -610,41 +906,48 @@ __global__ void fa_selftest_wait_kernel(unsigned int* status, unsigned long long
 // ------------------------------------------------------------------ launch
 
 template <int D>
-static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                                const CUtensorMap& tdo, const BwdParams& p, int grid, cudaStream_t stream) {
-  using C = BwdCfg<D>;
-  cudaError_t e = cudaFuncSetAttribute(fa_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+static cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                 const CUtensorMap& tdo, const BwdParams& p, int grid, cudaStream_t stream) {
+  using C = DkdvCfg<D>;
+  cudaError_t e =
+      cudaFuncSetAttribute(fa_bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  fa_bwd_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, p);
+  fa_bwd_dkdv_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const BwdParams& p, int grid, cudaStream_t stream) {
-  return d == 64 ? launch_bwd_t<64>(tq, tk, tv, tdo, p, grid, stream)
-                 : launch_bwd_t<128>(tq, tk, tv, tdo, p, grid, stream);
+template <int D>
+static cudaError_t launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                               const CUtensorMap& tdo, const BwdParams& p, int grid, cudaStream_t stream) {
+  using C = DqCfg<D>;
+  cudaError_t e =
+      cudaFuncSetAttribute(fa_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  fa_bwd_dq_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, p);
+  return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_preprocess(int d, const void* o, const void* dout, float* dvec, float* dq_acc, int rows,
+cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const BwdParams& p, int grid, cudaStream_t stream) {
+  return d == 64 ? launch_dkdv_t<64>(tq, tk, tv, tdo, p, grid, stream)
+                 : launch_dkdv_t<128>(tq, tk, tv, tdo, p, grid, stream);
+}
+
+cudaError_t launch_bwd_dq(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const CUtensorMap& tdo, const BwdParams& p, int grid, cudaStream_t stream) {
+  return d == 64 ? launch_dq_t<64>(tq, tk, tv, tdo, p, grid, stream)
+                 : launch_dq_t<128>(tq, tk, tv, tdo, p, grid, stream);
+}
+
+cudaError_t launch_bwd_preprocess(int d, const void* o, const void* dout, float* dvec, int rows,
                                   cudaStream_t stream) {
   const int grid = (rows + 7) / 8;
   const auto* po = static_cast<const __nv_bfloat16*>(o);
   const auto* pd = static_cast<const __nv_bfloat16*>(dout);
   if (d == 64)
-    fa_bwd_preprocess<64><<<grid, 256, 0, stream>>>(po, pd, dvec, dq_acc, rows);
+    fa_bwd_preprocess<64><<<grid, 256, 0, stream>>>(po, pd, dvec, rows);
   else
-    fa_bwd_preprocess<128><<<grid, 256, 0, stream>>>(po, pd, dvec, dq_acc, rows);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_dq_convert(int d, const float* dq_acc, void* dq, size_t elems, float scale, cudaStream_t stream) {
-  (void)d;
-  const size_t n4 = elems / 4;
-  size_t blocks = (n4 + 255) / 256;
-  if (blocks > 152 * 16) blocks = 152 * 16;
-  if (blocks == 0) blocks = 1;
-  fa_dq_convert<<<(unsigned)blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(dq_acc),
-                                                        static_cast<uint2*>(dq), n4, scale);
+    fa_bwd_preprocess<128><<<grid, 256, 0, stream>>>(po, pd, dvec, rows);
   return cudaGetLastError();
 }
 

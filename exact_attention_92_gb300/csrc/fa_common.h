@@ -62,11 +62,11 @@ struct BwdParams {
   float scale_log2;            // scale * log2(e)
   const float* lse;            // fp32 [B,H,N]
   const float* dvec;           // fp32 [B,H,N], D = rowsum(dO * O)
-  float* dq_acc;               // fp32 [B,H,N,d]
+  void* dq;                    // bf16 [B,H,N,d]
   void* dk;                    // bf16 [B,H,N,d]
   void* dv;                    // bf16 [B,H,N,d]
-  int num_kv_tiles;            // ceil(N / 128)
-  int num_units;               // B*H*num_kv_tiles
+  int num_tiles;               // ceil(N / 128): key tiles = query tiles
+  int num_units;               // B*H*num_tiles (both kernels)
   unsigned int* status;
   unsigned long long timeout_ns;
 };

@@ -163,9 +163,9 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&q_full[i], 1);
       mbar_init(&q_empty[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 4 * 32);
+      mbar_init(&p_full[i], 4);
       mbar_init(&o_full[i], 1);
-      mbar_init(&o_staged[i], 128);
+      mbar_init(&o_staged[i], 4);
     }
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&kv_full[i], 1);
@@ -426,7 +426,7 @@ __global__ void __launch_bounds__(384, 1)
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&p_full[t]);
+        mbar_arrive_warp(&p_full[t]);
       }
       if (!ok) break;
       ok = __all_sync(0xffffffffu, mbar_wait(&o_full[t], oc & 1, ctl, kWaitOFull));
@@ -460,7 +460,7 @@ __global__ void __launch_bounds__(384, 1)
           }
         }
         fence_proxy_async_smem();
-        mbar_arrive(&o_staged[t]);
+        mbar_arrive_warp(&o_staged[t]);
         if (row < p.N) p.lse[(size_t)w.bh * p.N + row] = lse;
         if ((warp & 3) == 0) {
           bool sent = true;

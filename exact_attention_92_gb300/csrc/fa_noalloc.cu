@@ -21,11 +21,12 @@ int internal_device_setup(unsigned int** status, int* sm_count);
 int internal_validate(int B, int H, int N, int d, float scale);
 int internal_encode_bhnd(CUtensorMap* m, const void* ptr, int BH, int N, int d);
 unsigned long long internal_wait_timeout_ns();
-cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const BwdParams& p, int grid, cudaStream_t stream);
-cudaError_t launch_bwd_preprocess(int d, const void* o, const void* dout, float* dvec, float* dq_acc, int rows,
+cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const BwdParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_bwd_dq(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const CUtensorMap& tdo, const BwdParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_bwd_preprocess(int d, const void* o, const void* dout, float* dvec, int rows,
                                   cudaStream_t stream);
-cudaError_t launch_dq_convert(int d, const float* dq_acc, void* dq, size_t elems, float scale, cudaStream_t stream);
 }  // namespace fa
 
 namespace {
@@ -72,7 +73,7 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
   int e = fa::internal_validate(B, H, N, d, scale);
   if (e) return e;
   const size_t rows = (size_t)B * H * N;
-  const size_t need = rows * ((size_t)d + 1) * sizeof(float);
+  const size_t need = rows * sizeof(float);
   if (need > (size_t)FA_BWD_NOALLOC_SCRATCH_BYTES) return FA_ERR_SCRATCH_TOO_SMALL;
   unsigned int* status = nullptr;
   int sm_count = 0;
@@ -89,10 +90,9 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
       fa::internal_encode_bhnd(&tv, v, BH, N, d) || fa::internal_encode_bhnd(&tdo, dout, BH, N, d))
     return FA_ERR_CUDA;
 
-  // Scratch layout: dQ accumulator [rows, d] fp32, then D [rows] fp32.  The
-  // preprocess kernel zeroes the accumulator rows and writes every D.
-  float* dq_acc = reinterpret_cast<float*>(scratch);
-  float* dvec = dq_acc + rows * d;
+  // Scratch layout: D [rows] fp32, every entry written by the preprocess
+  // kernel.
+  float* dvec = reinterpret_cast<float*>(scratch);
 
   fa::BwdParams p;
   std::memset(&p, 0, sizeof(p));
@@ -104,19 +104,17 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
   p.scale_log2 = scale * 1.4426950408889634f;
   p.lse = lse;
   p.dvec = dvec;
-  p.dq_acc = dq_acc;
+  p.dq = dq;
   p.dk = dk;
   p.dv = dv;
-  p.num_kv_tiles = (N + 127) / 128;
-  p.num_units = BH * p.num_kv_tiles;
+  p.num_tiles = (N + 127) / 128;
+  p.num_units = BH * p.num_tiles;
   p.status = status;
   p.timeout_ns = fa::internal_wait_timeout_ns();
 
-  cudaError_t ce = fa::launch_bwd_preprocess(d, o, dout, dvec, dq_acc, (int)rows, st);
-  if (ce == cudaSuccess) {
-    const int grid = p.num_units < sm_count ? p.num_units : sm_count;
-    ce = fa::launch_bwd(d, tq, tk, tv, tdo, p, grid, st);
-  }
-  if (ce == cudaSuccess) ce = fa::launch_dq_convert(d, dq_acc, dq, rows * d, scale, st);
+  const int grid = p.num_units < sm_count ? p.num_units : sm_count;
+  cudaError_t ce = fa::launch_bwd_preprocess(d, o, dout, dvec, (int)rows, st);
+  if (ce == cudaSuccess) ce = fa::launch_bwd_dkdv(d, tq, tk, tv, tdo, p, grid, st);
+  if (ce == cudaSuccess) ce = fa::launch_bwd_dq(d, tq, tk, tv, tdo, p, grid, st);
   return ce == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }

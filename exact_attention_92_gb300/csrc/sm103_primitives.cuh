@@ -58,6 +58,16 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// One arrival for the whole warp: every lane's prior writes (and, after the
+// lane's own tcgen05 wait and fence::before_thread_sync, its tensor-memory
+// accesses) are ordered before lane 0's release arrive by the warp barrier.
+// One arrive per warp instead of per thread keeps the barrier's arrival
+// traffic off the critical path.
+__device__ __forceinline__ void mbar_arrive_warp(uint64_t* bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
                "r"(bytes)

@@ -40,7 +40,7 @@
 extern "C" {
 #endif
 
-#define FA_ABI_VERSION 1
+#define FA_ABI_VERSION 2
 
 typedef enum {
   FA_OK = 0,
@@ -78,17 +78,20 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
               int causal, float scale, int num_splits, void* stream);
 
 /*
- * Backward pass.  "FlashAttention V2 in depth", section 7: key/value tiles in
- * the outer loop (dK, dV accumulated by one CTA each, no atomics), dQ
- * accumulated across CTAs with fp32 atomic adds into a workspace, P
- * recomputed from the saved logsumexp (section 7.1), and D_i = rowsum(dO_i *
- * O_i) from a separate preprocess kernel (section 7.3).
+ * Backward pass.  "FlashAttention V2 in depth", section 7: P recomputed from
+ * the saved logsumexp (section 7.1), D_i = rowsum(dO_i * O_i) from a separate
+ * preprocess kernel (section 7.3), dK and dV with key/value tiles in the
+ * outer loop (section 7.2, one CTA per key tile, no atomics), and dQ from a
+ * second kernel with query tiles in the outer loop (one CTA per query tile,
+ * no atomics) instead of the page's fp32 atomic accumulation across key
+ * tiles.
  *   q, k, v : in,  bf16 [B,H,N,d] (the forward inputs)
  *   o       : in,  bf16 [B,H,N,d] (the forward output)
  *   lse     : in,  fp32 [B,H,N]   (the forward logsumexp)
  *   dout    : in,  bf16 [B,H,N,d] (gradient of the loss w.r.t. O)
  *   dq,dk,dv: out, bf16 [B,H,N,d]
- * dq is not bitwise reproducible from run to run (atomic summation order).
+ * Workspace: D, B*H*N*4 bytes from cudaMallocAsync on `stream`.  The results
+ * are bitwise reproducible from run to run.
  */
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
            void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale, void* stream);
@@ -97,28 +100,28 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
  * Backward pass that allocates no device memory.  The paper has no
  * counterpart: this is a library convenience.
  *
- * fa_bwd takes its fp32 workspace (the dQ accumulator and D, B*H*N*(d+1)*4
- * bytes) from cudaMallocAsync on every call.  Some callers cannot allow
+ * fa_bwd takes its fp32 workspace (D, B*H*N*4 bytes) from cudaMallocAsync
+ * on every call.  Some callers cannot allow
  * that: a caller capturing a CUDA graph that must contain no memory-
  * allocation nodes, and a caller that has handed nearly all device memory
  * to its own pool up front (weights, KV caches) and cannot have a library
- * take tens of megabytes in the middle of a step.  fa_bwd_noalloc runs the
- * same three kernels as fa_bwd, with the workspace in one static device
+ * take megabytes in the middle of a step.  fa_bwd_noalloc runs the same
+ * three kernels as fa_bwd, with the workspace in one static device
  * array of FA_BWD_NOALLOC_SCRATCH_BYTES, which every device that sets this
  * entry point up keeps until the process exits.
  *
  *  - Arguments, layouts and ownership as fa_bwd; the caller still passes
  *    (and owns) every input and output.
  *  - Returns FA_ERR_SCRATCH_TOO_SMALL, before any device work, when
- *    B*H*N*(d+1)*4 exceeds FA_BWD_NOALLOC_SCRATCH_BYTES.
+ *    B*H*N*4 exceeds FA_BWD_NOALLOC_SCRATCH_BYTES.
  *  - The first call on a device sets up that device (with it current): it
  *    looks up the array's device address, and the library's status word,
  *    once.  Make that first call before any stream capture.
  *  - It calls no cudaMalloc/cudaMallocAsync/cudaFree and no allocating
  *    routine of any other library.
  *  - All calls on a device share the one array, and it keeps the last
- *    call's contents; each call clears the part that must start at zero
- *    (the dQ accumulator) itself.  Two calls whose kernels overlap on the GPU
+ *    call's contents; each call writes all of the part it reads (D) before
+ *    reading it.  Two calls whose kernels overlap on the GPU
  *    (different streams, or different host threads) race on the array and
  *    give wrong gradients: serialise them.
  */
@@ -155,7 +158,7 @@ int fa_selftest_wait_timeout(uint64_t timeout_ns, void* stream);
  * kernel is bracketed by two CUDA events recorded on the launch's stream.
  * Kernel ids: FA_KERNEL_FWD (forward main kernel), FA_KERNEL_COMBINE
  * (split-KV merge), FA_KERNEL_BWD_PRE (D preprocess), FA_KERNEL_BWD
- * (backward main kernel), FA_KERNEL_DQ_CONVERT.
+ * (backward dK/dV kernel), FA_KERNEL_BWD_DQ (backward dQ kernel).
  *   fa_timing_enable(on) : 1 starts recording (and drops old records), 0 stops.
  *   fa_timing_read(kernel, launches, total_ms) : waits for the recorded
  *       events of that kernel, returns how many launches were recorded and
@@ -167,7 +170,7 @@ int fa_selftest_wait_timeout(uint64_t timeout_ns, void* stream);
 #define FA_KERNEL_COMBINE 1
 #define FA_KERNEL_BWD_PRE 2
 #define FA_KERNEL_BWD 3
-#define FA_KERNEL_DQ_CONVERT 4
+#define FA_KERNEL_BWD_DQ 4
 int fa_timing_enable(int on);
 int fa_timing_read(int kernel, int* launches, double* total_ms);
 

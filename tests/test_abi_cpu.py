@@ -37,7 +37,7 @@ def test_no_driver_dependency():
 
 
 def test_version_and_strerror(lib):
-    assert fa.fa_abi_version() == 1
+    assert fa.fa_abi_version() == 2
     for code in range(6):
         assert fa.fa_strerror(code).startswith("FA_")
     assert "unknown" in fa.fa_strerror(99)
@@ -107,12 +107,12 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
 def test_build_refuses_spills_in_tmem_kernels():
     """A spill between tcgen05.ld and its wait would store garbage: the build
     rejects any spill in the kernels that read tensor memory."""
-    bad = ("ptxas info    : Compiling entry function '_ZN2fa13fa_bwd_kernelILi128EEEv' for 'sm_103a'\n"
+    bad = ("ptxas info    : Compiling entry function '_ZN2fa18fa_bwd_dkdv_kernelILi128EEEv' for 'sm_103a'\n"
            "    64 bytes stack frame, 32 bytes spill stores, 36 bytes spill loads\n")
     with pytest.raises(RuntimeError):
         build.check_spills(bad)
     ok = ("ptxas info    : Compiling entry function '_ZN2fa13fa_fwd_kernelILi64EEEv' for 'sm_103a'\n"
           "    24 bytes stack frame, 0 bytes spill stores, 0 bytes spill loads\n"
-          "ptxas info    : Compiling entry function '_ZN2fa13fa_dq_convertEv' for 'sm_103a'\n"
+          "ptxas info    : Compiling entry function '_ZN2fa17fa_bwd_preprocessILi64EEEv' for 'sm_103a'\n"
           "    8 bytes stack frame, 8 bytes spill stores, 8 bytes spill loads\n")
     build.check_spills(ok)

@@ -64,4 +64,4 @@ def test_timing_counts_launches(fa):
     assert counts[fa.FA_KERNEL_FWD][0] == 1 and counts[fa.FA_KERNEL_FWD][1] > 0
     assert counts[fa.FA_KERNEL_COMBINE][0] == 0
     assert counts[fa.FA_KERNEL_BWD][0] == 1 and counts[fa.FA_KERNEL_BWD_PRE][0] == 1
-    assert counts[fa.FA_KERNEL_DQ_CONVERT][0] == 1
+    assert counts[fa.FA_KERNEL_BWD_DQ][0] == 1

@@ -60,11 +60,12 @@ def test_noalloc_matches_fa_bwd_on_two_calls(shape, causal):
 def test_noalloc_refuses_problems_beyond_the_scratch():
     fa = ensure_built()
     lib = fa.load()
-    # 2 x 16 x 4096 rows x (128 + 1) fp32 = 67.6 MB > 64 MiB; refused on the
-    # host before any pointer is touched, so placeholder addresses suffice.
+    # The scratch holds D, one fp32 per row: 2 x 33 x 262144 rows x 4 bytes =
+    # 69.2 MB > 64 MiB; refused on the host before any pointer is touched, so
+    # placeholder addresses suffice.
     ptrs = [P(0x10000 * (i + 1)) for i in range(9)]
-    need = 2 * 16 * 4096 * (128 + 1) * 4
+    need = 2 * 33 * 262144 * 4
     assert need > fa_mod.FA_BWD_NOALLOC_SCRATCH_BYTES
-    st = lib.fa_bwd_noalloc(*ptrs, 2, 16, 4096, 128, 1, 0.088, None)
+    st = lib.fa_bwd_noalloc(*ptrs, 2, 33, 262144, 128, 1, 0.088, None)
     assert st == fa.FA_ERR_SCRATCH_TOO_SMALL
     assert "scratch" in fa.fa_strerror(st)
