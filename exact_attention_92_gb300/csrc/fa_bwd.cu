@@ -24,10 +24,12 @@
 // The softmax scale is applied once to dK and dQ when they are written.
 //
 // Roles (384 threads, three warpgroups, registers split with setmaxnreg as
-// in the forward kernel): warp 9 loads (TMA), warp 8 issues tcgen05 MMAs,
-// warps 10-11 idle, warps 0-7 do the element-wise work (a TMEM lane per
-// thread; warps w and w+4 split the 128 columns of a tile) and write the
-// results.
+// in the forward kernel): warp 9 loads (TMA), warps 8 and 10 issue tcgen05
+// MMAs (two issuers, split so that neither's products touch the TMEM
+// columns of the other's: a single issuing thread spends about 46 cycles per
+// MMA and one to two hundred per barrier wait, which the two overlap), warp
+// 11 idle, warps 0-7 do the element-wise work (a TMEM lane per thread; warps
+// w and w+4 split the 128 columns of a tile) and write the results.
 //
 // Pipelining.  The element-wise warps read a tile of S into registers and
 // compute P from it while the tensor core runs other products; they read dP
@@ -201,10 +203,10 @@ __global__ void __launch_bounds__(384, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    mbar_init(kv_empty, 1);
+    mbar_init(kv_empty, 2);  // the unit's last S^T and last dP^T
     for (int s = 0; s < C::kQStages; ++s) {
       mbar_init(&q_full[s], 1);
-      mbar_init(&q_empty[s], 1);
+      mbar_init(&q_empty[s], 2);  // S^T and dK
     }
     for (int s = 0; s < C::kDoStages; ++s) {
       mbar_init(&do_full[s], 1);
@@ -216,7 +218,7 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(p_ready, 8);
     mbar_init(dkv_full, 1);
     mbar_init(dkv_empty, 8);
-    mbar_init(drain, 1);
+    mbar_init(drain, 2);  // both MMA issuers
     fence_barrier_init();
   }
   if (warp == 8) {
@@ -312,94 +314,102 @@ __global__ void __launch_bounds__(384, 1)
         mbar_wait(&do_full[pos % C::kDoStages], (pos / C::kDoStages) & 1, ctl, kWaitDrain);
     }
     __syncwarp();
-  } else if (warp == 8) {
-    // ---------------------------------------------------------- MMA issuer
+  } else if (warp == 8 || warp == 10) {
+    // --------------------------------------------------------- MMA issuers
+    // Warp 8 issues S^T (into S, which no product reads); warp 10 issues
+    // dP^T, dK and dV (B, dV, dK), in that order per step, so the next dP^T
+    // overwrites B only after dK and dV have read P^T and dS^T there.  Q_i's
+    // stage is released after both S^T and dK (two arrivals), K_j / V_j
+    // after the unit's last S^T and last dP^T.
     reg_dealloc<R::kRegsCtl>();
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16(kTileM, kTileM, false, false);  // S^T, dP^T
       constexpr uint32_t id_kv = idesc_bf16(kTileM, D, false, true);       // dV, dK
       const uint32_t sk = smem_u32(smem + C::kOffK);
       const uint32_t sv = smem_u32(smem + C::kOffV);
-      uint32_t kc = 0, qc = 0, sn = 0, pc = 0, uc = 0;
+      uint32_t kc = 0, qc = 0;
       bool ok = true;
-      // S^T of the step at position `pos` into S, once the previous S^T has
-      // been read out.
-      auto issue_s = [&](uint32_t pos) -> bool {
-        const uint32_t sq = pos % C::kQStages;
-        if (!mbar_wait(&q_full[sq], (pos / C::kQStages) & 1, ctl, kWaitBwdMma)) return false;
-        if (sn > 0 && !mbar_wait(s_free, (sn - 1) & 1, ctl, kWaitBwdMma)) return false;
-        tc_fence_after();
-        const uint32_t sq_addr = smem_u32(smem + C::kOffQ + sq * C::kTileBytes);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
-          mma_ss(tmem + C::kColS, sdesc_sw128(sk + off, 16, 1024), sdesc_sw128(sq_addr + off, 16, 1024), id_s,
-                 kk > 0 ? 1u : 0u);
-        }
-        mma_commit(s_full);
-        ++sn;
-        return true;
-      };
-      for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units; ++rnd) {
-        const int u = snake_unit(rnd);
-        if (u >= p.num_units) continue;
-        const BwdUnit w = decode_dkdv(p, u);
-        ok = mbar_wait(kv_full, kc & 1, ctl, kWaitBwdMma);
-        ++kc;
-        if (!ok) break;
-        tc_fence_after();
-        ok = issue_s(qc);
-        for (int ii = 0; ok && ii < w.count; ++ii, ++qc) {
-          const uint32_t sq = qc % C::kQStages;
-          const uint32_t sd = qc % C::kDoStages;
-          const uint32_t sq_addr = smem_u32(smem + C::kOffQ + sq * C::kTileBytes);
-          const uint32_t sdo = smem_u32(smem + C::kOffDO + sd * C::kTileBytes);
-          // dP^T into B; the previous step's P^T / dS^T there were consumed
-          // by products issued earlier (the tensor pipe runs in issue order).
-          ok = mbar_wait(&do_full[sd], (qc / C::kDoStages) & 1, ctl, kWaitBwdMma);
-          if (!ok) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
-            mma_ss(tmem + C::kColB, sdesc_sw128(sv + off, 16, 1024), sdesc_sw128(sdo + off, 16, 1024), id_s,
-                   kk > 0 ? 1u : 0u);
-          }
-          mma_commit(dp_full);
-          // K_j and V_j are read by S^T and dP^T only: after the unit's last
-          // dP^T they can take the next unit's tiles.
-          if (ii + 1 == w.count) mma_commit(kv_empty);
-          // The next step's S^T, while the element-wise warps work on this one.
-          if (ii + 1 < w.count) {
-            ok = issue_s(qc + 1);
+      if (warp == 8) {
+        uint32_t sn = 0;
+        for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units; ++rnd) {
+          const int u = snake_unit(rnd);
+          if (u >= p.num_units) continue;
+          const BwdUnit w = decode_dkdv(p, u);
+          ok = mbar_wait(kv_full, kc & 1, ctl, kWaitBwdMma);
+          ++kc;
+          for (int ii = 0; ok && ii < w.count; ++ii, ++qc) {
+            // S^T once Q_i has landed and the previous S^T has been read.
+            const uint32_t sq = qc % C::kQStages;
+            ok = mbar_wait(&q_full[sq], (qc / C::kQStages) & 1, ctl, kWaitBwdMma);
+            if (ok && sn > 0) ok = mbar_wait(s_free, (sn - 1) & 1, ctl, kWaitBwdMma);
             if (!ok) break;
-          }
-          ok = mbar_wait(p_ready, pc & 1, ctl, kWaitBwdMma);
-          ++pc;
-          if (!ok) break;
-          if (ii == 0 && uc > 0) {
-            // dV / dK of the previous unit have been read out.
-            ok = mbar_wait(dkv_empty, (uc - 1) & 1, ctl, kWaitBwdMma);
-            if (!ok) break;
-          }
-          tc_fence_after();
-          // dK += dS^T Q_i (A = dS^T from TMEM, B = Q_i read MN-major), then
-          // Q_i's stage is free.
+            tc_fence_after();
+            const uint32_t sq_addr = smem_u32(smem + C::kOffQ + sq * C::kTileBytes);
 #pragma unroll
-          for (int kk = 0; kk < kTileM / 16; ++kk)
-            mma_ts(tmem + C::kColDK, tmem + C::kColB + packed_col(kk, true),
-                   sdesc_sw128(sq_addr + kk * 2048, C::kChunkBytes, 1024), id_kv, (ii > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&q_empty[sq]);
-          // dV += P^T dO_i.
-#pragma unroll
-          for (int kk = 0; kk < kTileM / 16; ++kk)
-            mma_ts(tmem + C::kColDV, tmem + C::kColB + packed_col(kk, false),
-                   sdesc_sw128(sdo + kk * 2048, C::kChunkBytes, 1024), id_kv, (ii > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&do_empty[sd]);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
+              mma_ss(tmem + C::kColS, sdesc_sw128(sk + off, 16, 1024), sdesc_sw128(sq_addr + off, 16, 1024), id_s,
+                     kk > 0 ? 1u : 0u);
+            }
+            mma_commit(s_full);
+            mma_commit(&q_empty[sq]);
+            if (ii + 1 == w.count) mma_commit(kv_empty);
+            ++sn;
+          }
         }
-        if (!ok) break;
-        mma_commit(dkv_full);
-        ++uc;
+      } else {
+        uint32_t pc = 0, uc = 0;
+        for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units; ++rnd) {
+          const int u = snake_unit(rnd);
+          if (u >= p.num_units) continue;
+          const BwdUnit w = decode_dkdv(p, u);
+          ok = mbar_wait(kv_full, kc & 1, ctl, kWaitBwdMma);
+          ++kc;
+          if (!ok) break;
+          for (int ii = 0; ok && ii < w.count; ++ii, ++qc) {
+            const uint32_t sq = qc % C::kQStages;
+            const uint32_t sd = qc % C::kDoStages;
+            const uint32_t sq_addr = smem_u32(smem + C::kOffQ + sq * C::kTileBytes);
+            const uint32_t sdo = smem_u32(smem + C::kOffDO + sd * C::kTileBytes);
+            // dP^T into B; the previous step's P^T / dS^T there were consumed
+            // by dK / dV this thread issued before.
+            ok = mbar_wait(&do_full[sd], (qc / C::kDoStages) & 1, ctl, kWaitBwdMma);
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
+              mma_ss(tmem + C::kColB, sdesc_sw128(sv + off, 16, 1024), sdesc_sw128(sdo + off, 16, 1024), id_s,
+                     kk > 0 ? 1u : 0u);
+            }
+            mma_commit(dp_full);
+            if (ii + 1 == w.count) mma_commit(kv_empty);
+            ok = mbar_wait(p_ready, pc & 1, ctl, kWaitBwdMma);
+            ++pc;
+            if (!ok) break;
+            if (ii == 0 && uc > 0) {
+              // dV / dK of the previous unit have been read out.
+              ok = mbar_wait(dkv_empty, (uc - 1) & 1, ctl, kWaitBwdMma);
+              if (!ok) break;
+            }
+            tc_fence_after();
+            // dK += dS^T Q_i (A = dS^T from TMEM, B = Q_i read MN-major).
+#pragma unroll
+            for (int kk = 0; kk < kTileM / 16; ++kk)
+              mma_ts(tmem + C::kColDK, tmem + C::kColB + packed_col(kk, true),
+                     sdesc_sw128(sq_addr + kk * 2048, C::kChunkBytes, 1024), id_kv, (ii > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(&q_empty[sq]);
+            // dV += P^T dO_i.
+#pragma unroll
+            for (int kk = 0; kk < kTileM / 16; ++kk)
+              mma_ts(tmem + C::kColDV, tmem + C::kColB + packed_col(kk, false),
+                     sdesc_sw128(sdo + kk * 2048, C::kChunkBytes, 1024), id_kv, (ii > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(&do_empty[sd]);
+          }
+          if (!ok) break;
+          mma_commit(dkv_full);
+          ++uc;
+        }
       }
       mma_commit(drain);
       mbar_wait(drain, 0, ctl, kWaitDrain);
@@ -600,7 +610,7 @@ __global__ void __launch_bounds__(384, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(qdo_full, 1);
-    mbar_init(qdo_empty, 1);
+    mbar_init(qdo_empty, 2);  // the last S and the last dP of a unit
     for (int s = 0; s < C::kKStages; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
@@ -616,7 +626,7 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(p_ready, 8);
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, 8);
-    mbar_init(drain, 1);
+    mbar_init(drain, 2);  // both MMA issuers
     fence_barrier_init();
   }
   if (warp == 8) {
@@ -679,98 +689,110 @@ __global__ void __launch_bounds__(384, 1)
         mbar_wait(&v_full[pos % C::kVStages], (pos / C::kVStages) & 1, ctl, kWaitDrain);
     }
     __syncwarp();
-  } else if (warp == 8) {
-    // ---------------------------------------------------------- MMA issuer
+  } else if (warp == 8 || warp == 10) {
+    // --------------------------------------------------------- MMA issuers
+    // Two threads issue the products, each in its own order, so that one
+    // thread's waits overlap the other's issue: warp 8 issues dP, warp 10
+    // issues dQ and S.  No product of one reads or writes TMEM columns the
+    // other's products touch; each thread's commits track its own products.
     reg_dealloc<R::kRegsCtl>();
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16(kTileM, kTileN, false, false);  // S, dP
       constexpr uint32_t id_dq = idesc_bf16(kTileM, D, false, true);       // dQ += dS K
       const uint32_t sq = smem_u32(smem + C::kOffQ);
       const uint32_t sdo = smem_u32(smem + C::kOffDO);
-      uint32_t uc = 0, kc = 0, dn = 0, pc = 0;
       bool ok = true;
-      // S of the step at position `pos` into S buffer (pos & 1).  The buffer
-      // last held the dS of step pos - 2, read by a dQ product issued
-      // earlier; its S was read before that dS was written.
-      auto issue_s = [&](uint32_t pos) -> bool {
-        const uint32_t sk = pos % C::kKStages;
-        if (!mbar_wait(&k_full[sk], (pos / C::kKStages) & 1, ctl, kWaitBwdMma)) return false;
-        tc_fence_after();
-        const uint32_t sk_addr = smem_u32(smem + C::kOffK + sk * C::kTileBytes);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
-          mma_ss(tmem + ((pos & 1) ? C::kColS1 : C::kColS0), sdesc_sw128(sq + off, 16, 1024),
-                 sdesc_sw128(sk_addr + off, 16, 1024), id_s, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(&s_full[pos & 1]);
-        return true;
-      };
-      // dP of the step at position `pos`, once the previous dP was read out.
-      // Q_i and dO_i are read by S and dP only: after the unit's last dP
-      // (`last`) they can take the next unit's tiles.
-      auto issue_dp = [&](uint32_t pos, bool last) -> bool {
-        const uint32_t sv = pos % C::kVStages;
-        if (!mbar_wait(&v_full[sv], (pos / C::kVStages) & 1, ctl, kWaitBwdMma)) return false;
-        if (dn > 0 && !mbar_wait(dp_free, (dn - 1) & 1, ctl, kWaitBwdMma)) return false;
-        tc_fence_after();
-        const uint32_t sv_addr = smem_u32(smem + C::kOffV + sv * C::kTileBytes);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
-          mma_ss(tmem + C::kColDP, sdesc_sw128(sdo + off, 16, 1024), sdesc_sw128(sv_addr + off, 16, 1024), id_s,
-                 kk > 0 ? 1u : 0u);
-        }
-        mma_commit(dp_full);
-        mma_commit(&v_empty[sv]);
-        if (last) mma_commit(qdo_empty);
-        ++dn;
-        return true;
-      };
-      for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units; ++rnd) {
-        const int u = snake_unit(rnd);
-        if (u >= p.num_units) continue;
-        const BwdUnit w = decode_dq(p, u);
-        ok = mbar_wait(qdo_full, uc & 1, ctl, kWaitBwdMma);
-        if (!ok) break;
-        tc_fence_after();
-        ok = issue_s(kc);
-        if (ok && w.count > 1) ok = issue_s(kc + 1);
-        if (ok) ok = issue_dp(kc, w.count == 1);
-        for (int jj = 0; ok && jj < w.count; ++jj, ++kc) {
-          // The next step's dP as soon as this one has been read out.
-          if (jj + 1 < w.count) {
-            ok = issue_dp(kc + 1, jj + 2 == w.count);
+      if (warp == 8) {
+        // dP of every step, once the previous dP was read out; Q_i / dO_i
+        // are released (first of two arrivals) after the unit's last dP.
+        uint32_t uc = 0, kc = 0, dn = 0;
+        for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units; ++rnd) {
+          const int u = snake_unit(rnd);
+          if (u >= p.num_units) continue;
+          const BwdUnit w = decode_dq(p, u);
+          ok = mbar_wait(qdo_full, uc & 1, ctl, kWaitBwdMma);
+          ++uc;
+          for (int jj = 0; ok && jj < w.count; ++jj, ++kc) {
+            const uint32_t sv = kc % C::kVStages;
+            ok = mbar_wait(&v_full[sv], (kc / C::kVStages) & 1, ctl, kWaitBwdMma);
+            if (ok && dn > 0) ok = mbar_wait(dp_free, (dn - 1) & 1, ctl, kWaitBwdMma);
             if (!ok) break;
+            tc_fence_after();
+            const uint32_t sv_addr = smem_u32(smem + C::kOffV + sv * C::kTileBytes);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
+              mma_ss(tmem + C::kColDP, sdesc_sw128(sdo + off, 16, 1024), sdesc_sw128(sv_addr + off, 16, 1024),
+                     id_s, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(dp_full);
+            mma_commit(&v_empty[sv]);
+            if (jj + 1 == w.count) mma_commit(qdo_empty);
+            ++dn;
           }
-          ok = mbar_wait(p_ready, pc & 1, ctl, kWaitBwdMma);
-          ++pc;
-          if (!ok) break;
-          if (jj == 0 && uc > 0) {
-            // The previous unit's dQ has been read out of TMEM.
-            ok = mbar_wait(dq_empty, (uc - 1) & 1, ctl, kWaitBwdMma);
-            if (!ok) break;
-          }
+        }
+      } else {
+        // dQ += dS K and S two steps ahead.
+        uint32_t uc = 0, kc = 0, pc = 0;
+        // S of the step at position `pos` into S buffer (pos & 1).  The
+        // buffer last held the dS of step pos - 2, read by a dQ product
+        // this thread issued earlier; its S was read before that dS was
+        // written.  `last`: the unit's last S, after which Q_i is released
+        // (second of two arrivals).
+        auto issue_s = [&](uint32_t pos, bool last) -> bool {
+          const uint32_t sk = pos % C::kKStages;
+          if (!mbar_wait(&k_full[sk], (pos / C::kKStages) & 1, ctl, kWaitBwdMma)) return false;
           tc_fence_after();
-          // dQ += dS K_j: A = dS (bf16 pairs in the step's S buffer), B = K_j
-          // read MN-major (N = head dim, K = keys).
-          const uint32_t sk = kc % C::kKStages;
           const uint32_t sk_addr = smem_u32(smem + C::kOffK + sk * C::kTileBytes);
-          const uint32_t ds_col = (kc & 1) ? C::kColS1 : C::kColS0;
 #pragma unroll
-          for (int kk = 0; kk < kTileN / 16; ++kk)
-            mma_ts(tmem + C::kColDQ, tmem + ds_col + packed_col(kk, false),
-                   sdesc_sw128(sk_addr + kk * 2048, C::kChunkBytes, 1024), id_dq, (jj > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&k_empty[sk]);
-          // S two steps ahead, into the buffer this dQ product reads from.
-          if (jj + 2 < w.count) {
-            ok = issue_s(kc + 2);
-            if (!ok) break;
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
+            mma_ss(tmem + ((pos & 1) ? C::kColS1 : C::kColS0), sdesc_sw128(sq + off, 16, 1024),
+                   sdesc_sw128(sk_addr + off, 16, 1024), id_s, kk > 0 ? 1u : 0u);
           }
+          mma_commit(&s_full[pos & 1]);
+          if (last) mma_commit(qdo_empty);
+          return true;
+        };
+        for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units; ++rnd) {
+          const int u = snake_unit(rnd);
+          if (u >= p.num_units) continue;
+          const BwdUnit w = decode_dq(p, u);
+          ok = mbar_wait(qdo_full, uc & 1, ctl, kWaitBwdMma);
+          if (!ok) break;
+          tc_fence_after();
+          ok = issue_s(kc, w.count == 1);
+          if (ok && w.count > 1) ok = issue_s(kc + 1, w.count == 2);
+          for (int jj = 0; ok && jj < w.count; ++jj, ++kc) {
+            ok = mbar_wait(p_ready, pc & 1, ctl, kWaitBwdMma);
+            ++pc;
+            if (!ok) break;
+            if (jj == 0 && uc > 0) {
+              // The previous unit's dQ has been read out of TMEM.
+              ok = mbar_wait(dq_empty, (uc - 1) & 1, ctl, kWaitBwdMma);
+              if (!ok) break;
+            }
+            tc_fence_after();
+            // dQ += dS K_j: A = dS (bf16 pairs in the step's S buffer), B =
+            // K_j read MN-major (N = head dim, K = keys).
+            const uint32_t sk = kc % C::kKStages;
+            const uint32_t sk_addr = smem_u32(smem + C::kOffK + sk * C::kTileBytes);
+            const uint32_t ds_col = (kc & 1) ? C::kColS1 : C::kColS0;
+#pragma unroll
+            for (int kk = 0; kk < kTileN / 16; ++kk)
+              mma_ts(tmem + C::kColDQ, tmem + ds_col + packed_col(kk, false),
+                     sdesc_sw128(sk_addr + kk * 2048, C::kChunkBytes, 1024), id_dq, (jj > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(&k_empty[sk]);
+            // S two steps ahead, into the buffer this dQ product reads from.
+            if (jj + 2 < w.count) {
+              ok = issue_s(kc + 2, jj + 3 == w.count);
+              if (!ok) break;
+            }
+          }
+          if (!ok) break;
+          mma_commit(dq_full);
+          ++uc;
         }
-        if (!ok) break;
-        mma_commit(dq_full);
-        ++uc;
       }
       mma_commit(drain);
       mbar_wait(drain, 0, ctl, kWaitDrain);
