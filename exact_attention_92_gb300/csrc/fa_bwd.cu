@@ -64,8 +64,9 @@ struct DkdvCfg {
   static constexpr int kQStages = 3;  // the next step's S^T needs Q early
   static constexpr int kDoStages = 2;
   static constexpr int kThreads = 384;
-  static constexpr uint32_t kColS = 0;    // S^T
-  static constexpr uint32_t kColB = 128;  // dP^T, then P^T | dS^T packed
+  // Two 128-column regions, one per step in flight: S^T, then dP^T, then
+  // P^T | dS^T packed.
+  __host__ __device__ static constexpr uint32_t col_r(uint32_t r) { return 128u * r; }
   static constexpr uint32_t kColDV = 256;
   static constexpr uint32_t kColDK = 256 + D;
   static constexpr uint32_t kTmemCols = 512;
@@ -76,7 +77,7 @@ struct DkdvCfg {
   static constexpr int kOffLse = kOffDO + kDoStages * kTileBytes;  // kQStages x 128 floats (log2 units)
   static constexpr int kOffDvec = kOffLse + kQStages * 128 * 4;    // kDoStages x 128 floats
   static constexpr int kOffBar = kOffDvec + kDoStages * 128 * 4;
-  static constexpr int kNumBars = 2 + 2 * kQStages + 2 * kDoStages + 7;
+  static constexpr int kNumBars = 2 + 2 * kQStages + 2 * kDoStages + 13;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16;
   static_assert(kSmemBytes <= 232448, "shared memory");
 };
@@ -187,11 +188,13 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* q_empty = q_full + C::kQStages;
   uint64_t* do_full = q_empty + C::kQStages;  // [kDoStages]: dO tile and its D values
   uint64_t* do_empty = do_full + C::kDoStages;
-  uint64_t* s_full = do_empty + C::kDoStages;  // S^T in TMEM
-  uint64_t* s_free = s_full + 1;               // S^T read by all element-wise warps
-  uint64_t* dp_full = s_free + 1;              // dP^T in TMEM
-  uint64_t* p_ready = dp_full + 1;             // P^T, dS^T packed in TMEM
-  uint64_t* dkv_full = p_ready + 1;
+  // Per TMEM region r (steps with pos & 1 == r):
+  uint64_t* s_full = do_empty + C::kDoStages;  // [2] S^T in region r
+  uint64_t* s_free = s_full + 2;               // [2] ... read by all element-wise warps
+  uint64_t* dp_full = s_free + 2;              // [2] dP^T in region r
+  uint64_t* kdone = dp_full + 2;               // [2] dK, dV have read region r's P^T, dS^T
+  uint64_t* p_ready = kdone + 2;               // [2] P^T, dS^T packed in region r
+  uint64_t* dkv_full = p_ready + 2;
   uint64_t* dkv_empty = dkv_full + 1;
   uint64_t* drain = dkv_empty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -203,19 +206,22 @@ __global__ void __launch_bounds__(384, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    mbar_init(kv_empty, 2);  // the unit's last S^T and last dP^T
+    mbar_init(kv_empty, 1);  // the unit's last dP^T (after its last S^T)
     for (int s = 0; s < C::kQStages; ++s) {
       mbar_init(&q_full[s], 1);
       mbar_init(&q_empty[s], 2);  // S^T and dK
     }
     for (int s = 0; s < C::kDoStages; ++s) {
       mbar_init(&do_full[s], 1);
-      mbar_init(&do_empty[s], 1);
+      mbar_init(&do_empty[s], 2);  // dP^T and dV
     }
-    mbar_init(s_full, 1);
-    mbar_init(s_free, 8);
-    mbar_init(dp_full, 1);
-    mbar_init(p_ready, 8);
+    for (int r = 0; r < 2; ++r) {
+      mbar_init(&s_full[r], 1);
+      mbar_init(&s_free[r], 8);
+      mbar_init(&dp_full[r], 1);
+      mbar_init(&kdone[r], 1);
+      mbar_init(&p_ready[r], 8);
+    }
     mbar_init(dkv_full, 1);
     mbar_init(dkv_empty, 8);
     mbar_init(drain, 2);  // both MMA issuers
@@ -316,11 +322,11 @@ __global__ void __launch_bounds__(384, 1)
     __syncwarp();
   } else if (warp == 8 || warp == 10) {
     // --------------------------------------------------------- MMA issuers
-    // Warp 8 issues S^T (into S, which no product reads); warp 10 issues
-    // dP^T, dK and dV (B, dV, dK), in that order per step, so the next dP^T
-    // overwrites B only after dK and dV have read P^T and dS^T there.  Q_i's
-    // stage is released after both S^T and dK (two arrivals), K_j / V_j
-    // after the unit's last S^T and last dP^T.
+    // Two steps are in flight: step pos uses TMEM region pos & 1 for its
+    // S^T, then (once S^T has been read) its dP^T, then its packed P^T and
+    // dS^T, which dK and dV read.  Warp 8 issues S^T and dP^T; warp 10
+    // issues dV and dK and marks the region free (kdone).  S^T of step pos
+    // waits for kdone of step pos - 2, which used the same region.
     reg_dealloc<R::kRegsCtl>();
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16(kTileM, kTileM, false, false);  // S^T, dP^T
@@ -330,62 +336,65 @@ __global__ void __launch_bounds__(384, 1)
       uint32_t kc = 0, qc = 0;
       bool ok = true;
       if (warp == 8) {
-        uint32_t sn = 0;
+        // S^T of the step at position `pos` into region pos & 1.
+        auto issue_s = [&](uint32_t pos) -> bool {
+          const uint32_t sq = pos % C::kQStages;
+          const uint32_t r = pos & 1, n = pos >> 1;
+          if (!mbar_wait(&q_full[sq], (pos / C::kQStages) & 1, ctl, kWaitBwdMma)) return false;
+          if (n > 0 && !mbar_wait(&kdone[r], (n - 1) & 1, ctl, kWaitBwdMma)) return false;
+          tc_fence_after();
+          const uint32_t sq_addr = smem_u32(smem + C::kOffQ + sq * C::kTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
+            mma_ss(tmem + C::col_r(r), sdesc_sw128(sk + off, 16, 1024), sdesc_sw128(sq_addr + off, 16, 1024), id_s,
+                   kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&s_full[r]);
+          mma_commit(&q_empty[sq]);
+          return true;
+        };
         for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units; ++rnd) {
           const int u = snake_unit(rnd);
           if (u >= p.num_units) continue;
           const BwdUnit w = decode_dkdv(p, u);
           ok = mbar_wait(kv_full, kc & 1, ctl, kWaitBwdMma);
           ++kc;
+          if (ok) ok = issue_s(qc);
           for (int ii = 0; ok && ii < w.count; ++ii, ++qc) {
-            // S^T once Q_i has landed and the previous S^T has been read.
-            const uint32_t sq = qc % C::kQStages;
-            ok = mbar_wait(&q_full[sq], (qc / C::kQStages) & 1, ctl, kWaitBwdMma);
-            if (ok && sn > 0) ok = mbar_wait(s_free, (sn - 1) & 1, ctl, kWaitBwdMma);
+            // dP^T into the step's region once its S^T has been read out.
+            const uint32_t r = qc & 1;
+            const uint32_t sd = qc % C::kDoStages;
+            ok = mbar_wait(&do_full[sd], (qc / C::kDoStages) & 1, ctl, kWaitBwdMma);
+            if (ok) ok = mbar_wait(&s_free[r], (qc >> 1) & 1, ctl, kWaitBwdMma);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t sq_addr = smem_u32(smem + C::kOffQ + sq * C::kTileBytes);
+            const uint32_t sdo = smem_u32(smem + C::kOffDO + sd * C::kTileBytes);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
-              mma_ss(tmem + C::kColS, sdesc_sw128(sk + off, 16, 1024), sdesc_sw128(sq_addr + off, 16, 1024), id_s,
+              mma_ss(tmem + C::col_r(r), sdesc_sw128(sv + off, 16, 1024), sdesc_sw128(sdo + off, 16, 1024), id_s,
                      kk > 0 ? 1u : 0u);
             }
-            mma_commit(s_full);
-            mma_commit(&q_empty[sq]);
+            mma_commit(&dp_full[r]);
+            mma_commit(&do_empty[sd]);
+            // K_j and V_j are read by S^T and dP^T only.
             if (ii + 1 == w.count) mma_commit(kv_empty);
-            ++sn;
+            // The next step's S^T, in the other region.
+            if (ii + 1 < w.count) ok = issue_s(qc + 1);
           }
         }
       } else {
-        uint32_t pc = 0, uc = 0;
+        uint32_t uc = 0;
         for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units; ++rnd) {
           const int u = snake_unit(rnd);
           if (u >= p.num_units) continue;
           const BwdUnit w = decode_dkdv(p, u);
-          ok = mbar_wait(kv_full, kc & 1, ctl, kWaitBwdMma);
-          ++kc;
-          if (!ok) break;
           for (int ii = 0; ok && ii < w.count; ++ii, ++qc) {
+            const uint32_t r = qc & 1;
             const uint32_t sq = qc % C::kQStages;
             const uint32_t sd = qc % C::kDoStages;
-            const uint32_t sq_addr = smem_u32(smem + C::kOffQ + sq * C::kTileBytes);
-            const uint32_t sdo = smem_u32(smem + C::kOffDO + sd * C::kTileBytes);
-            // dP^T into B; the previous step's P^T / dS^T there were consumed
-            // by dK / dV this thread issued before.
-            ok = mbar_wait(&do_full[sd], (qc / C::kDoStages) & 1, ctl, kWaitBwdMma);
-            if (!ok) break;
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
-              mma_ss(tmem + C::kColB, sdesc_sw128(sv + off, 16, 1024), sdesc_sw128(sdo + off, 16, 1024), id_s,
-                     kk > 0 ? 1u : 0u);
-            }
-            mma_commit(dp_full);
-            if (ii + 1 == w.count) mma_commit(kv_empty);
-            ok = mbar_wait(p_ready, pc & 1, ctl, kWaitBwdMma);
-            ++pc;
+            ok = mbar_wait(&p_ready[r], (qc >> 1) & 1, ctl, kWaitBwdMma);
             if (!ok) break;
             if (ii == 0 && uc > 0) {
               // dV / dK of the previous unit have been read out.
@@ -393,18 +402,21 @@ __global__ void __launch_bounds__(384, 1)
               if (!ok) break;
             }
             tc_fence_after();
-            // dK += dS^T Q_i (A = dS^T from TMEM, B = Q_i read MN-major).
+            const uint32_t sq_addr = smem_u32(smem + C::kOffQ + sq * C::kTileBytes);
+            const uint32_t sdo = smem_u32(smem + C::kOffDO + sd * C::kTileBytes);
+            // dV += P^T dO_i (A = P^T from TMEM, B = dO_i read MN-major).
 #pragma unroll
             for (int kk = 0; kk < kTileM / 16; ++kk)
-              mma_ts(tmem + C::kColDK, tmem + C::kColB + packed_col(kk, true),
-                     sdesc_sw128(sq_addr + kk * 2048, C::kChunkBytes, 1024), id_kv, (ii > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(&q_empty[sq]);
-            // dV += P^T dO_i.
-#pragma unroll
-            for (int kk = 0; kk < kTileM / 16; ++kk)
-              mma_ts(tmem + C::kColDV, tmem + C::kColB + packed_col(kk, false),
+              mma_ts(tmem + C::kColDV, tmem + C::col_r(r) + packed_col(kk, false),
                      sdesc_sw128(sdo + kk * 2048, C::kChunkBytes, 1024), id_kv, (ii > 0 || kk > 0) ? 1u : 0u);
             mma_commit(&do_empty[sd]);
+            // dK += dS^T Q_i.
+#pragma unroll
+            for (int kk = 0; kk < kTileM / 16; ++kk)
+              mma_ts(tmem + C::kColDK, tmem + C::col_r(r) + packed_col(kk, true),
+                     sdesc_sw128(sq_addr + kk * 2048, C::kChunkBytes, 1024), id_kv, (ii > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(&q_empty[sq]);
+            mma_commit(&kdone[r]);
           }
           if (!ok) break;
           mma_commit(dkv_full);
@@ -421,59 +433,55 @@ __global__ void __launch_bounds__(384, 1)
     const int g = warp & 3;    // TMEM lane quarter
     const int hc = warp >> 2;  // query-column half
     const uint32_t lane_off = (uint32_t)(32 * g) << 16;
-    const uint32_t tS = tmem + lane_off + C::kColS + 64 * hc;
-    const uint32_t tB = tmem + lane_off + C::kColB + 64 * hc;
-    const int r = 32 * g + lane;  // key row within the tile
+    const int r_key = 32 * g + lane;  // key row within the tile
     const float sl2 = p.scale_log2;
-    uint32_t sc = 0, uc = 0, qc = 0, dc = 0;
+    uint32_t uc = 0, qc = 0;
     bool ok = true;
-    uint32_t pv[64];  // P^T of the current step (fp32 bits), 64 query columns
-    uint32_t pk[32];  // the same, packed to bf16 pairs for the dV product
-    // Wait for S^T of the step at position `pos`, read this warp's 64
-    // columns, release them and compute P^T.
-    auto load_p = [&](uint32_t pos, int q0, int kr) -> bool {
-      const uint32_t sq = pos % C::kQStages;
-      if (!__all_sync(0xffffffffu, mbar_wait(&q_full[sq], (pos / C::kQStages) & 1, ctl, kWaitBwdSoftmax)))
-        return false;
-      if (!__all_sync(0xffffffffu, mbar_wait(s_full, sc & 1, ctl, kWaitBwdSoftmax))) return false;
-      ++sc;
-      tc_fence_after();
-      tmem_ld32(tS, pv);
-      tmem_ld32(tS + 32, pv + 32);
-      tmem_ld_wait<64>(pv);
-      tc_fence_before();
-      mbar_arrive_warp(s_free);
-      const float* bl = sLse + sq * 128 + 64 * hc;
-      const int qf = q0 + 64 * hc;
-      if ((kr >= p.N) || (p.causal && kr > qf))
-        p64_colL<true>(pv, bl, sl2, kr, qf, kr >= p.N, p.causal != 0);
-      else
-        p64_colL<false>(pv, bl, sl2, kr, qf, false, false);
-#pragma unroll
-      for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(__uint_as_float(pv[2 * e]), __uint_as_float(pv[2 * e + 1]));
-      return true;
-    };
     for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units; ++rnd) {
       const int u = snake_unit(rnd);
       if (u >= p.num_units) continue;
       const BwdUnit w = decode_dkdv(p, u);
-      const int kr = w.t * kTileN + r;  // key index
+      const int kr = w.t * kTileN + r_key;  // key index
       const size_t head = (size_t)w.bh * p.N;
-      ok = load_p(qc, w.first * kTileM, kr);
       for (int ii = 0; ok && ii < w.count; ++ii, ++qc) {
         const int q0 = (w.first + ii) * kTileM;
+        const uint32_t reg = qc & 1;
+        const uint32_t tZ = tmem + lane_off + C::col_r(reg) + 64 * hc;
+        const uint32_t sq = qc % C::kQStages;
         const uint32_t sd = qc % C::kDoStages;
-        // dS^T = P^T * (dP^T - D); P^T and dS^T packed over this warp's dP^T
-        // columns.
+        // P^T = exp2(S^T * scale * log2 e - L) over this warp's 64 query
+        // columns; the S^T columns are released as soon as they are read.
+        ok = __all_sync(0xffffffffu, mbar_wait(&q_full[sq], (qc / C::kQStages) & 1, ctl, kWaitBwdSoftmax));
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&s_full[reg], (qc >> 1) & 1, ctl, kWaitBwdSoftmax));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t pv[64];
+        tmem_ld32(tZ, pv);
+        tmem_ld32(tZ + 32, pv + 32);
+        tmem_ld_wait<64>(pv);
+        tc_fence_before();
+        mbar_arrive_warp(&s_free[reg]);
+        {
+          const float* bl = sLse + sq * 128 + 64 * hc;
+          const int qf = q0 + 64 * hc;
+          if ((kr >= p.N) || (p.causal && kr > qf))
+            p64_colL<true>(pv, bl, sl2, kr, qf, kr >= p.N, p.causal != 0);
+          else
+            p64_colL<false>(pv, bl, sl2, kr, qf, false, false);
+        }
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(__uint_as_float(pv[2 * e]), __uint_as_float(pv[2 * e + 1]));
+        // dS^T = P^T * (dP^T - D); P^T and dS^T packed over this warp's
+        // dP^T columns of the region.
         ok = __all_sync(0xffffffffu, mbar_wait(&do_full[sd], (qc / C::kDoStages) & 1, ctl, kWaitBwdSoftmax));
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(dp_full, dc & 1, ctl, kWaitBwdSoftmax));
-        ++dc;
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&dp_full[reg], (qc >> 1) & 1, ctl, kWaitBwdSoftmax));
         if (!ok) break;
         tc_fence_after();
         {
           uint32_t dpv[64];
-          tmem_ld32(tB, dpv);
-          tmem_ld32(tB + 32, dpv + 32);
+          tmem_ld32(tZ, dpv);
+          tmem_ld32(tZ + 32, dpv + 32);
           tmem_ld_wait<64>(dpv);
           const float* bd = sDv + sd * 128 + 64 * hc;
           uint32_t dk[32];
@@ -492,17 +500,12 @@ __global__ void __launch_bounds__(384, 1)
             dk[2 * e4] = pack_bf16(ds01.x, ds01.y);
             dk[2 * e4 + 1] = pack_bf16(ds23.x, ds23.y);
           }
-          tmem_st32(tB, pk);
-          tmem_st32(tB + 32, dk);
+          tmem_st32(tZ, pk);
+          tmem_st32(tZ + 32, dk);
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive_warp(p_ready);
-        // The next step's P^T while the tensor core runs dK and dV.
-        if (ii + 1 < w.count) {
-          ok = load_p(qc + 1, q0 + kTileM, kr);
-          if (!ok) break;
-        }
+        mbar_arrive_warp(&p_ready[reg]);
       }
       if (!ok) break;
       // dK_j = scale * sum dS^T Q and dV_j = sum P^T dO of this unit; this
@@ -572,7 +575,7 @@ struct DqCfg {
   static constexpr int kOffK = 2 * kTileBytes;
   static constexpr int kOffV = kOffK + kKStages * kTileBytes;
   static constexpr int kOffBar = kOffV + kVStages * kTileBytes;
-  static constexpr int kNumBars = 2 + 2 * kKStages + 2 * kVStages + 8;
+  static constexpr int kNumBars = 2 + 2 * kKStages + 2 * kVStages + 9;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16;
   static_assert(kSmemBytes <= 232448, "shared memory");
 };
@@ -599,8 +602,8 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* s_full = v_empty + C::kVStages;  // [2]: S of even / odd steps in TMEM
   uint64_t* dp_full = s_full + 2;            // dP in TMEM
   uint64_t* dp_free = dp_full + 1;           // dP read by all element-wise warps
-  uint64_t* p_ready = dp_free + 1;           // dS packed in TMEM
-  uint64_t* dq_full = p_ready + 1;           // the unit's dQ complete
+  uint64_t* p_ready = dp_free + 1;           // [2] dS packed in S buffer 0 / 1
+  uint64_t* dq_full = p_ready + 2;           // the unit's dQ complete
   uint64_t* dq_empty = dq_full + 1;          // ... and read out
   uint64_t* drain = dq_empty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -623,7 +626,8 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(&s_full[1], 1);
     mbar_init(dp_full, 1);
     mbar_init(dp_free, 8);
-    mbar_init(p_ready, 8);
+    mbar_init(&p_ready[0], 8);
+    mbar_init(&p_ready[1], 8);
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, 8);
     mbar_init(drain, 2);  // both MMA issuers
@@ -733,7 +737,7 @@ __global__ void __launch_bounds__(384, 1)
         }
       } else {
         // dQ += dS K and S two steps ahead.
-        uint32_t uc = 0, kc = 0, pc = 0;
+        uint32_t uc = 0, kc = 0;
         // S of the step at position `pos` into S buffer (pos & 1).  The
         // buffer last held the dS of step pos - 2, read by a dQ product
         // this thread issued earlier; its S was read before that dS was
@@ -764,8 +768,7 @@ __global__ void __launch_bounds__(384, 1)
           ok = issue_s(kc, w.count == 1);
           if (ok && w.count > 1) ok = issue_s(kc + 1, w.count == 2);
           for (int jj = 0; ok && jj < w.count; ++jj, ++kc) {
-            ok = mbar_wait(p_ready, pc & 1, ctl, kWaitBwdMma);
-            ++pc;
+            ok = mbar_wait(&p_ready[kc & 1], (kc >> 1) & 1, ctl, kWaitBwdMma);
             if (!ok) break;
             if (jj == 0 && uc > 0) {
               // The previous unit's dQ has been read out of TMEM.
@@ -856,7 +859,7 @@ __global__ void __launch_bounds__(384, 1)
         tmem_st32(tS, dk);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive_warp(p_ready);
+        mbar_arrive_warp(&p_ready[kc & 1]);
       }
       if (!ok) break;
       // dQ_i = scale * sum dS K of this unit: lane = query row, this warp
