@@ -396,6 +396,8 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
   p.dq = dq;
   p.dk = dk;
   p.dv = dv;
+  p.store32 = ((reinterpret_cast<uintptr_t>(dq) | reinterpret_cast<uintptr_t>(dk) |
+                reinterpret_cast<uintptr_t>(dv)) & 31u) == 0 ? 1 : 0;
   p.num_tiles = (N + 127) / 128;
   p.num_units = BH * p.num_tiles;
   p.status = s->status;

@@ -77,7 +77,7 @@ struct DkdvCfg {
   static constexpr int kOffLse = kOffDO + kDoStages * kTileBytes;  // kQStages x 128 floats (log2 units)
   static constexpr int kOffDvec = kOffLse + kQStages * 128 * 4;    // kDoStages x 128 floats
   static constexpr int kOffBar = kOffDvec + kDoStages * 128 * 4;
-  static constexpr int kNumBars = 2 + 2 * kQStages + 2 * kDoStages + 13;
+  static constexpr int kNumBars = 4 + 2 * kQStages + 2 * kDoStages + 11;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16;
   static_assert(kSmemBytes <= 232448, "shared memory");
 };
@@ -182,9 +182,14 @@ __global__ void __launch_bounds__(384, 1)
     return;
   }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
-  uint64_t* kv_full = bars;
-  uint64_t* kv_empty = bars + 1;
-  uint64_t* q_full = bars + 2;  // [kQStages]: Q tile and its L values
+  // K_j and V_j of a unit have separate barriers: K is released after the
+  // unit's last S^T, two steps before its end, so the next unit's K loads
+  // early; V after the last dP^T.
+  uint64_t* k_full = bars;
+  uint64_t* k_empty = bars + 1;
+  uint64_t* v_full = bars + 2;
+  uint64_t* v_empty = bars + 3;
+  uint64_t* q_full = bars + 4;  // [kQStages]: Q tile and its L values
   uint64_t* q_empty = q_full + C::kQStages;
   uint64_t* do_full = q_empty + C::kQStages;  // [kDoStages]: dO tile and its D values
   uint64_t* do_empty = do_full + C::kDoStages;
@@ -192,8 +197,7 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* s_full = do_empty + C::kDoStages;  // [2] S^T in region r
   uint64_t* s_free = s_full + 2;               // [2] ... read by all element-wise warps
   uint64_t* dp_full = s_free + 2;              // [2] dP^T in region r
-  uint64_t* kdone = dp_full + 2;               // [2] dK, dV have read region r's P^T, dS^T
-  uint64_t* p_ready = kdone + 2;               // [2] P^T, dS^T packed in region r
+  uint64_t* p_ready = dp_full + 2;             // [2] P^T, dS^T packed in region r
   uint64_t* dkv_full = p_ready + 2;
   uint64_t* dkv_empty = dkv_full + 1;
   uint64_t* drain = dkv_empty + 1;
@@ -205,11 +209,13 @@ __global__ void __launch_bounds__(384, 1)
   const int lane = threadIdx.x % 32;
 
   if (threadIdx.x == 0) {
-    mbar_init(kv_full, 1);
-    mbar_init(kv_empty, 1);  // the unit's last dP^T (after its last S^T)
+    mbar_init(k_full, 1);
+    mbar_init(k_empty, 1);  // the unit's last S^T
+    mbar_init(v_full, 1);
+    mbar_init(v_empty, 1);  // the unit's last dP^T
     for (int s = 0; s < C::kQStages; ++s) {
       mbar_init(&q_full[s], 1);
-      mbar_init(&q_empty[s], 2);  // S^T and dK
+      mbar_init(&q_empty[s], 1);  // dK (issued after the step's S^T)
     }
     for (int s = 0; s < C::kDoStages; ++s) {
       mbar_init(&do_full[s], 1);
@@ -219,7 +225,6 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&s_full[r], 1);
       mbar_init(&s_free[r], 8);
       mbar_init(&dp_full[r], 1);
-      mbar_init(&kdone[r], 1);
       mbar_init(&p_ready[r], 8);
     }
     mbar_init(dkv_full, 1);
@@ -253,16 +258,13 @@ __global__ void __launch_bounds__(384, 1)
       if (u >= p.num_units) continue;
       const BwdUnit w = decode_dkdv(p, u);
       const size_t head = (size_t)w.bh * p.N;
-      ok = __all_sync(0xffffffffu, mbar_wait(kv_empty, (kc & 1) ^ 1, ctl, kWaitBwdLoad));
+      ok = __all_sync(0xffffffffu, mbar_wait(k_empty, (kc & 1) ^ 1, ctl, kWaitBwdLoad));
       if (!ok) break;
       if (lane == 0) {
-        mbar_arrive_expect_tx(kv_full, 2 * C::kTileBytes);
-        for (int c = 0; c < C::kChunks; ++c) {
-          tma_load_3d(smem + C::kOffK + c * C::kChunkBytes, &tm_k, kv_full, c * 64, w.t * kTileN, w.bh);
-          tma_load_3d(smem + C::kOffV + c * C::kChunkBytes, &tm_v, kv_full, c * 64, w.t * kTileN, w.bh);
-        }
+        mbar_arrive_expect_tx(k_full, C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(smem + C::kOffK + c * C::kChunkBytes, &tm_k, k_full, c * 64, w.t * kTileN, w.bh);
       }
-      ++kc;
       for (int ii = 0; ok && ii < w.count; ++ii, ++qc) {
         const int row = (w.first + ii) * kTileM;
         // Q_i with L_i (log2 units; rows past N get +inf so their weights
@@ -309,11 +311,25 @@ __global__ void __launch_bounds__(384, 1)
             tma_load_3d(smem + C::kOffDO + sd * C::kTileBytes + c * C::kChunkBytes, &tm_do, &do_full[sd],
                         c * 64, row, w.bh);
         }
+        if (ii == 0) {
+          // V_j, needed by the first dP^T, after the first step's Q and dO.
+          ok = __all_sync(0xffffffffu, mbar_wait(v_empty, (kc & 1) ^ 1, ctl, kWaitBwdLoad));
+          if (!ok) break;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(v_full, C::kTileBytes);
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_load_3d(smem + C::kOffV + c * C::kChunkBytes, &tm_v, v_full, c * 64, w.t * kTileN, w.bh);
+          }
+        }
       }
+      ++kc;
     }
     if (lane == 0) {
       // Every copy this warp issued has landed before the CTA exits.
-      if (kc > 0) mbar_wait(kv_full, (kc - 1) & 1, ctl, kWaitDrain);
+      if (kc > 0) {
+        mbar_wait(k_full, (kc - 1) & 1, ctl, kWaitDrain);
+        mbar_wait(v_full, (kc - 1) & 1, ctl, kWaitDrain);
+      }
       for (uint32_t pos = qc > (uint32_t)C::kQStages ? qc - C::kQStages : 0u; pos < qc; ++pos)
         mbar_wait(&q_full[pos % C::kQStages], (pos / C::kQStages) & 1, ctl, kWaitDrain);
       for (uint32_t pos = qc > (uint32_t)C::kDoStages ? qc - C::kDoStages : 0u; pos < qc; ++pos)
@@ -324,9 +340,10 @@ __global__ void __launch_bounds__(384, 1)
     // --------------------------------------------------------- MMA issuers
     // Two steps are in flight: step pos uses TMEM region pos & 1 for its
     // S^T, then (once S^T has been read) its dP^T, then its packed P^T and
-    // dS^T, which dK and dV read.  Warp 8 issues S^T and dP^T; warp 10
-    // issues dV and dK and marks the region free (kdone).  S^T of step pos
-    // waits for kdone of step pos - 2, which used the same region.
+    // dS^T, which dK and dV read.  Warp 8 issues dP^T.  Warp 10 issues dV
+    // and dK of a step and then S^T of the step two ahead into the same
+    // region, so the tensor pipe's issue order keeps S^T behind the products
+    // that read the region.
     reg_dealloc<R::kRegsCtl>();
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16(kTileM, kTileM, false, false);  // S^T, dP^T
@@ -336,31 +353,12 @@ __global__ void __launch_bounds__(384, 1)
       uint32_t kc = 0, qc = 0;
       bool ok = true;
       if (warp == 8) {
-        // S^T of the step at position `pos` into region pos & 1.
-        auto issue_s = [&](uint32_t pos) -> bool {
-          const uint32_t sq = pos % C::kQStages;
-          const uint32_t r = pos & 1, n = pos >> 1;
-          if (!mbar_wait(&q_full[sq], (pos / C::kQStages) & 1, ctl, kWaitBwdMma)) return false;
-          if (n > 0 && !mbar_wait(&kdone[r], (n - 1) & 1, ctl, kWaitBwdMma)) return false;
-          tc_fence_after();
-          const uint32_t sq_addr = smem_u32(smem + C::kOffQ + sq * C::kTileBytes);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
-            mma_ss(tmem + C::col_r(r), sdesc_sw128(sk + off, 16, 1024), sdesc_sw128(sq_addr + off, 16, 1024), id_s,
-                   kk > 0 ? 1u : 0u);
-          }
-          mma_commit(&s_full[r]);
-          mma_commit(&q_empty[sq]);
-          return true;
-        };
         for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units; ++rnd) {
           const int u = snake_unit(rnd);
           if (u >= p.num_units) continue;
           const BwdUnit w = decode_dkdv(p, u);
-          ok = mbar_wait(kv_full, kc & 1, ctl, kWaitBwdMma);
+          ok = mbar_wait(v_full, kc & 1, ctl, kWaitBwdMma);
           ++kc;
-          if (ok) ok = issue_s(qc);
           for (int ii = 0; ok && ii < w.count; ++ii, ++qc) {
             // dP^T into the step's region once its S^T has been read out.
             const uint32_t r = qc & 1;
@@ -378,18 +376,38 @@ __global__ void __launch_bounds__(384, 1)
             }
             mma_commit(&dp_full[r]);
             mma_commit(&do_empty[sd]);
-            // K_j and V_j are read by S^T and dP^T only.
-            if (ii + 1 == w.count) mma_commit(kv_empty);
-            // The next step's S^T, in the other region.
-            if (ii + 1 < w.count) ok = issue_s(qc + 1);
+            // V_j is read by dP^T only.
+            if (ii + 1 == w.count) mma_commit(v_empty);
           }
         }
       } else {
+        // S^T of the step at position `pos` into region pos & 1; `last`: the
+        // unit's last S^T, after which K_j is released.
+        auto issue_s = [&](uint32_t pos, bool last) -> bool {
+          const uint32_t sq = pos % C::kQStages;
+          const uint32_t r = pos & 1;
+          if (!mbar_wait(&q_full[sq], (pos / C::kQStages) & 1, ctl, kWaitBwdMma)) return false;
+          tc_fence_after();
+          const uint32_t sq_addr = smem_u32(smem + C::kOffQ + sq * C::kTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
+            mma_ss(tmem + C::col_r(r), sdesc_sw128(sk + off, 16, 1024), sdesc_sw128(sq_addr + off, 16, 1024), id_s,
+                   kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&s_full[r]);
+          if (last) mma_commit(k_empty);
+          return true;
+        };
         uint32_t uc = 0;
         for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units; ++rnd) {
           const int u = snake_unit(rnd);
           if (u >= p.num_units) continue;
           const BwdUnit w = decode_dkdv(p, u);
+          ok = mbar_wait(k_full, kc & 1, ctl, kWaitBwdMma);
+          ++kc;
+          if (ok) ok = issue_s(qc, w.count == 1);
+          if (ok && w.count > 1) ok = issue_s(qc + 1, w.count == 2);
           for (int ii = 0; ok && ii < w.count; ++ii, ++qc) {
             const uint32_t r = qc & 1;
             const uint32_t sq = qc % C::kQStages;
@@ -416,7 +434,8 @@ __global__ void __launch_bounds__(384, 1)
               mma_ts(tmem + C::kColDK, tmem + C::col_r(r) + packed_col(kk, true),
                      sdesc_sw128(sq_addr + kk * 2048, C::kChunkBytes, 1024), id_kv, (ii > 0 || kk > 0) ? 1u : 0u);
             mma_commit(&q_empty[sq]);
-            mma_commit(&kdone[r]);
+            // S^T two steps ahead, into the region dV and dK have just read.
+            if (ii + 2 < w.count) ok = issue_s(qc + 2, ii + 3 == w.count);
           }
           if (!ok) break;
           mma_commit(dkv_full);
@@ -437,6 +456,52 @@ __global__ void __launch_bounds__(384, 1)
     const float sl2 = p.scale_log2;
     uint32_t uc = 0, qc = 0;
     bool ok = true;
+    // dK_j = scale * sum dS^T Q and dV_j = sum P^T dO of unit (kr, head);
+    // this warp writes head-dim columns [D/2 hc, D/2 hc + D/2).  Run after
+    // the next unit's first P^T, while its dP^T is computed.
+    auto write_dkdv = [&](int kr, size_t head) -> bool {
+      if (!__all_sync(0xffffffffu, mbar_wait(dkv_full, uc & 1, ctl, kWaitBwdSoftmax))) return false;
+      ++uc;
+      tc_fence_after();
+      __nv_bfloat16* dvp = reinterpret_cast<__nv_bfloat16*>(p.dv) + (head + kr) * D;
+      __nv_bfloat16* dkp = reinterpret_cast<__nv_bfloat16*>(p.dk) + (head + kr) * D;
+#pragma unroll 1
+      for (int c = hc * (D / 64); c < (hc + 1) * (D / 64); ++c) {
+        uint32_t a[32], b[32];
+        tmem_ld32(tmem + lane_off + C::kColDV + 32 * c, a);
+        tmem_ld32(tmem + lane_off + C::kColDK + 32 * c, b);
+        tmem_ld_wait<32>(a);
+        tmem_ld_wait<32>(b);
+        if (kr < p.N) {
+          // One row of 32 columns per tensor: 64 bytes, as two 32-byte
+          // stores when the buffers allow it (a warp store then fills whole
+          // 32-byte sectors of 32 rows).
+          uint32_t va[16], vb[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            va[i] = pack_bf16(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
+            vb[i] = pack_bf16(__uint_as_float(b[2 * i]) * p.scale, __uint_as_float(b[2 * i + 1]) * p.scale);
+          }
+          if (p.store32) {
+            st_global_v8(dvp + 32 * c, va);
+            st_global_v8(dvp + 32 * c + 16, va + 8);
+            st_global_v8(dkp + 32 * c, vb);
+            st_global_v8(dkp + 32 * c + 16, vb + 8);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              reinterpret_cast<uint4*>(dvp)[c * 4 + i] = make_uint4(va[4 * i], va[4 * i + 1], va[4 * i + 2], va[4 * i + 3]);
+              reinterpret_cast<uint4*>(dkp)[c * 4 + i] = make_uint4(vb[4 * i], vb[4 * i + 1], vb[4 * i + 2], vb[4 * i + 3]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive_warp(dkv_empty);
+      return true;
+    };
+    int pend_kr = -1;  // the unit whose dK / dV are still in TMEM
+    size_t pend_head = 0;
     for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units; ++rnd) {
       const int u = snake_unit(rnd);
       if (u >= p.num_units) continue;
@@ -472,6 +537,10 @@ __global__ void __launch_bounds__(384, 1)
         uint32_t pk[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(__uint_as_float(pv[2 * e]), __uint_as_float(pv[2 * e + 1]));
+        if (ii == 0 && pend_kr >= 0) {
+          ok = write_dkdv(pend_kr, pend_head);
+          if (!ok) break;
+        }
         // dS^T = P^T * (dP^T - D); P^T and dS^T packed over this warp's
         // dP^T columns of the region.
         ok = __all_sync(0xffffffffu, mbar_wait(&do_full[sd], (qc / C::kDoStages) & 1, ctl, kWaitBwdSoftmax));
@@ -508,41 +577,10 @@ __global__ void __launch_bounds__(384, 1)
         mbar_arrive_warp(&p_ready[reg]);
       }
       if (!ok) break;
-      // dK_j = scale * sum dS^T Q and dV_j = sum P^T dO of this unit; this
-      // warp writes head-dim columns [D/2 hc, D/2 hc + D/2).
-      ok = __all_sync(0xffffffffu, mbar_wait(dkv_full, uc & 1, ctl, kWaitBwdSoftmax));
-      ++uc;
-      if (!ok) break;
-      tc_fence_after();
-      __nv_bfloat16* dvp = reinterpret_cast<__nv_bfloat16*>(p.dv) + (head + kr) * D;
-      __nv_bfloat16* dkp = reinterpret_cast<__nv_bfloat16*>(p.dk) + (head + kr) * D;
-#pragma unroll 1
-      for (int c = hc * (D / 64); c < (hc + 1) * (D / 64); ++c) {
-        uint32_t a[32], b[32];
-        tmem_ld32(tmem + lane_off + C::kColDV + 32 * c, a);
-        tmem_ld32(tmem + lane_off + C::kColDK + 32 * c, b);
-        tmem_ld_wait<32>(a);
-        tmem_ld_wait<32>(b);
-        if (kr < p.N) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            uint4 va, vb;
-            va.x = pack_bf16(__uint_as_float(a[8 * i + 0]), __uint_as_float(a[8 * i + 1]));
-            va.y = pack_bf16(__uint_as_float(a[8 * i + 2]), __uint_as_float(a[8 * i + 3]));
-            va.z = pack_bf16(__uint_as_float(a[8 * i + 4]), __uint_as_float(a[8 * i + 5]));
-            va.w = pack_bf16(__uint_as_float(a[8 * i + 6]), __uint_as_float(a[8 * i + 7]));
-            vb.x = pack_bf16(__uint_as_float(b[8 * i + 0]) * p.scale, __uint_as_float(b[8 * i + 1]) * p.scale);
-            vb.y = pack_bf16(__uint_as_float(b[8 * i + 2]) * p.scale, __uint_as_float(b[8 * i + 3]) * p.scale);
-            vb.z = pack_bf16(__uint_as_float(b[8 * i + 4]) * p.scale, __uint_as_float(b[8 * i + 5]) * p.scale);
-            vb.w = pack_bf16(__uint_as_float(b[8 * i + 6]) * p.scale, __uint_as_float(b[8 * i + 7]) * p.scale);
-            reinterpret_cast<uint4*>(dvp)[c * 4 + i] = va;
-            reinterpret_cast<uint4*>(dkp)[c * 4 + i] = vb;
-          }
-        }
-      }
-      tc_fence_before();
-      mbar_arrive_warp(dkv_empty);
+      pend_kr = kr;
+      pend_head = head;
     }
+    if (ok && pend_kr >= 0) write_dkdv(pend_kr, pend_head);
   } else {
     reg_dealloc<R::kRegsCtl>();
   }
@@ -575,7 +613,7 @@ struct DqCfg {
   static constexpr int kOffK = 2 * kTileBytes;
   static constexpr int kOffV = kOffK + kKStages * kTileBytes;
   static constexpr int kOffBar = kOffV + kVStages * kTileBytes;
-  static constexpr int kNumBars = 2 + 2 * kKStages + 2 * kVStages + 9;
+  static constexpr int kNumBars = 4 + 2 * kKStages + 2 * kVStages + 9;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16;
   static_assert(kSmemBytes <= 232448, "shared memory");
 };
@@ -593,9 +631,13 @@ __global__ void __launch_bounds__(384, 1)
     return;
   }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
-  uint64_t* qdo_full = bars;
-  uint64_t* qdo_empty = bars + 1;
-  uint64_t* k_full = bars + 2;  // [kKStages]
+  // Q_i (read by S only) and dO_i (read by dP only) have separate barriers,
+  // so the next unit's tiles load as soon as the last S / dP was issued.
+  uint64_t* q_full = bars;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* do_full = bars + 2;
+  uint64_t* do_empty = bars + 3;
+  uint64_t* k_full = bars + 4;  // [kKStages]
   uint64_t* k_empty = k_full + C::kKStages;
   uint64_t* v_full = k_empty + C::kKStages;  // [kVStages]
   uint64_t* v_empty = v_full + C::kVStages;
@@ -612,8 +654,10 @@ __global__ void __launch_bounds__(384, 1)
   const int lane = threadIdx.x % 32;
 
   if (threadIdx.x == 0) {
-    mbar_init(qdo_full, 1);
-    mbar_init(qdo_empty, 2);  // the last S and the last dP of a unit
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);  // the unit's last S
+    mbar_init(do_full, 1);
+    mbar_init(do_empty, 1);  // the unit's last dP
     for (int s = 0; s < C::kKStages; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
@@ -659,14 +703,11 @@ __global__ void __launch_bounds__(384, 1)
         const int u = snake_unit(rnd);
         if (u >= p.num_units) continue;
         const BwdUnit w = decode_dq(p, u);
-        ok = mbar_wait(qdo_empty, (uc & 1) ^ 1, ctl, kWaitBwdLoad);
+        ok = mbar_wait(q_empty, (uc & 1) ^ 1, ctl, kWaitBwdLoad);
         if (!ok) break;
-        mbar_arrive_expect_tx(qdo_full, 2 * C::kTileBytes);
-        for (int c = 0; c < C::kChunks; ++c) {
-          tma_load_3d(smem + C::kOffQ + c * C::kChunkBytes, &tm_q, qdo_full, c * 64, w.t * kTileM, w.bh);
-          tma_load_3d(smem + C::kOffDO + c * C::kChunkBytes, &tm_do, qdo_full, c * 64, w.t * kTileM, w.bh);
-        }
-        ++uc;
+        mbar_arrive_expect_tx(q_full, C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(smem + C::kOffQ + c * C::kChunkBytes, &tm_q, q_full, c * 64, w.t * kTileM, w.bh);
         for (int jj = 0; ok && jj < w.count; ++jj, ++kc) {
           const int key0 = (w.first + jj) * kTileN;
           const uint32_t sk = kc % C::kKStages;
@@ -676,6 +717,14 @@ __global__ void __launch_bounds__(384, 1)
           for (int c = 0; c < C::kChunks; ++c)
             tma_load_3d(smem + C::kOffK + sk * C::kTileBytes + c * C::kChunkBytes, &tm_k, &k_full[sk], c * 64, key0,
                         w.bh);
+          if (jj == 0) {
+            // dO_i, needed by the first dP, after the first K.
+            ok = mbar_wait(do_empty, (uc & 1) ^ 1, ctl, kWaitBwdLoad);
+            if (!ok) break;
+            mbar_arrive_expect_tx(do_full, C::kTileBytes);
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_load_3d(smem + C::kOffDO + c * C::kChunkBytes, &tm_do, do_full, c * 64, w.t * kTileM, w.bh);
+          }
           const uint32_t sv = kc % C::kVStages;
           ok = mbar_wait(&v_empty[sv], ((kc / C::kVStages) & 1) ^ 1, ctl, kWaitBwdLoad);
           if (!ok) break;
@@ -684,9 +733,13 @@ __global__ void __launch_bounds__(384, 1)
             tma_load_3d(smem + C::kOffV + sv * C::kTileBytes + c * C::kChunkBytes, &tm_v, &v_full[sv], c * 64, key0,
                         w.bh);
         }
+        ++uc;
       }
       // Every copy this thread issued has landed before the CTA exits.
-      if (uc > 0) mbar_wait(qdo_full, (uc - 1) & 1, ctl, kWaitDrain);
+      if (uc > 0) {
+        mbar_wait(q_full, (uc - 1) & 1, ctl, kWaitDrain);
+        mbar_wait(do_full, (uc - 1) & 1, ctl, kWaitDrain);
+      }
       for (uint32_t pos = kc > (uint32_t)C::kKStages ? kc - C::kKStages : 0u; pos < kc; ++pos)
         mbar_wait(&k_full[pos % C::kKStages], (pos / C::kKStages) & 1, ctl, kWaitDrain);
       for (uint32_t pos = kc > (uint32_t)C::kVStages ? kc - C::kVStages : 0u; pos < kc; ++pos)
@@ -697,7 +750,8 @@ __global__ void __launch_bounds__(384, 1)
     // --------------------------------------------------------- MMA issuers
     // Two threads issue the products, each in its own order, so that one
     // thread's waits overlap the other's issue: warp 8 issues dP, warp 10
-    // issues dQ and S.  No product of one reads or writes TMEM columns the
+    // issues dQ and S (S into a buffer after the dQ that read it, in this
+    // thread's order).  No product of one reads or writes TMEM columns the
     // other's products touch; each thread's commits track its own products.
     reg_dealloc<R::kRegsCtl>();
     if (lane == 0) {
@@ -707,14 +761,14 @@ __global__ void __launch_bounds__(384, 1)
       const uint32_t sdo = smem_u32(smem + C::kOffDO);
       bool ok = true;
       if (warp == 8) {
-        // dP of every step, once the previous dP was read out; Q_i / dO_i
-        // are released (first of two arrivals) after the unit's last dP.
+        // dP of every step, once the previous dP was read out; dO_i is
+        // released after the unit's last dP.
         uint32_t uc = 0, kc = 0, dn = 0;
         for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units; ++rnd) {
           const int u = snake_unit(rnd);
           if (u >= p.num_units) continue;
           const BwdUnit w = decode_dq(p, u);
-          ok = mbar_wait(qdo_full, uc & 1, ctl, kWaitBwdMma);
+          ok = mbar_wait(do_full, uc & 1, ctl, kWaitBwdMma);
           ++uc;
           for (int jj = 0; ok && jj < w.count; ++jj, ++kc) {
             const uint32_t sv = kc % C::kVStages;
@@ -731,7 +785,7 @@ __global__ void __launch_bounds__(384, 1)
             }
             mma_commit(dp_full);
             mma_commit(&v_empty[sv]);
-            if (jj + 1 == w.count) mma_commit(qdo_empty);
+            if (jj + 1 == w.count) mma_commit(do_empty);
             ++dn;
           }
         }
@@ -741,8 +795,7 @@ __global__ void __launch_bounds__(384, 1)
         // S of the step at position `pos` into S buffer (pos & 1).  The
         // buffer last held the dS of step pos - 2, read by a dQ product
         // this thread issued earlier; its S was read before that dS was
-        // written.  `last`: the unit's last S, after which Q_i is released
-        // (second of two arrivals).
+        // written.  `last`: the unit's last S, after which Q_i is released.
         auto issue_s = [&](uint32_t pos, bool last) -> bool {
           const uint32_t sk = pos % C::kKStages;
           if (!mbar_wait(&k_full[sk], (pos / C::kKStages) & 1, ctl, kWaitBwdMma)) return false;
@@ -755,14 +808,14 @@ __global__ void __launch_bounds__(384, 1)
                    sdesc_sw128(sk_addr + off, 16, 1024), id_s, kk > 0 ? 1u : 0u);
           }
           mma_commit(&s_full[pos & 1]);
-          if (last) mma_commit(qdo_empty);
+          if (last) mma_commit(q_empty);
           return true;
         };
         for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units; ++rnd) {
           const int u = snake_unit(rnd);
           if (u >= p.num_units) continue;
           const BwdUnit w = decode_dq(p, u);
-          ok = mbar_wait(qdo_full, uc & 1, ctl, kWaitBwdMma);
+          ok = mbar_wait(q_full, uc & 1, ctl, kWaitBwdMma);
           if (!ok) break;
           tc_fence_after();
           ok = issue_s(kc, w.count == 1);
@@ -810,6 +863,39 @@ __global__ void __launch_bounds__(384, 1)
     const float sl2 = p.scale_log2;
     uint32_t uc = 0, kc = 0, dc = 0;
     bool ok = true;
+    // dQ_i = scale * sum dS K of a unit: lane = query row q of head `head`,
+    // this warp writes head-dim columns [D/2 hc, D/2 hc + D/2).  Run after
+    // the next unit's first P, while its dP is computed.
+    auto write_dq = [&](int q, size_t head) -> bool {
+      if (!__all_sync(0xffffffffu, mbar_wait(dq_full, uc & 1, ctl, kWaitBwdDq))) return false;
+      ++uc;
+      tc_fence_after();
+      uint32_t v[D / 2];
+      tmem_ld32(tmem + lane_off + C::kColDQ + (D / 2) * hc, v);
+      if constexpr (D == 128) tmem_ld32(tmem + lane_off + C::kColDQ + (D / 2) * hc + 32, v + 32);
+      tmem_ld_wait<D / 2>(v);
+      tc_fence_before();
+      mbar_arrive_warp(dq_empty);
+      if (q < p.N) {
+        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.dq) + (head + q) * D + (D / 2) * hc;
+        const float sc = p.scale;
+        uint32_t w[D / 4];
+#pragma unroll
+        for (int i = 0; i < D / 4; ++i)
+          w[i] = pack_bf16(__uint_as_float(v[2 * i]) * sc, __uint_as_float(v[2 * i + 1]) * sc);
+        if (p.store32) {
+#pragma unroll
+          for (int i = 0; i < D / 32; ++i) st_global_v8(dst + 16 * i, w + 8 * i);
+        } else {
+#pragma unroll
+          for (int i = 0; i < D / 16; ++i)
+            reinterpret_cast<uint4*>(dst)[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        }
+      }
+      return true;
+    };
+    int pend_q = -1;  // the unit whose dQ is still in TMEM
+    size_t pend_head = 0;
     for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units; ++rnd) {
       const int u = snake_unit(rnd);
       if (u >= p.num_units) continue;
@@ -833,6 +919,10 @@ __global__ void __launch_bounds__(384, 1)
           p64_rowL<true>(pv, L, sl2, q, k_first, p.N, p.causal != 0);
         else
           p64_rowL<false>(pv, L, sl2, q, k_first, p.N, false);
+        if (jj == 0 && pend_q >= 0) {
+          ok = write_dq(pend_q, pend_head);
+          if (!ok) break;
+        }
         ok = __all_sync(0xffffffffu, mbar_wait(dp_full, dc & 1, ctl, kWaitBwdSoftmax));
         ++dc;
         if (!ok) break;
@@ -862,29 +952,10 @@ __global__ void __launch_bounds__(384, 1)
         mbar_arrive_warp(&p_ready[kc & 1]);
       }
       if (!ok) break;
-      // dQ_i = scale * sum dS K of this unit: lane = query row, this warp
-      // writes head-dim columns [D/2 hc, D/2 hc + D/2).
-      ok = __all_sync(0xffffffffu, mbar_wait(dq_full, uc & 1, ctl, kWaitBwdDq));
-      ++uc;
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t v[D / 2];
-      tmem_ld32(tmem + lane_off + C::kColDQ + (D / 2) * hc, v);
-      if constexpr (D == 128) tmem_ld32(tmem + lane_off + C::kColDQ + (D / 2) * hc + 32, v + 32);
-      tmem_ld_wait<D / 2>(v);
-      tc_fence_before();
-      mbar_arrive_warp(dq_empty);
-      if (q < p.N) {
-        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.dq) + (head + q) * D + (D / 2) * hc);
-        const float sc = p.scale;
-#pragma unroll
-        for (int i = 0; i < D / 16; ++i)
-          dst[i] = make_uint4(pack_bf16(__uint_as_float(v[8 * i + 0]) * sc, __uint_as_float(v[8 * i + 1]) * sc),
-                              pack_bf16(__uint_as_float(v[8 * i + 2]) * sc, __uint_as_float(v[8 * i + 3]) * sc),
-                              pack_bf16(__uint_as_float(v[8 * i + 4]) * sc, __uint_as_float(v[8 * i + 5]) * sc),
-                              pack_bf16(__uint_as_float(v[8 * i + 6]) * sc, __uint_as_float(v[8 * i + 7]) * sc));
-      }
+      pend_q = q;
+      pend_head = head;
     }
+    if (ok && pend_q >= 0) write_dq(pend_q, pend_head);
   } else {
     reg_dealloc<R::kRegsCtl>();
   }
@@ -897,23 +968,33 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-// D_i = sum_c dO_ic * O_ic, one warp per row.
+// D_i = sum_c dO_ic * O_ic.  D/8 lanes per row, 16 bytes of O and of dO
+// per lane, so a warp reads 256 / D whole rows with 16-byte accesses.
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_preprocess(const __nv_bfloat16* __restrict__ o,
                                                          const __nv_bfloat16* __restrict__ dout,
                                                          float* __restrict__ dvec, int rows) {
-  const int row = blockIdx.x * 8 + threadIdx.x / 32;
-  const int lane = threadIdx.x % 32;
-  if (row >= rows) return;
-  constexpr int kPer = D / 32;
-  const __nv_bfloat16* a = o + (size_t)row * D + lane * kPer;
-  const __nv_bfloat16* b = dout + (size_t)row * D + lane * kPer;
+  constexpr int kLanes = D / 8;                 // lanes per row
+  constexpr int kRowsPerBlock = 256 / kLanes;
+  const int row = blockIdx.x * kRowsPerBlock + threadIdx.x / kLanes;
+  const int part = threadIdx.x % kLanes;
   float acc = 0.f;
+  if (row < rows) {
+    const uint4 a = reinterpret_cast<const uint4*>(o + (size_t)row * D)[part];
+    const uint4 b = reinterpret_cast<const uint4*>(dout + (size_t)row * D)[part];
+    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
 #pragma unroll
-  for (int i = 0; i < kPer; ++i) acc = fmaf(__bfloat162float(a[i]), __bfloat162float(b[i]), acc);
+    for (int i = 0; i < 4; ++i) {
+      const float2 x = __bfloat1622float2(a2[i]);
+      const float2 y = __bfloat1622float2(b2[i]);
+      acc = fmaf(x.x, y.x, acc);
+      acc = fmaf(x.y, y.y, acc);
+    }
+  }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) dvec[row] = acc;
+  for (int off = kLanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (row < rows && part == 0) dvec[row] = acc;
 }
 
 // A wait on an mbarrier that nothing arrives on: exercises the give-up path.
@@ -966,7 +1047,8 @@ cudaError_t launch_bwd_dq(int d, const CUtensorMap& tq, const CUtensorMap& tk, c
 
 cudaError_t launch_bwd_preprocess(int d, const void* o, const void* dout, float* dvec, int rows,
                                   cudaStream_t stream) {
-  const int grid = (rows + 7) / 8;
+  const int per_block = 256 / (d / 8);  // rows per 256-thread block
+  const int grid = (rows + per_block - 1) / per_block;
   const auto* po = static_cast<const __nv_bfloat16*>(o);
   const auto* pd = static_cast<const __nv_bfloat16*>(dout);
   if (d == 64)

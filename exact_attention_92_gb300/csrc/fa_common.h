@@ -65,6 +65,7 @@ struct BwdParams {
   void* dq;                    // bf16 [B,H,N,d]
   void* dk;                    // bf16 [B,H,N,d]
   void* dv;                    // bf16 [B,H,N,d]
+  int store32;                 // dq, dk, dv all 32-byte aligned: 32-byte stores
   int num_tiles;               // ceil(N / 128): key tiles = query tiles
   int num_units;               // B*H*num_tiles (both kernels)
   unsigned int* status;

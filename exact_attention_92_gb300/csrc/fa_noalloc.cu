@@ -107,6 +107,8 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
   p.dq = dq;
   p.dk = dk;
   p.dv = dv;
+  p.store32 = ((reinterpret_cast<uintptr_t>(dq) | reinterpret_cast<uintptr_t>(dk) |
+                reinterpret_cast<uintptr_t>(dv)) & 31u) == 0 ? 1 : 0;
   p.num_tiles = (N + 127) / 128;
   p.num_units = BH * p.num_tiles;
   p.status = status;
