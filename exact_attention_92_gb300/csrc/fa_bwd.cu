@@ -169,6 +169,51 @@ __device__ __forceinline__ void p64_rowL(uint32_t* s, float L, float sl2, int q,
   }
 }
 
+// Stores one segment of 32 * U bytes per lane (w: 8 * U words) at
+// row_ptr, the lane's own row; rows of the warp are `stride` bytes apart and
+// the lane's row is `row`; rows >= `rows` are not written.  A warp store
+// with one row per lane would touch 32 lines per instruction; here the
+// 32-byte units are first transposed inside each group of U lanes (a
+// butterfly over shuffles) so that every store instruction writes U
+// consecutive units of one row per group: 32 / U whole segments.  store32:
+// 32-byte stores (the buffer is 32-byte aligned), else pairs of 16-byte ones.
+// Every lane of the warp must call it.
+template <int U>
+__device__ __forceinline__ void store_rows(uint8_t* row_ptr, size_t stride, int row, int rows, uint32_t* w,
+                                           bool store32) {
+  const int l = threadIdx.x & (U - 1);
+#pragma unroll
+  for (int b = 1; b < U; b <<= 1) {
+    const bool hi = (l & b) != 0;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (u & b) continue;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint32_t send = hi ? w[8 * u + k] : w[8 * (u | b) + k];
+        const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, b);
+        if (hi)
+          w[8 * u + k] = recv;
+        else
+          w[8 * (u | b) + k] = recv;
+      }
+    }
+  }
+  // Slot s now holds unit l of row (row - l + s).
+#pragma unroll
+  for (int s = 0; s < U; ++s) {
+    if (row - l + s < rows) {
+      uint8_t* dst = row_ptr + (ptrdiff_t)(s - l) * (ptrdiff_t)stride + 32 * l;
+      if (store32) {
+        st_global_v8(dst, w + 8 * s);
+      } else {
+        reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[8 * s], w[8 * s + 1], w[8 * s + 2], w[8 * s + 3]);
+        reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[8 * s + 4], w[8 * s + 5], w[8 * s + 6], w[8 * s + 7]);
+      }
+    }
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(384, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -463,41 +508,31 @@ __global__ void __launch_bounds__(384, 1)
       if (!__all_sync(0xffffffffu, mbar_wait(dkv_full, uc & 1, ctl, kWaitBwdSoftmax))) return false;
       ++uc;
       tc_fence_after();
-      __nv_bfloat16* dvp = reinterpret_cast<__nv_bfloat16*>(p.dv) + (head + kr) * D;
-      __nv_bfloat16* dkp = reinterpret_cast<__nv_bfloat16*>(p.dk) + (head + kr) * D;
-#pragma unroll 1
-      for (int c = hc * (D / 64); c < (hc + 1) * (D / 64); ++c) {
-        uint32_t a[32], b[32];
-        tmem_ld32(tmem + lane_off + C::kColDV + 32 * c, a);
-        tmem_ld32(tmem + lane_off + C::kColDK + 32 * c, b);
-        tmem_ld_wait<32>(a);
-        tmem_ld_wait<32>(b);
-        if (kr < p.N) {
-          // One row of 32 columns per tensor: 64 bytes, as two 32-byte
-          // stores when the buffers allow it (a warp store then fills whole
-          // 32-byte sectors of 32 rows).
-          uint32_t va[16], vb[16];
+      // This warp's half row (D/2 columns) of dV and of dK, packed to bf16
+      // and released from TMEM before any store is issued, so that the next
+      // unit's accumulation does not wait behind the stores.
+      uint32_t w[2][D / 4];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            va[i] = pack_bf16(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
-            vb[i] = pack_bf16(__uint_as_float(b[2 * i]) * p.scale, __uint_as_float(b[2 * i + 1]) * p.scale);
-          }
-          if (p.store32) {
-            st_global_v8(dvp + 32 * c, va);
-            st_global_v8(dvp + 32 * c + 16, va + 8);
-            st_global_v8(dkp + 32 * c, vb);
-            st_global_v8(dkp + 32 * c + 16, vb + 8);
-          } else {
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t col = (which ? C::kColDK : C::kColDV) + (D / 2) * hc;
+        const float sc = which ? p.scale : 1.f;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              reinterpret_cast<uint4*>(dvp)[c * 4 + i] = make_uint4(va[4 * i], va[4 * i + 1], va[4 * i + 2], va[4 * i + 3]);
-              reinterpret_cast<uint4*>(dkp)[c * 4 + i] = make_uint4(vb[4 * i], vb[4 * i + 1], vb[4 * i + 2], vb[4 * i + 3]);
-            }
-          }
+        for (int c = 0; c < D / 64; ++c) {
+          uint32_t a[32];
+          tmem_ld32(tmem + lane_off + col + 32 * c, a);
+          tmem_ld_wait<32>(a);
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            w[which][16 * c + i] = pack_bf16(__uint_as_float(a[2 * i]) * sc, __uint_as_float(a[2 * i + 1]) * sc);
         }
       }
       tc_fence_before();
       mbar_arrive_warp(dkv_empty);
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(which ? p.dk : p.dv) + (head + kr) * D + (D / 2) * hc;
+        store_rows<D / 32>(reinterpret_cast<uint8_t*>(dst), (size_t)D * 2, kr, p.N, w[which], p.store32 != 0);
+      }
       return true;
     };
     int pend_kr = -1;  // the unit whose dK / dV are still in TMEM
@@ -534,13 +569,13 @@ __global__ void __launch_bounds__(384, 1)
           else
             p64_colL<false>(pv, bl, sl2, kr, qf, false, false);
         }
-        uint32_t pk[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(__uint_as_float(pv[2 * e]), __uint_as_float(pv[2 * e + 1]));
         if (ii == 0 && pend_kr >= 0) {
           ok = write_dkdv(pend_kr, pend_head);
           if (!ok) break;
         }
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(__uint_as_float(pv[2 * e]), __uint_as_float(pv[2 * e + 1]));
         // dS^T = P^T * (dP^T - D); P^T and dS^T packed over this warp's
         // dP^T columns of the region.
         ok = __all_sync(0xffffffffu, mbar_wait(&do_full[sd], (qc / C::kDoStages) & 1, ctl, kWaitBwdSoftmax));
@@ -876,20 +911,25 @@ __global__ void __launch_bounds__(384, 1)
       tmem_ld_wait<D / 2>(v);
       tc_fence_before();
       mbar_arrive_warp(dq_empty);
-      if (q < p.N) {
+      {
         __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.dq) + (head + q) * D + (D / 2) * hc;
         const float sc = p.scale;
         uint32_t w[D / 4];
 #pragma unroll
         for (int i = 0; i < D / 4; ++i)
           w[i] = pack_bf16(__uint_as_float(v[2 * i]) * sc, __uint_as_float(v[2 * i + 1]) * sc);
-        if (p.store32) {
+        // One row per lane here: the dQ stores follow the TMEM release and
+        // overlap the next unit's first steps, and the shuffles of
+        // store_rows measured slower than the scattered lines they save.
+        if (q < p.N) {
+          if (p.store32) {
 #pragma unroll
-          for (int i = 0; i < D / 32; ++i) st_global_v8(dst + 16 * i, w + 8 * i);
-        } else {
+            for (int i = 0; i < D / 32; ++i) st_global_v8(dst + 16 * i, w + 8 * i);
+          } else {
 #pragma unroll
-          for (int i = 0; i < D / 16; ++i)
-            reinterpret_cast<uint4*>(dst)[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+            for (int i = 0; i < D / 16; ++i)
+              reinterpret_cast<uint4*>(dst)[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          }
         }
       }
       return true;
