@@ -16,7 +16,7 @@
 
 namespace fa {
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& to, const FwdParams& p, int grid, cudaStream_t stream);
+                       const FwdParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_combine(int d, const CombineParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const BwdParams& p, int grid, cudaStream_t stream);
@@ -302,9 +302,8 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
   const int per_split = (nkv + S - 1) / S;
   S = (nkv + per_split - 1) / per_split;  // no empty split
 
-  CUtensorMap tq, tk, tv, to;
-  if (encode_bhnd(&tq, q, BH, N, d) || encode_bhnd(&tk, k, BH, N, d) || encode_bhnd(&tv, v, BH, N, d) ||
-      encode_bhnd(&to, o, BH, N, d))
+  CUtensorMap tq, tk, tv;
+  if (encode_bhnd(&tq, q, BH, N, d) || encode_bhnd(&tk, k, BH, N, d) || encode_bhnd(&tv, v, BH, N, d))
     return FA_ERR_CUDA;
 
   FwdParams p;
@@ -320,6 +319,7 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
   p.num_units = BH * p.num_q_blocks * S;
   p.o = o;
   p.lse = lse;
+  p.store32 = (reinterpret_cast<uintptr_t>(o) & 31) == 0 ? 1 : 0;
   p.status = s->status;
   p.timeout_ns = g_timeout_ns.load();
 
@@ -335,7 +335,7 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
     p.lse_part = p.o_part + (size_t)S * rows * d;
   }
   const int grid = p.num_units < s->sm_count ? p.num_units : s->sm_count;
-  cudaError_t ce = timed(FA_KERNEL_FWD, st, [&] { return fa::launch_fwd(d, tq, tk, tv, to, p, grid, st); });
+  cudaError_t ce = timed(FA_KERNEL_FWD, st, [&] { return fa::launch_fwd(d, tq, tk, tv, p, grid, st); });
   if (ce == cudaSuccess && S > 1) {
     fa::CombineParams c;
     c.rows = (int)rows;

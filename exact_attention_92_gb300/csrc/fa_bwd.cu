@@ -169,51 +169,6 @@ __device__ __forceinline__ void p64_rowL(uint32_t* s, float L, float sl2, int q,
   }
 }
 
-// Stores one segment of 32 * U bytes per lane (w: 8 * U words) at
-// row_ptr, the lane's own row; rows of the warp are `stride` bytes apart and
-// the lane's row is `row`; rows >= `rows` are not written.  A warp store
-// with one row per lane would touch 32 lines per instruction; here the
-// 32-byte units are first transposed inside each group of U lanes (a
-// butterfly over shuffles) so that every store instruction writes U
-// consecutive units of one row per group: 32 / U whole segments.  store32:
-// 32-byte stores (the buffer is 32-byte aligned), else pairs of 16-byte ones.
-// Every lane of the warp must call it.
-template <int U>
-__device__ __forceinline__ void store_rows(uint8_t* row_ptr, size_t stride, int row, int rows, uint32_t* w,
-                                           bool store32) {
-  const int l = threadIdx.x & (U - 1);
-#pragma unroll
-  for (int b = 1; b < U; b <<= 1) {
-    const bool hi = (l & b) != 0;
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      if (u & b) continue;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint32_t send = hi ? w[8 * u + k] : w[8 * (u | b) + k];
-        const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, b);
-        if (hi)
-          w[8 * u + k] = recv;
-        else
-          w[8 * (u | b) + k] = recv;
-      }
-    }
-  }
-  // Slot s now holds unit l of row (row - l + s).
-#pragma unroll
-  for (int s = 0; s < U; ++s) {
-    if (row - l + s < rows) {
-      uint8_t* dst = row_ptr + (ptrdiff_t)(s - l) * (ptrdiff_t)stride + 32 * l;
-      if (store32) {
-        st_global_v8(dst, w + 8 * s);
-      } else {
-        reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[8 * s], w[8 * s + 1], w[8 * s + 2], w[8 * s + 3]);
-        reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[8 * s + 4], w[8 * s + 5], w[8 * s + 6], w[8 * s + 7]);
-      }
-    }
-  }
-}
-
 template <int D>
 __global__ void __launch_bounds__(384, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,

@@ -42,6 +42,7 @@ struct FwdParams {
   float* lse;                  // fp32 [B,H,N]              (num_splits == 1)
   float* o_part;               // fp32 [S,B,H,N,d]          (num_splits > 1)
   float* lse_part;             // fp32 [S,B,H,N]            (num_splits > 1)
+  int store32;                 // o is 32-byte aligned: 32-byte stores
   unsigned int* status;
   unsigned long long timeout_ns;
 };

@@ -6,13 +6,15 @@
 // query tiles Q0, Q1 that stay in shared memory (loaded once, section 2.3)
 // and share one stream of 128-key K/V tiles (the inner loop).  Roles:
 //   warp 9     TMA producer: Q tiles, then K_j, V_j into a ring of slots.
-//              A Q buffer is refilled once the softmax warps have stored
-//              that tile's O through it (O is staged there for a TMA store).
+//              A Q buffer is refilled as soon as the last S product that
+//              reads it has completed, so the next unit's Q, K and V arrive
+//              while the current unit's last steps run.
 //   warp 8     MMA issuer (one thread): S_t = Q_t K_j^T and O_t += P_t V_j
 //              with tcgen05 into tensor memory (TMEM).
 //   warps 0-3  softmax of query tile 0, warps 4-7 of tile 1: each thread owns
 //              one query row (the "split along Q" of section 4.2), so row max
-//              and row sum need no communication.
+//              and row sum need no communication.  They also write O and L
+//              straight from registers at the end of the unit.
 // TMEM (512 columns): S0 | S1 | O0 | O1.  P (bf16) overwrites the first half
 // of its own S columns and feeds the PV MMA straight from TMEM.
 //
@@ -51,7 +53,7 @@ struct FwdCfg {
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = 2 * kTileBytes;
   static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
-  static constexpr int kNumBars = 2 + 2 + 2 * kStages + 2 + 2 + 2 + 1 + 2;
+  static constexpr int kNumBars = 2 + 2 + 2 * kStages + 2 + 2 + 2 + 1;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16;
   static constexpr float kRescaleThreshold = 8.0f;     // log2 units
   // Register split (setmaxnreg).  At 384 threads and one CTA per SM each
@@ -131,8 +133,7 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint3
 template <int D>
 __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                  const FwdParams p) {
+                  const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
   using C = FwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   // The 128-byte swizzle anchors at 1024-byte boundaries: refuse to run (and
@@ -152,8 +153,7 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* p_full = s_full + 2;
   uint64_t* o_full = p_full + 2;
   uint64_t* drain = o_full + 2;
-  uint64_t* o_staged = drain + 1;  // [2]: a tile's O rows written to its staging buffer
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_staged + 2);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -165,7 +165,6 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 4);
       mbar_init(&o_full[i], 1);
-      mbar_init(&o_staged[i], 4);
     }
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&kv_full[i], 1);
@@ -182,7 +181,6 @@ __global__ void __launch_bounds__(384, 1)
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
-    tma_prefetch_desc(&tm_o);
   }
   tc_fence_before();
   __syncthreads();
@@ -267,6 +265,7 @@ __global__ void __launch_bounds__(384, 1)
             if (w.n[t] == 0) continue;
             issue_qk<D>(tmem + C::col_s(t), q_lo0 + t * kTileStep, k_lo0 + slot_k * kTileStep, hi);
             mma_commit(&s_full[t]);
+            if (w.n[t] == 1) mma_commit(&q_empty[t]);  // Q_t's last product
           }
           mma_commit(&kv_empty[slot_k]);
         }
@@ -295,9 +294,8 @@ __global__ void __launch_bounds__(384, 1)
               }
               issue_qk<D>(tmem + C::col_s(t), q_lo0 + t * kTileStep, k_lo0 + slot_k * kTileStep, hi);
               mma_commit(&s_full[t]);
+              if (j + 2 == w.n[t]) mma_commit(&q_empty[t]);  // Q_t's last product
             } else {
-              // Q_t is released by the softmax warps once O_t, staged in
-              // Q_t's buffer, has been stored.
               mma_commit(&o_full[t]);
             }
           }
@@ -436,48 +434,28 @@ __global__ void __launch_bounds__(384, 1)
       const float inv_l = 1.0f / l;
       const float lse = (m_ref + lg2_approx(l)) * 0.69314718055994530942f;
       if (p.num_splits == 1) {
-        // O rows -> Q_t's buffer (no longer read: every S_t MMA finished
-        // before O_t did) in the 128-byte-swizzled layout of the tensor map,
-        // then one TMA store per 64 columns; rows past N are clipped by the
-        // copy.
-        uint8_t* stg = sQ + t * C::kTileBytes;
+        // O = O~ / l in bf16, 64 columns (128 bytes of the row) at a time,
+        // stored with whole row segments per warp store; rows past N are
+        // skipped.
+        uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) + ((size_t)w.bh * p.N + row) * (D * 2);
+        const float2 il = make_float2(inv_l, inv_l);
+#pragma unroll 1
+        for (int hb = 0; hb < D / 64; ++hb) {
+          uint32_t ob[32];
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + 32 * c, o);
-          tmem_ld_wait<32>(o);
-          uint8_t* rowp = stg + (c / 2) * C::kChunkBytes + r_in_tile * 128;
+          for (int c = 0; c < 2; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + 64 * hb + 32 * c, o);
+            tmem_ld_wait<32>(o);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float2 il = make_float2(inv_l, inv_l);
-            const float2 a = __fmul2_rn(make_float2(__uint_as_float(o[8 * i + 0]), __uint_as_float(o[8 * i + 1])), il);
-            const float2 b = __fmul2_rn(make_float2(__uint_as_float(o[8 * i + 2]), __uint_as_float(o[8 * i + 3])), il);
-            const float2 e = __fmul2_rn(make_float2(__uint_as_float(o[8 * i + 4]), __uint_as_float(o[8 * i + 5])), il);
-            const float2 g = __fmul2_rn(make_float2(__uint_as_float(o[8 * i + 6]), __uint_as_float(o[8 * i + 7])), il);
-            const int unit = (c % 2) * 4 + i;
-            *reinterpret_cast<uint4*>(rowp + ((unit ^ (r_in_tile & 7)) << 4)) =
-                make_uint4(pack_bf16(a.x, a.y), pack_bf16(b.x, b.y), pack_bf16(e.x, e.y), pack_bf16(g.x, g.y));
-          }
-        }
-        fence_proxy_async_smem();
-        mbar_arrive_warp(&o_staged[t]);
-        if (row < p.N) p.lse[(size_t)w.bh * p.N + row] = lse;
-        if ((warp & 3) == 0) {
-          bool sent = true;
-          if (lane == 0) {
-            sent = mbar_wait(&o_staged[t], stc & 1, ctl, kWaitOFull);
-            if (sent) {
-              for (int c = 0; c < C::kChunks; ++c)
-                tma_store_3d(&tm_o, stg + c * C::kChunkBytes, c * 64, row0, w.bh);
-              bulk_commit();
-              // The buffer takes the next unit's Q_t once the store has read it.
-              bulk_wait_read_all();
-              mbar_arrive(&q_empty[t]);
+            for (int i = 0; i < 16; ++i) {
+              const float2 a = __fmul2_rn(make_float2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), il);
+              ob[16 * c + i] = pack_bf16(a.x, a.y);
             }
           }
-          ok = __shfl_sync(0xffffffffu, sent, 0);
+          store_rows<4>(orow + 128 * hb, (size_t)D * 2, row, p.N, ob, p.store32 != 0);
         }
-        ++stc;
+        if (row < p.N) p.lse[(size_t)w.bh * p.N + row] = lse;
       } else {
         const size_t prow = ((size_t)split * p.B * p.H + w.bh) * p.N + row;
         float4* dst = reinterpret_cast<float4*>(p.o_part + prow * D);
@@ -495,12 +473,8 @@ __global__ void __launch_bounds__(384, 1)
           }
         }
         if (row < p.N) p.lse_part[prow] = lse;
-        // Q_t's buffer is free: every S_t MMA completed before O_t did.
-        if ((warp & 3) == 0 && lane == 0) mbar_arrive(&q_empty[t]);
       }
     }
-    // Every O store this warpgroup issued has landed before the CTA exits.
-    if ((warp & 3) == 0 && lane == 0) bulk_wait_all();
     __syncwarp();
   } else {
     reg_dealloc<C::kRegsCtl>();
@@ -553,18 +527,17 @@ __global__ void __launch_bounds__(256) fa_combine_kernel(const CombineParams p) 
 
 template <int D>
 static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                                const CUtensorMap& to, const FwdParams& p, int grid, cudaStream_t stream) {
+                                const FwdParams& p, int grid, cudaStream_t stream) {
   using C = FwdCfg<D>;
   cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  fa_fwd_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, to, p);
+  fa_fwd_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& to, const FwdParams& p, int grid, cudaStream_t stream) {
-  return d == 64 ? launch_fwd_t<64>(tq, tk, tv, to, p, grid, stream)
-                 : launch_fwd_t<128>(tq, tk, tv, to, p, grid, stream);
+                       const FwdParams& p, int grid, cudaStream_t stream) {
+  return d == 64 ? launch_fwd_t<64>(tq, tk, tv, p, grid, stream) : launch_fwd_t<128>(tq, tk, tv, p, grid, stream);
 }
 
 cudaError_t launch_combine(int d, const CombineParams& p, cudaStream_t stream) {

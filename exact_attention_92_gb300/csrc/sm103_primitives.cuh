@@ -347,7 +347,6 @@ __device__ __forceinline__ void bulk_wait_read_all() {
 // Wait until every committed bulk store has completed.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
-// Two floats to packed bf16 (round to nearest even); `lo` in bits [0,16).
 // 32-byte global store (address 32-byte aligned).
 __device__ __forceinline__ void st_global_v8(void* p, const uint32_t* r) {
   asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(r[0]), "r"(r[1]),
@@ -355,6 +354,51 @@ __device__ __forceinline__ void st_global_v8(void* p, const uint32_t* r) {
                : "memory");
 }
 
+// Stores one segment of 32 * U bytes per lane (w: 8 * U words) at
+// row_ptr, the lane's own row; rows of the warp are `stride` bytes apart and
+// the lane's row is `row`; rows >= `rows` are not written.  A warp store
+// with one row per lane would touch 32 lines per instruction; here the
+// 32-byte units are first transposed inside each group of U lanes (a
+// butterfly over shuffles) so that every store instruction writes U
+// consecutive units of one row per group: 32 / U whole segments.  store32:
+// 32-byte stores (the buffer is 32-byte aligned), else pairs of 16-byte ones.
+// Every lane of the warp must call it.
+template <int U>
+__device__ __forceinline__ void store_rows(uint8_t* row_ptr, size_t stride, int row, int rows, uint32_t* w,
+                                           bool store32) {
+  const int l = threadIdx.x & (U - 1);
+#pragma unroll
+  for (int b = 1; b < U; b <<= 1) {
+    const bool hi = (l & b) != 0;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (u & b) continue;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        // Register selects only (no runtime index into w).
+        const uint32_t lo_v = w[8 * u + k], hi_v = w[8 * (u | b) + k];
+        const uint32_t recv = __shfl_xor_sync(0xffffffffu, hi ? lo_v : hi_v, b);
+        w[8 * u + k] = hi ? recv : lo_v;
+        w[8 * (u | b) + k] = hi ? hi_v : recv;
+      }
+    }
+  }
+  // Slot s now holds unit l of row (row - l + s).
+#pragma unroll
+  for (int s = 0; s < U; ++s) {
+    if (row - l + s < rows) {
+      uint8_t* dst = row_ptr + (ptrdiff_t)(s - l) * (ptrdiff_t)stride + 32 * l;
+      if (store32) {
+        st_global_v8(dst, w + 8 * s);
+      } else {
+        reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[8 * s], w[8 * s + 1], w[8 * s + 2], w[8 * s + 3]);
+        reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[8 * s + 4], w[8 * s + 5], w[8 * s + 6], w[8 * s + 7]);
+      }
+    }
+  }
+}
+
+// Two floats to packed bf16 (round to nearest even); `lo` in bits [0,16).
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
