@@ -115,7 +115,7 @@ __device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint32_t q_lo, uint32_
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint32_t off = ((kk / 4) * C::kChunkBytes + (kk % 4) * 32) >> 4;
-    mma_ss_lh(tmem_s, q_lo + off, hi, k_lo + off, hi, idesc, kk > 0 ? 1u : 0u);
+    mma_ss_lh_w(tmem_s, q_lo + off, hi, k_lo + off, hi, idesc, kk > 0 ? 1u : 0u);
   }
 }
 
@@ -127,7 +127,7 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint3
   constexpr uint32_t idesc = idesc_bf16(kTileM, D, false, true);
 #pragma unroll
   for (int kk = 0; kk < kTileN / 16; ++kk)
-    mma_ts_lh(tmem_o, tmem_p + kk * 8, v_lo + ((kk * 2048) >> 4), hi, idesc, (accumulate || kk > 0) ? 1u : 0u);
+    mma_ts_lh_w(tmem_o, tmem_p + kk * 8, v_lo + ((kk * 2048) >> 4), hi, idesc, (accumulate || kk > 0) ? 1u : 0u);
 }
 
 template <int D>
@@ -233,7 +233,9 @@ __global__ void __launch_bounds__(384, 1)
   } else if (warp == 8) {
     reg_dealloc<C::kRegsCtl>();
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    // The whole warp walks the schedule (operands stay warp-uniform); one
+    // elected lane issues each tcgen05.mma / commit.
+    {
       // Descriptor low halves: buffer i of a kind is (i * tile bytes) / 16
       // past the first; V differs from K only in its leading byte offset.
       constexpr uint32_t hi = sdesc_hi(1024);
@@ -252,62 +254,62 @@ __global__ void __launch_bounds__(384, 1)
         if (nmax == 0) continue;
         for (int t = 0; ok && t < 2; ++t) {
           if (w.n[t] == 0) continue;
-          ok = mbar_wait(&q_full[t], qc[t] & 1, ctl, kWaitQFull);
+          ok = __all_sync(0xffffffffu, mbar_wait(&q_full[t], qc[t] & 1, ctl, kWaitQFull));
           ++qc[t];
         }
         if (!ok) break;
         {
           const uint32_t slot_k = rc % C::kStages;
-          ok = mbar_wait(&kv_full[slot_k], (rc / C::kStages) & 1, ctl, kWaitKvFull);
+          ok = __all_sync(0xffffffffu, mbar_wait(&kv_full[slot_k], (rc / C::kStages) & 1, ctl, kWaitKvFull));
           if (!ok) break;
           tc_fence_after();
           for (int t = 0; t < 2; ++t) {
             if (w.n[t] == 0) continue;
             issue_qk<D>(tmem + C::col_s(t), q_lo0 + t * kTileStep, k_lo0 + slot_k * kTileStep, hi);
-            mma_commit(&s_full[t]);
-            if (w.n[t] == 1) mma_commit(&q_empty[t]);  // Q_t's last product
+            mma_commit_w(&s_full[t]);
+            if (w.n[t] == 1) mma_commit_w(&q_empty[t]);  // Q_t's last product
           }
-          mma_commit(&kv_empty[slot_k]);
+          mma_commit_w(&kv_empty[slot_k]);
         }
         for (int j = 0; ok && j < nmax; ++j) {
           const uint32_t pos_v = rc + 2 * j + 1;
           const uint32_t pos_k = pos_v + 1;
           const uint32_t slot_v = pos_v % C::kStages;
           const uint32_t slot_k = pos_k % C::kStages;
-          ok = mbar_wait(&kv_full[slot_v], (pos_v / C::kStages) & 1, ctl, kWaitKvFull);
+          ok = __all_sync(0xffffffffu, mbar_wait(&kv_full[slot_v], (pos_v / C::kStages) & 1, ctl, kWaitKvFull));
           if (!ok) break;
           tc_fence_after();
           bool k_ready = false;
           for (int t = 0; t < 2; ++t) {
             if (j >= w.n[t]) continue;
-            ok = mbar_wait(&p_full[t], pc[t] & 1, ctl, kWaitPFull);
+            ok = __all_sync(0xffffffffu, mbar_wait(&p_full[t], pc[t] & 1, ctl, kWaitPFull));
             ++pc[t];
             if (!ok) break;
             tc_fence_after();
             issue_pv<D>(tmem + C::col_o(t), tmem + C::col_s(t), v_lo0 + slot_v * kTileStep, hi, j > 0);
             if (j + 1 < w.n[t]) {
               if (!k_ready) {
-                ok = mbar_wait(&kv_full[slot_k], (pos_k / C::kStages) & 1, ctl, kWaitKvFull);
+                ok = __all_sync(0xffffffffu, mbar_wait(&kv_full[slot_k], (pos_k / C::kStages) & 1, ctl, kWaitKvFull));
                 if (!ok) break;
                 tc_fence_after();
                 k_ready = true;
               }
               issue_qk<D>(tmem + C::col_s(t), q_lo0 + t * kTileStep, k_lo0 + slot_k * kTileStep, hi);
-              mma_commit(&s_full[t]);
-              if (j + 2 == w.n[t]) mma_commit(&q_empty[t]);  // Q_t's last product
+              mma_commit_w(&s_full[t]);
+              if (j + 2 == w.n[t]) mma_commit_w(&q_empty[t]);  // Q_t's last product
             } else {
-              mma_commit(&o_full[t]);
+              mma_commit_w(&o_full[t]);
             }
           }
           if (!ok) break;
-          mma_commit(&kv_empty[slot_v]);
-          if (j + 1 < nmax) mma_commit(&kv_empty[slot_k]);
+          mma_commit_w(&kv_empty[slot_v]);
+          if (j + 1 < nmax) mma_commit_w(&kv_empty[slot_k]);
         }
         rc += 2 * nmax;
       }
-      // Every MMA this thread issued completes before TMEM is released.
-      mma_commit(drain);
-      mbar_wait(drain, 0, ctl, kWaitDrain);
+      // Every MMA this warp issued completes before TMEM is released.
+      mma_commit_w(drain);
+      (void)__all_sync(0xffffffffu, mbar_wait(drain, 0, ctl, kWaitDrain));
     }
     __syncwarp();
   } else if (warp < 8) {
@@ -319,7 +321,7 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t tO = tmem + lane_off + C::col_o(t);
     const int r_in_tile = 32 * (warp & 3) + lane;
     const float sl2 = p.scale_log2;
-    uint32_t sc = 0, oc = 0, stc = 0;
+    uint32_t sc = 0, oc = 0;
     bool ok = true;
     for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units; ++rnd) {
       const int u = snake_unit(rnd);
