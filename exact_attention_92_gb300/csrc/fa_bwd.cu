@@ -25,11 +25,12 @@
 //
 // Roles (384 threads, three warpgroups, registers split with setmaxnreg as
 // in the forward kernel): warp 9 loads (TMA), warps 8 and 10 issue tcgen05
-// MMAs (two issuers, split so that neither's products touch the TMEM
-// columns of the other's: a single issuing thread spends about 46 cycles per
-// MMA and one to two hundred per barrier wait, which the two overlap), warp
-// 11 idle, warps 0-7 do the element-wise work (a TMEM lane per thread; warps
-// w and w+4 split the 128 columns of a tile) and write the results.
+// MMAs (two issuing warps, split so that neither's products touch the TMEM
+// columns of the other's, so that one's barrier waits overlap the other's
+// issue; each walks its schedule as a whole warp and an elected lane issues
+// every MMA and commit), warp 11 idle, warps 0-7 do the element-wise work (a
+// TMEM lane per thread; warps w and w+4 split the 128 columns of a tile) and
+// write the results.
 //
 // Pipelining.  The element-wise warps read a tile of S into registers and
 // compute P from it while the tensor core runs other products; they read dP
@@ -345,7 +346,7 @@ __global__ void __launch_bounds__(384, 1)
     // region, so the tensor pipe's issue order keeps S^T behind the products
     // that read the region.
     reg_dealloc<R::kRegsCtl>();
-    if (lane == 0) {
+    {
       constexpr uint32_t id_s = idesc_bf16(kTileM, kTileM, false, false);  // S^T, dP^T
       constexpr uint32_t id_kv = idesc_bf16(kTileM, D, false, true);       // dV, dK
       const uint32_t sk = smem_u32(smem + C::kOffK);
@@ -357,27 +358,27 @@ __global__ void __launch_bounds__(384, 1)
           const int u = snake_unit(rnd);
           if (u >= p.num_units) continue;
           const BwdUnit w = decode_dkdv(p, u);
-          ok = mbar_wait(v_full, kc & 1, ctl, kWaitBwdMma);
+          ok = __all_sync(0xffffffffu, mbar_wait(v_full, kc & 1, ctl, kWaitBwdMma));
           ++kc;
           for (int ii = 0; ok && ii < w.count; ++ii, ++qc) {
             // dP^T into the step's region once its S^T has been read out.
             const uint32_t r = qc & 1;
             const uint32_t sd = qc % C::kDoStages;
-            ok = mbar_wait(&do_full[sd], (qc / C::kDoStages) & 1, ctl, kWaitBwdMma);
-            if (ok) ok = mbar_wait(&s_free[r], (qc >> 1) & 1, ctl, kWaitBwdMma);
+            ok = __all_sync(0xffffffffu, mbar_wait(&do_full[sd], (qc / C::kDoStages) & 1, ctl, kWaitBwdMma));
+            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&s_free[r], (qc >> 1) & 1, ctl, kWaitBwdMma));
             if (!ok) break;
             tc_fence_after();
             const uint32_t sdo = smem_u32(smem + C::kOffDO + sd * C::kTileBytes);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
-              mma_ss(tmem + C::col_r(r), sdesc_sw128(sv + off, 16, 1024), sdesc_sw128(sdo + off, 16, 1024), id_s,
+              mma_ss_w(tmem + C::col_r(r), sdesc_sw128(sv + off, 16, 1024), sdesc_sw128(sdo + off, 16, 1024), id_s,
                      kk > 0 ? 1u : 0u);
             }
-            mma_commit(&dp_full[r]);
-            mma_commit(&do_empty[sd]);
+            mma_commit_w(&dp_full[r]);
+            mma_commit_w(&do_empty[sd]);
             // V_j is read by dP^T only.
-            if (ii + 1 == w.count) mma_commit(v_empty);
+            if (ii + 1 == w.count) mma_commit_w(v_empty);
           }
         }
       } else {
@@ -386,17 +387,17 @@ __global__ void __launch_bounds__(384, 1)
         auto issue_s = [&](uint32_t pos, bool last) -> bool {
           const uint32_t sq = pos % C::kQStages;
           const uint32_t r = pos & 1;
-          if (!mbar_wait(&q_full[sq], (pos / C::kQStages) & 1, ctl, kWaitBwdMma)) return false;
+          if (!__all_sync(0xffffffffu, mbar_wait(&q_full[sq], (pos / C::kQStages) & 1, ctl, kWaitBwdMma))) return false;
           tc_fence_after();
           const uint32_t sq_addr = smem_u32(smem + C::kOffQ + sq * C::kTileBytes);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
-            mma_ss(tmem + C::col_r(r), sdesc_sw128(sk + off, 16, 1024), sdesc_sw128(sq_addr + off, 16, 1024), id_s,
+            mma_ss_w(tmem + C::col_r(r), sdesc_sw128(sk + off, 16, 1024), sdesc_sw128(sq_addr + off, 16, 1024), id_s,
                    kk > 0 ? 1u : 0u);
           }
-          mma_commit(&s_full[r]);
-          if (last) mma_commit(k_empty);
+          mma_commit_w(&s_full[r]);
+          if (last) mma_commit_w(k_empty);
           return true;
         };
         uint32_t uc = 0;
@@ -404,7 +405,7 @@ __global__ void __launch_bounds__(384, 1)
           const int u = snake_unit(rnd);
           if (u >= p.num_units) continue;
           const BwdUnit w = decode_dkdv(p, u);
-          ok = mbar_wait(k_full, kc & 1, ctl, kWaitBwdMma);
+          ok = __all_sync(0xffffffffu, mbar_wait(k_full, kc & 1, ctl, kWaitBwdMma));
           ++kc;
           if (ok) ok = issue_s(qc, w.count == 1);
           if (ok && w.count > 1) ok = issue_s(qc + 1, w.count == 2);
@@ -412,11 +413,11 @@ __global__ void __launch_bounds__(384, 1)
             const uint32_t r = qc & 1;
             const uint32_t sq = qc % C::kQStages;
             const uint32_t sd = qc % C::kDoStages;
-            ok = mbar_wait(&p_ready[r], (qc >> 1) & 1, ctl, kWaitBwdMma);
+            ok = __all_sync(0xffffffffu, mbar_wait(&p_ready[r], (qc >> 1) & 1, ctl, kWaitBwdMma));
             if (!ok) break;
             if (ii == 0 && uc > 0) {
               // dV / dK of the previous unit have been read out.
-              ok = mbar_wait(dkv_empty, (uc - 1) & 1, ctl, kWaitBwdMma);
+              ok = __all_sync(0xffffffffu, mbar_wait(dkv_empty, (uc - 1) & 1, ctl, kWaitBwdMma));
               if (!ok) break;
             }
             tc_fence_after();
@@ -425,25 +426,25 @@ __global__ void __launch_bounds__(384, 1)
             // dV += P^T dO_i (A = P^T from TMEM, B = dO_i read MN-major).
 #pragma unroll
             for (int kk = 0; kk < kTileM / 16; ++kk)
-              mma_ts(tmem + C::kColDV, tmem + C::col_r(r) + packed_col(kk, false),
+              mma_ts_w(tmem + C::kColDV, tmem + C::col_r(r) + packed_col(kk, false),
                      sdesc_sw128(sdo + kk * 2048, C::kChunkBytes, 1024), id_kv, (ii > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(&do_empty[sd]);
+            mma_commit_w(&do_empty[sd]);
             // dK += dS^T Q_i.
 #pragma unroll
             for (int kk = 0; kk < kTileM / 16; ++kk)
-              mma_ts(tmem + C::kColDK, tmem + C::col_r(r) + packed_col(kk, true),
+              mma_ts_w(tmem + C::kColDK, tmem + C::col_r(r) + packed_col(kk, true),
                      sdesc_sw128(sq_addr + kk * 2048, C::kChunkBytes, 1024), id_kv, (ii > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(&q_empty[sq]);
+            mma_commit_w(&q_empty[sq]);
             // S^T two steps ahead, into the region dV and dK have just read.
             if (ii + 2 < w.count) ok = issue_s(qc + 2, ii + 3 == w.count);
           }
           if (!ok) break;
-          mma_commit(dkv_full);
+          mma_commit_w(dkv_full);
           ++uc;
         }
       }
-      mma_commit(drain);
-      mbar_wait(drain, 0, ctl, kWaitDrain);
+      mma_commit_w(drain);
+      (void)__all_sync(0xffffffffu, mbar_wait(drain, 0, ctl, kWaitDrain));
     }
     __syncwarp();
   } else if (warp < 8) {
@@ -738,13 +739,14 @@ __global__ void __launch_bounds__(384, 1)
     __syncwarp();
   } else if (warp == 8 || warp == 10) {
     // --------------------------------------------------------- MMA issuers
-    // Two threads issue the products, each in its own order, so that one
-    // thread's waits overlap the other's issue: warp 8 issues dP, warp 10
+    // Two warps issue the products, each in its own order, so that one
+    // warp's waits overlap the other's issue: warp 8 issues dP, warp 10
     // issues dQ and S (S into a buffer after the dQ that read it, in this
-    // thread's order).  No product of one reads or writes TMEM columns the
-    // other's products touch; each thread's commits track its own products.
+    // warp's order).  No product of one reads or writes TMEM columns the
+    // other's products touch; each warp's commits track its own products
+    // (the elected lane is the same for every instruction of a warp).
     reg_dealloc<R::kRegsCtl>();
-    if (lane == 0) {
+    {
       constexpr uint32_t id_s = idesc_bf16(kTileM, kTileN, false, false);  // S, dP
       constexpr uint32_t id_dq = idesc_bf16(kTileM, D, false, true);       // dQ += dS K
       const uint32_t sq = smem_u32(smem + C::kOffQ);
@@ -758,24 +760,24 @@ __global__ void __launch_bounds__(384, 1)
           const int u = snake_unit(rnd);
           if (u >= p.num_units) continue;
           const BwdUnit w = decode_dq(p, u);
-          ok = mbar_wait(do_full, uc & 1, ctl, kWaitBwdMma);
+          ok = __all_sync(0xffffffffu, mbar_wait(do_full, uc & 1, ctl, kWaitBwdMma));
           ++uc;
           for (int jj = 0; ok && jj < w.count; ++jj, ++kc) {
             const uint32_t sv = kc % C::kVStages;
-            ok = mbar_wait(&v_full[sv], (kc / C::kVStages) & 1, ctl, kWaitBwdMma);
-            if (ok && dn > 0) ok = mbar_wait(dp_free, (dn - 1) & 1, ctl, kWaitBwdMma);
+            ok = __all_sync(0xffffffffu, mbar_wait(&v_full[sv], (kc / C::kVStages) & 1, ctl, kWaitBwdMma));
+            if (ok && dn > 0) ok = __all_sync(0xffffffffu, mbar_wait(dp_free, (dn - 1) & 1, ctl, kWaitBwdMma));
             if (!ok) break;
             tc_fence_after();
             const uint32_t sv_addr = smem_u32(smem + C::kOffV + sv * C::kTileBytes);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
-              mma_ss(tmem + C::kColDP, sdesc_sw128(sdo + off, 16, 1024), sdesc_sw128(sv_addr + off, 16, 1024),
+              mma_ss_w(tmem + C::kColDP, sdesc_sw128(sdo + off, 16, 1024), sdesc_sw128(sv_addr + off, 16, 1024),
                      id_s, kk > 0 ? 1u : 0u);
             }
-            mma_commit(dp_full);
-            mma_commit(&v_empty[sv]);
-            if (jj + 1 == w.count) mma_commit(do_empty);
+            mma_commit_w(dp_full);
+            mma_commit_w(&v_empty[sv]);
+            if (jj + 1 == w.count) mma_commit_w(do_empty);
             ++dn;
           }
         }
@@ -784,38 +786,38 @@ __global__ void __launch_bounds__(384, 1)
         uint32_t uc = 0, kc = 0;
         // S of the step at position `pos` into S buffer (pos & 1).  The
         // buffer last held the dS of step pos - 2, read by a dQ product
-        // this thread issued earlier; its S was read before that dS was
+        // this warp issued earlier; its S was read before that dS was
         // written.  `last`: the unit's last S, after which Q_i is released.
         auto issue_s = [&](uint32_t pos, bool last) -> bool {
           const uint32_t sk = pos % C::kKStages;
-          if (!mbar_wait(&k_full[sk], (pos / C::kKStages) & 1, ctl, kWaitBwdMma)) return false;
+          if (!__all_sync(0xffffffffu, mbar_wait(&k_full[sk], (pos / C::kKStages) & 1, ctl, kWaitBwdMma))) return false;
           tc_fence_after();
           const uint32_t sk_addr = smem_u32(smem + C::kOffK + sk * C::kTileBytes);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
-            mma_ss(tmem + ((pos & 1) ? C::kColS1 : C::kColS0), sdesc_sw128(sq + off, 16, 1024),
+            mma_ss_w(tmem + ((pos & 1) ? C::kColS1 : C::kColS0), sdesc_sw128(sq + off, 16, 1024),
                    sdesc_sw128(sk_addr + off, 16, 1024), id_s, kk > 0 ? 1u : 0u);
           }
-          mma_commit(&s_full[pos & 1]);
-          if (last) mma_commit(q_empty);
+          mma_commit_w(&s_full[pos & 1]);
+          if (last) mma_commit_w(q_empty);
           return true;
         };
         for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units; ++rnd) {
           const int u = snake_unit(rnd);
           if (u >= p.num_units) continue;
           const BwdUnit w = decode_dq(p, u);
-          ok = mbar_wait(q_full, uc & 1, ctl, kWaitBwdMma);
+          ok = __all_sync(0xffffffffu, mbar_wait(q_full, uc & 1, ctl, kWaitBwdMma));
           if (!ok) break;
           tc_fence_after();
           ok = issue_s(kc, w.count == 1);
           if (ok && w.count > 1) ok = issue_s(kc + 1, w.count == 2);
           for (int jj = 0; ok && jj < w.count; ++jj, ++kc) {
-            ok = mbar_wait(&p_ready[kc & 1], (kc >> 1) & 1, ctl, kWaitBwdMma);
+            ok = __all_sync(0xffffffffu, mbar_wait(&p_ready[kc & 1], (kc >> 1) & 1, ctl, kWaitBwdMma));
             if (!ok) break;
             if (jj == 0 && uc > 0) {
               // The previous unit's dQ has been read out of TMEM.
-              ok = mbar_wait(dq_empty, (uc - 1) & 1, ctl, kWaitBwdMma);
+              ok = __all_sync(0xffffffffu, mbar_wait(dq_empty, (uc - 1) & 1, ctl, kWaitBwdMma));
               if (!ok) break;
             }
             tc_fence_after();
@@ -826,9 +828,9 @@ __global__ void __launch_bounds__(384, 1)
             const uint32_t ds_col = (kc & 1) ? C::kColS1 : C::kColS0;
 #pragma unroll
             for (int kk = 0; kk < kTileN / 16; ++kk)
-              mma_ts(tmem + C::kColDQ, tmem + ds_col + packed_col(kk, false),
+              mma_ts_w(tmem + C::kColDQ, tmem + ds_col + packed_col(kk, false),
                      sdesc_sw128(sk_addr + kk * 2048, C::kChunkBytes, 1024), id_dq, (jj > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(&k_empty[sk]);
+            mma_commit_w(&k_empty[sk]);
             // S two steps ahead, into the buffer this dQ product reads from.
             if (jj + 2 < w.count) {
               ok = issue_s(kc + 2, jj + 3 == w.count);
@@ -836,12 +838,12 @@ __global__ void __launch_bounds__(384, 1)
             }
           }
           if (!ok) break;
-          mma_commit(dq_full);
+          mma_commit_w(dq_full);
           ++uc;
         }
       }
-      mma_commit(drain);
-      mbar_wait(drain, 0, ctl, kWaitDrain);
+      mma_commit_w(drain);
+      (void)__all_sync(0xffffffffu, mbar_wait(drain, 0, ctl, kWaitDrain));
     }
     __syncwarp();
   } else if (warp < 8) {
