@@ -24,13 +24,14 @@
 // The softmax scale is applied once to dK and dQ when they are written.
 //
 // Roles (384 threads, three warpgroups, registers split with setmaxnreg as
-// in the forward kernel): warp 9 loads (TMA), warps 8 and 10 issue tcgen05
-// MMAs (two issuing warps, split so that neither's products touch the TMEM
-// columns of the other's, so that one's barrier waits overlap the other's
-// issue; each walks its schedule as a whole warp and an elected lane issues
-// every MMA and commit), warp 11 idle, warps 0-7 do the element-wise work (a
-// TMEM lane per thread; warps w and w+4 split the 128 columns of a tile) and
-// write the results.
+// in the forward kernel): warp 9 loads (TMA); tcgen05 MMAs are issued by
+// warp 8 alone in the dK/dV kernel (one ordered stream of products) and by
+// warps 8 and 10 in the dQ kernel (split so that neither's products touch
+// the TMEM columns of the other's); an issuing warp walks its schedule as a
+// whole warp and an elected lane issues every MMA and commit.  The other
+// control warps idle; warps 0-7 do the element-wise work (a TMEM lane per
+// thread; warps w and w+4 split the 128 columns of a tile) and write the
+// results.
 //
 // Pipelining.  The element-wise warps read a tile of S into registers and
 // compute P from it while the tensor core runs other products; they read dP
@@ -220,7 +221,7 @@ __global__ void __launch_bounds__(384, 1)
     }
     for (int s = 0; s < C::kDoStages; ++s) {
       mbar_init(&do_full[s], 1);
-      mbar_init(&do_empty[s], 2);  // dP^T and dV
+      mbar_init(&do_empty[s], 1);  // dV (issued after the step's dP^T)
     }
     for (int r = 0; r < 2; ++r) {
       mbar_init(&s_full[r], 1);
@@ -230,7 +231,7 @@ __global__ void __launch_bounds__(384, 1)
     }
     mbar_init(dkv_full, 1);
     mbar_init(dkv_empty, 8);
-    mbar_init(drain, 2);  // both MMA issuers
+    mbar_init(drain, 1);
     fence_barrier_init();
   }
   if (warp == 8) {
@@ -337,115 +338,163 @@ __global__ void __launch_bounds__(384, 1)
         mbar_wait(&do_full[pos % C::kDoStages], (pos / C::kDoStages) & 1, ctl, kWaitDrain);
     }
     __syncwarp();
-  } else if (warp == 8 || warp == 10) {
-    // --------------------------------------------------------- MMA issuers
-    // Two steps are in flight: step pos uses TMEM region pos & 1 for its
-    // S^T, then (once S^T has been read) its dP^T, then its packed P^T and
-    // dS^T, which dK and dV read.  Warp 8 issues dP^T.  Warp 10 issues dV
-    // and dK of a step and then S^T of the step two ahead into the same
-    // region, so the tensor pipe's issue order keeps S^T behind the products
-    // that read the region.
+  } else if (warp == 8) {
+    // ---------------------------------------------------------- MMA issuer
+    // One warp issues every product (the warp walks the schedule, an
+    // elected lane issues) as one stream of steps over all of this CTA's
+    // units.  Step g uses TMEM region g & 1: S^T, then (once S^T has been
+    // read) dP^T, then P^T and dS^T packed, which dV and dK read.  Within
+    // step g the order is
+    //   dP^T(g), dK(g-1), S^T(g+1), [P^T(g), dS^T(g) ready] dV(g)
+    // so dP^T, which the element-wise warps wait for next, enters the tensor
+    // pipe behind a single product (dV of the step before) rather than
+    // behind dV, dK and S^T.  S^T(g+1) goes into the region dK(g-1) has just
+    // read (the pipe runs one thread's products in issue order).  At the
+    // first step of a unit, V_j is new and may still be loading: dK(g-1) and
+    // S^T(g+1) go first.
     reg_dealloc<R::kRegsCtl>();
-    {
-      constexpr uint32_t id_s = idesc_bf16(kTileM, kTileM, false, false);  // S^T, dP^T
-      constexpr uint32_t id_kv = idesc_bf16(kTileM, D, false, true);       // dV, dK
-      const uint32_t sk = smem_u32(smem + C::kOffK);
-      const uint32_t sv = smem_u32(smem + C::kOffV);
-      uint32_t kc = 0, qc = 0;
-      bool ok = true;
-      if (warp == 8) {
-        for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units; ++rnd) {
-          const int u = snake_unit(rnd);
-          if (u >= p.num_units) continue;
-          const BwdUnit w = decode_dkdv(p, u);
-          ok = __all_sync(0xffffffffu, mbar_wait(v_full, kc & 1, ctl, kWaitBwdMma));
-          ++kc;
-          for (int ii = 0; ok && ii < w.count; ++ii, ++qc) {
-            // dP^T into the step's region once its S^T has been read out.
-            const uint32_t r = qc & 1;
-            const uint32_t sd = qc % C::kDoStages;
-            ok = __all_sync(0xffffffffu, mbar_wait(&do_full[sd], (qc / C::kDoStages) & 1, ctl, kWaitBwdMma));
-            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&s_free[r], (qc >> 1) & 1, ctl, kWaitBwdMma));
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t sdo = smem_u32(smem + C::kOffDO + sd * C::kTileBytes);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
-              mma_ss_w(tmem + C::col_r(r), sdesc_sw128(sv + off, 16, 1024), sdesc_sw128(sdo + off, 16, 1024), id_s,
-                     kk > 0 ? 1u : 0u);
-            }
-            mma_commit_w(&dp_full[r]);
-            mma_commit_w(&do_empty[sd]);
-            // V_j is read by dP^T only.
-            if (ii + 1 == w.count) mma_commit_w(v_empty);
-          }
-        }
-      } else {
-        // S^T of the step at position `pos` into region pos & 1; `last`: the
-        // unit's last S^T, after which K_j is released.
-        auto issue_s = [&](uint32_t pos, bool last) -> bool {
-          const uint32_t sq = pos % C::kQStages;
-          const uint32_t r = pos & 1;
-          if (!__all_sync(0xffffffffu, mbar_wait(&q_full[sq], (pos / C::kQStages) & 1, ctl, kWaitBwdMma))) return false;
-          tc_fence_after();
-          const uint32_t sq_addr = smem_u32(smem + C::kOffQ + sq * C::kTileBytes);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
-            mma_ss_w(tmem + C::col_r(r), sdesc_sw128(sk + off, 16, 1024), sdesc_sw128(sq_addr + off, 16, 1024), id_s,
-                   kk > 0 ? 1u : 0u);
-          }
-          mma_commit_w(&s_full[r]);
-          if (last) mma_commit_w(k_empty);
-          return true;
-        };
-        uint32_t uc = 0;
-        for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units; ++rnd) {
-          const int u = snake_unit(rnd);
-          if (u >= p.num_units) continue;
-          const BwdUnit w = decode_dkdv(p, u);
-          ok = __all_sync(0xffffffffu, mbar_wait(k_full, kc & 1, ctl, kWaitBwdMma));
-          ++kc;
-          if (ok) ok = issue_s(qc, w.count == 1);
-          if (ok && w.count > 1) ok = issue_s(qc + 1, w.count == 2);
-          for (int ii = 0; ok && ii < w.count; ++ii, ++qc) {
-            const uint32_t r = qc & 1;
-            const uint32_t sq = qc % C::kQStages;
-            const uint32_t sd = qc % C::kDoStages;
-            ok = __all_sync(0xffffffffu, mbar_wait(&p_ready[r], (qc >> 1) & 1, ctl, kWaitBwdMma));
-            if (!ok) break;
-            if (ii == 0 && uc > 0) {
-              // dV / dK of the previous unit have been read out.
-              ok = __all_sync(0xffffffffu, mbar_wait(dkv_empty, (uc - 1) & 1, ctl, kWaitBwdMma));
-              if (!ok) break;
-            }
-            tc_fence_after();
-            const uint32_t sq_addr = smem_u32(smem + C::kOffQ + sq * C::kTileBytes);
-            const uint32_t sdo = smem_u32(smem + C::kOffDO + sd * C::kTileBytes);
-            // dV += P^T dO_i (A = P^T from TMEM, B = dO_i read MN-major).
-#pragma unroll
-            for (int kk = 0; kk < kTileM / 16; ++kk)
-              mma_ts_w(tmem + C::kColDV, tmem + C::col_r(r) + packed_col(kk, false),
-                     sdesc_sw128(sdo + kk * 2048, C::kChunkBytes, 1024), id_kv, (ii > 0 || kk > 0) ? 1u : 0u);
-            mma_commit_w(&do_empty[sd]);
-            // dK += dS^T Q_i.
-#pragma unroll
-            for (int kk = 0; kk < kTileM / 16; ++kk)
-              mma_ts_w(tmem + C::kColDK, tmem + C::col_r(r) + packed_col(kk, true),
-                     sdesc_sw128(sq_addr + kk * 2048, C::kChunkBytes, 1024), id_kv, (ii > 0 || kk > 0) ? 1u : 0u);
-            mma_commit_w(&q_empty[sq]);
-            // S^T two steps ahead, into the region dV and dK have just read.
-            if (ii + 2 < w.count) ok = issue_s(qc + 2, ii + 3 == w.count);
-          }
-          if (!ok) break;
-          mma_commit_w(dkv_full);
-          ++uc;
+    constexpr uint32_t id_s = idesc_bf16(kTileM, kTileM, false, false);  // S^T, dP^T
+    constexpr uint32_t id_kv = idesc_bf16(kTileM, D, false, true);       // dV, dK
+    const uint32_t sk = smem_u32(smem + C::kOffK);
+    const uint32_t sv = smem_u32(smem + C::kOffV);
+    auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctl, kWaitBwdMma));
+    };
+    // Position in this CTA's stream of steps: unit `rnd` of the snake order
+    // (the `un`-th unit this CTA runs), step `ii` of it.
+    struct Cur {
+      int rnd, ii, un;
+      BwdUnit w;
+      bool valid;
+    };
+    auto seek = [&](Cur& c, int rnd, int un) {
+      c.valid = false;
+      for (; rnd * (int)gridDim.x < p.num_units; ++rnd) {
+        const int u = snake_unit(rnd);
+        if (u < p.num_units) {
+          c.rnd = rnd;
+          c.ii = 0;
+          c.un = un;
+          c.w = decode_dkdv(p, u);
+          c.valid = true;
+          return;
         }
       }
-      mma_commit_w(drain);
-      (void)__all_sync(0xffffffffu, mbar_wait(drain, 0, ctl, kWaitDrain));
+    };
+    auto advance = [&](Cur& c) {
+      if (++c.ii >= c.w.count) seek(c, c.rnd + 1, c.un + 1);
+    };
+    auto q_addr = [&](uint32_t g) { return smem_u32(smem + C::kOffQ + (g % C::kQStages) * C::kTileBytes); };
+    auto do_addr = [&](uint32_t g) { return smem_u32(smem + C::kOffDO + (g % C::kDoStages) * C::kTileBytes); };
+    auto issue_s = [&](uint32_t g) {  // S^T(g) = K_j Q_i^T
+      const uint32_t qa = q_addr(g);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
+        mma_ss_w(tmem + C::col_r(g & 1), sdesc_sw128(sk + off, 16, 1024), sdesc_sw128(qa + off, 16, 1024), id_s,
+                 kk > 0 ? 1u : 0u);
+      }
+      mma_commit_w(&s_full[g & 1]);
+    };
+    auto issue_dp = [&](uint32_t g) {  // dP^T(g) = V_j dO_i^T
+      const uint32_t da = do_addr(g);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
+        mma_ss_w(tmem + C::col_r(g & 1), sdesc_sw128(sv + off, 16, 1024), sdesc_sw128(da + off, 16, 1024), id_s,
+                 kk > 0 ? 1u : 0u);
+      }
+      mma_commit_w(&dp_full[g & 1]);
+    };
+    auto issue_dv = [&](uint32_t g, bool acc) {  // dV += P^T dO_i (B read MN-major)
+      const uint32_t da = do_addr(g);
+#pragma unroll
+      for (int kk = 0; kk < kTileM / 16; ++kk)
+        mma_ts_w(tmem + C::kColDV, tmem + C::col_r(g & 1) + packed_col(kk, false),
+                 sdesc_sw128(da + kk * 2048, C::kChunkBytes, 1024), id_kv, (acc || kk > 0) ? 1u : 0u);
+      mma_commit_w(&do_empty[g % C::kDoStages]);  // dO_i: read by dP^T and dV
+    };
+    auto issue_dk = [&](uint32_t g, bool acc) {  // dK += dS^T Q_i
+      const uint32_t qa = q_addr(g);
+#pragma unroll
+      for (int kk = 0; kk < kTileM / 16; ++kk)
+        mma_ts_w(tmem + C::kColDK, tmem + C::col_r(g & 1) + packed_col(kk, true),
+                 sdesc_sw128(qa + kk * 2048, C::kChunkBytes, 1024), id_kv, (acc || kk > 0) ? 1u : 0u);
+      mma_commit_w(&q_empty[g % C::kQStages]);  // Q_i: read by S^T and dK
+    };
+    bool ok = true;
+    Cur cur, nxt;
+    seek(cur, 0, 0);
+    if (cur.valid) {
+      ok = wait(k_full, 0) && wait(&q_full[0], 0);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        if (cur.w.count == 1) mma_commit_w(k_empty);  // K_j: read by S^T only
+      }
     }
+    nxt = cur;
+    if (nxt.valid) advance(nxt);
+    uint32_t g = 0;
+    // dK of step g - 1, issued during step g: pending, accumulate, and
+    // whether it closes its unit.
+    bool pend = false, pend_acc = false, pend_last = false;
+    for (; ok && cur.valid; ++g) {
+      const bool first = cur.ii == 0;
+      auto dp_step = [&]() -> bool {
+        if (first && !wait(v_full, cur.un & 1)) return false;
+        if (!wait(&do_full[g % C::kDoStages], (g / C::kDoStages) & 1)) return false;
+        if (!wait(&s_free[g & 1], (g >> 1) & 1)) return false;
+        tc_fence_after();
+        issue_dp(g);
+        if (cur.ii + 1 == cur.w.count) mma_commit_w(v_empty);  // V_j: read by dP^T only
+        return true;
+      };
+      auto dk_prev = [&]() {
+        if (!pend) return;
+        issue_dk(g - 1, pend_acc);
+        if (pend_last) mma_commit_w(dkv_full);
+      };
+      auto s_next = [&]() -> bool {
+        if (!nxt.valid) return true;
+        if (nxt.ii == 0 && !wait(k_full, nxt.un & 1)) return false;
+        if (!wait(&q_full[(g + 1) % C::kQStages], ((g + 1) / C::kQStages) & 1)) return false;
+        tc_fence_after();
+        issue_s(g + 1);
+        if (nxt.ii + 1 == nxt.w.count) mma_commit_w(k_empty);
+        return true;
+      };
+      if (first) {
+        dk_prev();
+        ok = s_next() && dp_step();
+      } else {
+        ok = dp_step();
+        if (ok) {
+          dk_prev();
+          ok = s_next();
+        }
+      }
+      if (!ok) break;
+      // dV(g) once P^T(g) and dS^T(g) are in the region; the first step of a
+      // unit also needs the previous unit's dV and dK read out of TMEM.
+      ok = wait(&p_ready[g & 1], (g >> 1) & 1);
+      if (ok && first && cur.un > 0) ok = wait(dkv_empty, (cur.un - 1) & 1);
+      if (!ok) break;
+      tc_fence_after();
+      issue_dv(g, !first);
+      pend = true;
+      pend_acc = !first;
+      pend_last = cur.ii + 1 == cur.w.count;
+      cur = nxt;
+      if (nxt.valid) advance(nxt);
+    }
+    if (ok && pend) {
+      issue_dk(g - 1, pend_acc);
+      if (pend_last) mma_commit_w(dkv_full);
+    }
+    // Every MMA this warp issued completes before TMEM is released.
+    mma_commit_w(drain);
+    (void)wait(drain, 0);
     __syncwarp();
   } else if (warp < 8) {
     // ------------------------------------------ P^T, dS^T and dK/dV output
