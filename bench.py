@@ -275,7 +275,7 @@ def run_ours(args, world, rank, local):
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
-    fa.fa_timing_enable(True)
+    count0 = [fa.fa_launch_count(kid) for kid in range(len(KERNEL_NAMES))]
     for i in range(args.steps):
         flush.zero_()  # L2 flush between steps, outside the step's events
         starts[i].record(stream)
@@ -284,6 +284,21 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop() if rank == 0 else None
+    count1 = [fa.fa_launch_count(kid) for kid in range(len(KERNEL_NAMES))]
+    st = fa.fa_poll_status()
+    if st != 0:
+        raise RuntimeError(f"device status after timed steps: {fa.fa_strerror(st)}")
+    # Per-launch device times come from a second timed region of the same
+    # steps with events around every launch: events between kernels stop a
+    # launch from overlapping the previous kernel's drain and lengthen a step
+    # by a few percent, so the step time above is taken without them.
+    barrier(world)
+    torch.cuda.synchronize()
+    fa.fa_timing_enable(True)
+    for i in range(args.steps):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
     per_kernel = {}
     for kid, name in enumerate(KERNEL_NAMES):
         n, ms = fa.fa_timing_read(kid)
@@ -291,10 +306,10 @@ def run_ours(args, world, rank, local):
     fa.fa_timing_enable(False)
     st = fa.fa_poll_status()
     if st != 0:
-        raise RuntimeError(f"device status after timed steps: {fa.fa_strerror(st)}")
+        raise RuntimeError(f"device status after the per-launch timing steps: {fa.fa_strerror(st)}")
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     total_ms = sum(step_ms)
-    launches = sum(v["launches"] for v in per_kernel.values())
+    launches = sum(c1 - c0 for c0, c1 in zip(count0, count1))
     kern_ms = [per_kernel[n]["total_ms"] for n in KERNEL_NAMES]
     (total_ms_max, *kern_max), (launches_sum,) = reduce_max_sum(world, [total_ms] + kern_ms, [launches], device)
 
@@ -349,6 +364,8 @@ def run_ours(args, world, rank, local):
         "roofline": roofline,
         "kernels": {n: {"launches": v["launches"], "ms_per_launch": round(v["total_ms"] / v["launches"], 4)}
                     for n, v in per_kernel.items() if v["launches"]},
+        "kernel_timing": ("per-launch CUDA events in a second timed region of the same steps; the step time "
+                          "comes from a region without them"),
         "gpu_launches": int(launches_sum),
         "e2e": e2e,
         "clocks": clk,

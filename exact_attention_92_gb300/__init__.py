@@ -28,6 +28,7 @@ from ._binding import (  # noqa: F401
     fa_selftest_wait_timeout,
     fa_set_wait_timeout_ns,
     fa_strerror,
+    fa_launch_count,
     fa_timing_enable,
     fa_timing_read,
     forward,

@@ -56,6 +56,7 @@ _SIGNATURES = {
     "fa_abi_version": ([], _i),
     "fa_timing_enable": ([_i], _i),
     "fa_timing_read": ([_i, ctypes.POINTER(_i), ctypes.POINTER(ctypes.c_double)], _i),
+    "fa_launch_count": ([_i, ctypes.POINTER(ctypes.c_uint64)], _i),
 }
 
 
@@ -215,6 +216,13 @@ def fa_timing_read(kernel: int):
     ms = ctypes.c_double(0.0)
     _check(load().fa_timing_read(int(kernel), ctypes.byref(n), ctypes.byref(ms)), "fa_timing_read")
     return n.value, ms.value
+
+
+def fa_launch_count(kernel: int) -> int:
+    """Launches of one library kernel since the library was loaded."""
+    n = ctypes.c_uint64(0)
+    _check(load().fa_launch_count(int(kernel), ctypes.byref(n)), "fa_launch_count")
+    return n.value
 
 
 # ------------------------------------------------------- convenience calls

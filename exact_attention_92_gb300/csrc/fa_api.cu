@@ -150,6 +150,8 @@ struct TimingRec {
 };
 std::mutex g_tmu;
 bool g_timing = false;
+// Launches of each library kernel since the library was loaded (always on).
+std::atomic<unsigned long long> g_launches[FA_KERNEL_BWD_DQ + 1];
 std::vector<TimingRec> g_recs;
 std::vector<cudaEvent_t> g_pool;
 
@@ -178,6 +180,7 @@ cudaError_t timed(int kernel, cudaStream_t stream, F&& launch) {
   }
   if (r.a && r.b) cudaEventRecord(r.a, stream);
   cudaError_t e = launch();
+  if (e == cudaSuccess) g_launches[kernel].fetch_add(1, std::memory_order_relaxed);
   if (r.a && r.b) {
     cudaEventRecord(r.b, stream);
     std::lock_guard<std::mutex> g(g_tmu);
@@ -203,6 +206,7 @@ int internal_encode_bhnd(CUtensorMap* m, const void* ptr, int BH, int N, int d) 
   return encode_bhnd(m, ptr, BH, N, d);
 }
 unsigned long long internal_wait_timeout_ns() { return g_timeout_ns.load(); }
+void internal_count_launch(int kernel) { g_launches[kernel].fetch_add(1, std::memory_order_relaxed); }
 }  // namespace fa
 
 extern "C" {
@@ -216,6 +220,12 @@ int fa_timing_enable(int on) {
   }
   g_recs.clear();
   g_timing = on != 0;
+  return FA_OK;
+}
+
+int fa_launch_count(int kernel, uint64_t* count) {
+  if (!count || kernel < 0 || kernel > FA_KERNEL_BWD_DQ) return FA_ERR_INVALID_ARG;
+  *count = g_launches[kernel].load(std::memory_order_relaxed);
   return FA_OK;
 }
 

@@ -21,6 +21,7 @@ int internal_device_setup(unsigned int** status, int* sm_count);
 int internal_validate(int B, int H, int N, int d, float scale);
 int internal_encode_bhnd(CUtensorMap* m, const void* ptr, int BH, int N, int d);
 unsigned long long internal_wait_timeout_ns();
+void internal_count_launch(int kernel);
 cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const BwdParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_bwd_dq(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
@@ -116,7 +117,14 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
 
   const int grid = p.num_units < sm_count ? p.num_units : sm_count;
   cudaError_t ce = fa::launch_bwd_preprocess(d, o, dout, dvec, (int)rows, st);
-  if (ce == cudaSuccess) ce = fa::launch_bwd_dkdv(d, tq, tk, tv, tdo, p, grid, st);
-  if (ce == cudaSuccess) ce = fa::launch_bwd_dq(d, tq, tk, tv, tdo, p, grid, st);
+  if (ce == cudaSuccess) {
+    fa::internal_count_launch(FA_KERNEL_BWD_PRE);
+    ce = fa::launch_bwd_dkdv(d, tq, tk, tv, tdo, p, grid, st);
+  }
+  if (ce == cudaSuccess) {
+    fa::internal_count_launch(FA_KERNEL_BWD);
+    ce = fa::launch_bwd_dq(d, tq, tk, tv, tdo, p, grid, st);
+  }
+  if (ce == cudaSuccess) fa::internal_count_launch(FA_KERNEL_BWD_DQ);
   return ce == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }

@@ -174,6 +174,14 @@ int fa_selftest_wait_timeout(uint64_t timeout_ns, void* stream);
 int fa_timing_enable(int on);
 int fa_timing_read(int kernel, int* launches, double* total_ms);
 
+/*
+ * Launch counter (always on, no events): `*count` receives how many times
+ * the kernel with id `kernel` (FA_KERNEL_*) has been launched by this
+ * library since it was loaded.  Returns FA_OK or FA_ERR_INVALID_ARG (bad id
+ * or null `count`).
+ */
+int fa_launch_count(int kernel, uint64_t* count);
+
 /* Human-readable name of an fa_status code (static storage). */
 const char* fa_strerror(int status);
 

@@ -90,6 +90,17 @@ def test_timing_read_argument_errors(lib):
     assert lib.fa_timing_read(0, None, ctypes.byref(ms)) == fa.FA_ERR_INVALID_ARG
 
 
+def test_launch_count_arguments(lib):
+    """The launch counter is host-side: it answers without a GPU and rejects
+    bad ids and null pointers."""
+    n = ctypes.c_uint64(123)
+    assert lib.fa_launch_count(0, ctypes.byref(n)) == fa.FA_OK
+    assert n.value >= 0
+    assert lib.fa_launch_count(5, ctypes.byref(n)) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_launch_count(-1, ctypes.byref(n)) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_launch_count(0, None) == fa.FA_ERR_INVALID_ARG
+
+
 def test_python_binding_rejects_cpu_tensors(lib):
     torch = pytest.importorskip("torch")
     q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)

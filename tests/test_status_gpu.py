@@ -65,3 +65,19 @@ def test_timing_counts_launches(fa):
     assert counts[fa.FA_KERNEL_COMBINE][0] == 0
     assert counts[fa.FA_KERNEL_BWD][0] == 1 and counts[fa.FA_KERNEL_BWD_PRE][0] == 1
     assert counts[fa.FA_KERNEL_BWD_DQ][0] == 1
+
+
+def test_launch_counter_without_events(fa):
+    """fa_launch_count advances by exactly the kernels a call launches, with
+    per-launch timing off."""
+    torch = torch_cuda()
+    case = inputs.make_case(1, 2, 1024, 128, True, seed=4, with_do=True)
+    q, k, v, do = case_tensors(case)
+    before = [fa.fa_launch_count(kid) for kid in range(5)]
+    o, lse = fa.forward(q, k, v, causal=True, num_splits=1)
+    fa.backward(q, k, v, o, lse, do, causal=True)
+    torch.cuda.synchronize()
+    after = [fa.fa_launch_count(kid) for kid in range(5)]
+    delta = [a - b for a, b in zip(after, before)]
+    assert delta[fa.FA_KERNEL_FWD] == 1 and delta[fa.FA_KERNEL_COMBINE] == 0
+    assert delta[fa.FA_KERNEL_BWD_PRE] == 1 and delta[fa.FA_KERNEL_BWD] == 1 and delta[fa.FA_KERNEL_BWD_DQ] == 1
