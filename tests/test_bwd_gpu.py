@@ -95,3 +95,35 @@ def test_outputs_only_16_byte_aligned(fa, d):
     assert fa.fa_poll_status() == fa.FA_OK
     for got, want in zip(outs, ref):
         assert torch.equal(got, want)
+
+
+def test_many_heads_many_units_per_cta(fa):
+    """272 heads at N=1024, d=64 causal: every persistent CTA walks many
+    units of both backward kernels and of the forward kernel, across the last
+    partial round.  O, L and the gradients of heads spread over the unit order
+    match the oracle."""
+    from parity import check_lse, check_o
+
+    case = inputs.make_case(17, 16, 1024, 64, True, seed=601, with_do=True)
+    q, k, v, do = case_tensors(case)
+    o, lse = fa.forward(q, k, v, causal=True)
+    dq, dk, dv = fa.backward(q, k, v, o, lse, do, causal=True)
+    st = fa.fa_poll_status()
+    assert st == 0, fa.fa_strerror(st)
+    o, lse = host(o), lse.cpu().numpy().astype(np.float64)
+    dq, dk, dv = host(dq), host(dk), host(dv)
+    Q, K, V, DO = case.f64("q"), case.f64("k"), case.f64("v"), case.f64("do")
+    for b, h in [(0, 0), (7, 9), (15, 15), (16, 0), (16, 7), (16, 15)]:
+        what = f"head {(b, h)}"
+        O, L = att.forward_head(Q[b, h], K[b, h], V[b, h], case.scale, True)
+
+        def row_weights(ix, b=b, h=h):
+            P = att.probabilities_head(Q[b, h], K[b, h], case.scale, True, rows=[ix[-1]])[0]
+            return P, V[b, h]
+
+        check_o(o[b, h][None, None], O[None, None], what, row_weights)
+        check_lse(lse[b, h], L, what)
+        rq, rk, rv = att.backward_head(Q[b, h], K[b, h], V[b, h], DO[b, h], case.scale, True)
+        check_grad(dq[b, h], rq, "dQ", what)
+        check_grad(dk[b, h], rk, "dK", what)
+        check_grad(dv[b, h], rv, "dV", what)
