@@ -1015,21 +1015,36 @@ __global__ void __launch_bounds__(384, 1)
 }
 
 // D_i = sum_c dO_ic * O_ic.  D/8 lanes per row, 16 bytes of O and of dO
-// per lane, so a warp reads 256 / D whole rows with 16-byte accesses.
+// per lane; a block reads 256 / (D/8) consecutive rows per pass (whole rows,
+// 16-byte accesses) and kRowsPerThread passes, whose loads are all issued
+// before any is used so that enough bytes are in flight to stream from DRAM.
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_preprocess(const __nv_bfloat16* __restrict__ o,
                                                          const __nv_bfloat16* __restrict__ dout,
                                                          float* __restrict__ dvec, int rows) {
-  constexpr int kLanes = D / 8;                 // lanes per row
-  constexpr int kRowsPerBlock = 256 / kLanes;
-  const int row = blockIdx.x * kRowsPerBlock + threadIdx.x / kLanes;
+  constexpr int kLanes = D / 8;               // lanes per row
+  constexpr int kSlots = 256 / kLanes;        // rows per pass
+  constexpr int kRowsPerThread = 4;           // passes
   const int part = threadIdx.x % kLanes;
-  float acc = 0.f;
-  if (row < rows) {
-    const uint4 a = reinterpret_cast<const uint4*>(o + (size_t)row * D)[part];
-    const uint4 b = reinterpret_cast<const uint4*>(dout + (size_t)row * D)[part];
-    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+  const int slot = threadIdx.x / kLanes;
+  const int base = blockIdx.x * kSlots * kRowsPerThread;
+  uint4 a[kRowsPerThread], b[kRowsPerThread];
+#pragma unroll
+  for (int r = 0; r < kRowsPerThread; ++r) {
+    const int row = base + r * kSlots + slot;
+    if (row < rows) {
+      a[r] = reinterpret_cast<const uint4*>(o + (size_t)row * D)[part];
+      b[r] = reinterpret_cast<const uint4*>(dout + (size_t)row * D)[part];
+    } else {
+      a[r] = make_uint4(0u, 0u, 0u, 0u);
+      b[r] = a[r];
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < kRowsPerThread; ++r) {
+    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a[r]);
+    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b[r]);
+    float acc = 0.f;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const float2 x = __bfloat1622float2(a2[i]);
@@ -1037,10 +1052,11 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess(const __nv_bfloat16* __
       acc = fmaf(x.x, y.x, acc);
       acc = fmaf(x.y, y.y, acc);
     }
-  }
 #pragma unroll
-  for (int off = kLanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (row < rows && part == 0) dvec[row] = acc;
+    for (int off = kLanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    const int row = base + r * kSlots + slot;
+    if (row < rows && part == 0) dvec[row] = acc;
+  }
 }
 
 // A wait on an mbarrier that nothing arrives on: exercises the give-up path.
@@ -1093,7 +1109,7 @@ cudaError_t launch_bwd_dq(int d, const CUtensorMap& tq, const CUtensorMap& tk, c
 
 cudaError_t launch_bwd_preprocess(int d, const void* o, const void* dout, float* dvec, int rows,
                                   cudaStream_t stream) {
-  const int per_block = 256 / (d / 8);  // rows per 256-thread block
+  const int per_block = (256 / (d / 8)) * 4;  // rows per 256-thread block (4 passes)
   const int grid = (rows + per_block - 1) / per_block;
   const auto* po = static_cast<const __nv_bfloat16*>(o);
   const auto* pd = static_cast<const __nv_bfloat16*>(dout);
