@@ -340,6 +340,7 @@ def run_ours(args, world, rank, local):
     e2e = e2e_run(args, fa, case, device, stream, B, H, N, d, causal, f + b, world)
 
     extra = fwd_targets(fa, device, peaks, args) if (rank == 0 and not args.no_extra) else None
+    extra_bwd = bwd_targets(fa, device, peaks, args) if (rank == 0 and not args.no_extra) else None
 
     if rank != 0:
         return None
@@ -372,6 +373,8 @@ def run_ours(args, world, rank, local):
     }
     if extra is not None:
         line["fwd_targets"] = extra
+    if extra_bwd is not None:
+        line["bwd_targets"] = extra_bwd
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tf, dt, desc = oracle_sample()
         line["cpu_baseline"] = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
@@ -452,6 +455,51 @@ def e2e_run(args, fa, case, device, stream, B, H, N, d, causal, flops, world):
             "h2d_bytes_per_step": 4 * elem, "d2h_bytes_per_step": 3 * elem,
             "ms_per_step": round(ms_max / n, 4),
             "copies": "pinned host buffers; copy-in, compute and copy-out on three streams, double-buffered"}
+
+
+def bwd_targets(fa, device, peaks, args):
+    """Backward-only throughput (fa_bwd: D preprocess, dQ and dK/dV kernels)
+    on the 16K-token sweep at d=128, N >= 4K; 2.5x the forward FLOPs."""
+    import torch
+
+    from exact_attention_92_gb300 import inputs
+
+    out = []
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    for N in (4096, 8192, 16384):
+        for causal in (False, True):
+            B, H, d = 16384 // N, 16, 128
+            g = torch.Generator(device=device)
+            g.manual_seed(5000)
+            shape = (B, H, N, d)
+            q, k, v, do = (torch.randn(shape, generator=g, device=device).to(torch.bfloat16) for _ in range(4))
+            o = torch.empty_like(q)
+            lse = torch.empty(shape[:3], dtype=torch.float32, device=device)
+            dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+            fa.fa_fwd(q, k, v, o, lse, causal)
+            for _ in range(3):
+                fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, causal)
+            torch.cuda.synchronize()
+            reps, tot = 10, 0.0
+            for _ in range(reps):
+                flush.zero_()
+                s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                s.record(stream)
+                fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, causal)
+                e.record(stream)
+                torch.cuda.synchronize()
+                tot += s.elapsed_time(e)
+            st = fa.fa_poll_status()
+            if st != 0:
+                raise RuntimeError(f"device status after the backward cases: {fa.fa_strerror(st)}")
+            fl = 2.5 * inputs.fwd_flops(B, H, N, d, causal)
+            tf = fl * reps / (tot / 1e3) / 1e12
+            out.append({"case": f"B={B} H={H} N={N} d={d} {'causal' if causal else 'non-causal'}",
+                        "tflops": round(tf, 1), "frac": round(tf / peaks["bf16_tflops"], 4),
+                        "ms": round(tot / reps, 4)})
+            del q, k, v, do, o, lse, dq, dk, dv
+    return out
 
 
 def fwd_targets(fa, device, peaks, args):
@@ -596,7 +644,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--no-extra", action="store_true", help="skip the forward-only target cases")
+    ap.add_argument("--no-extra", action="store_true", help="skip the forward-only and backward-only target cases")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip timing the CPU oracle")
     ap.add_argument("--profile", choices=["fwd", "bwd"], help="3 launches of one kernel, for ncu")
     args = ap.parse_args(argv)
