@@ -341,6 +341,7 @@ def run_ours(args, world, rank, local):
 
     extra = fwd_targets(fa, device, peaks, args) if (rank == 0 and not args.no_extra) else None
     extra_bwd = bwd_targets(fa, device, peaks, args) if (rank == 0 and not args.no_extra) else None
+    extra_gqa = gqa_targets(fa, device, peaks, args) if (rank == 0 and not args.no_extra) else None
 
     if rank != 0:
         return None
@@ -375,6 +376,8 @@ def run_ours(args, world, rank, local):
         line["fwd_targets"] = extra
     if extra_bwd is not None:
         line["bwd_targets"] = extra_bwd
+    if extra_gqa is not None:
+        line["gqa_targets"] = extra_gqa
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tf, dt, desc = oracle_sample()
         line["cpu_baseline"] = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
@@ -481,15 +484,17 @@ def bwd_targets(fa, device, peaks, args):
             for _ in range(3):
                 fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, causal)
             torch.cuda.synchronize()
-            reps, tot = 10, 0.0
-            for _ in range(reps):
+            # All repetitions are queued before one synchronise, so the host's
+            # enqueue time never shows inside the events.
+            reps = 10
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+            for s, e in ev:
                 flush.zero_()
-                s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 s.record(stream)
                 fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, causal)
                 e.record(stream)
-                torch.cuda.synchronize()
-                tot += s.elapsed_time(e)
+            torch.cuda.synchronize()
+            tot = sum(s.elapsed_time(e) for s, e in ev)
             st = fa.fa_poll_status()
             if st != 0:
                 raise RuntimeError(f"device status after the backward cases: {fa.fa_strerror(st)}")
@@ -500,6 +505,51 @@ def bwd_targets(fa, device, peaks, args):
                         "ms": round(tot / reps, 4)})
             del q, k, v, do, o, lse, dq, dk, dv
     return out
+
+
+def gqa_targets(fa, device, peaks, args):
+    """Grouped-query attention (fa_fwd_gqa, fa_bwd_gqa): 32 query heads over 8
+    key/value heads, B=2, N=4096, d=128, causal; FLOPs counted per query head
+    as for multi-head attention."""
+    import torch
+
+    from exact_attention_92_gb300 import inputs
+
+    B, H, Hkv, N, d, causal = 2, 32, 8, 4096, 128, True
+    g = torch.Generator(device=device)
+    g.manual_seed(6000)
+    q, do = (torch.randn((B, H, N, d), generator=g, device=device).to(torch.bfloat16) for _ in range(2))
+    k, v = (torch.randn((B, Hkv, N, d), generator=g, device=device).to(torch.bfloat16) for _ in range(2))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def timed(fn, reps=10):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for s, e in ev:  # queued before one synchronise (host time stays out)
+            flush.zero_()
+            s.record(stream)
+            fn()
+            e.record(stream)
+        torch.cuda.synchronize()
+        return sum(s.elapsed_time(e) for s, e in ev) / reps
+
+    ms_f = timed(lambda: fa.fa_fwd_gqa(q, k, v, o, lse, causal))
+    ms_b = timed(lambda: fa.fa_bwd_gqa(q, k, v, o, lse, do, dq, dk, dv, causal))
+    st = fa.fa_poll_status()
+    if st != 0:
+        raise RuntimeError(f"device status after the GQA cases: {fa.fa_strerror(st)}")
+    f = inputs.fwd_flops(B, H, N, d, causal)
+    name = f"B={B} H={H} Hkv={Hkv} N={N} d={d} causal"
+    return [{"case": name + " forward", "tflops": round(f / ms_f / 1e9, 1),
+             "frac": round(f / ms_f / 1e9 / peaks["bf16_tflops"], 4), "ms": round(ms_f, 4)},
+            {"case": name + " backward", "tflops": round(2.5 * f / ms_b / 1e9, 1),
+             "frac": round(2.5 * f / ms_b / 1e9 / peaks["bf16_tflops"], 4), "ms": round(ms_b, 4)}]
 
 
 def fwd_targets(fa, device, peaks, args):
@@ -534,15 +584,14 @@ def fwd_targets(fa, device, peaks, args):
         torch.cuda.synchronize()
         reps = 10
         fa.fa_timing_enable(True)
-        tot = 0.0
-        for _ in range(reps):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for s, e in ev:  # queued before one synchronise (host time stays out)
             flush.zero_()
-            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             s.record(stream)
             fa.fa_fwd(q, k, v, o, lse, c["causal"])
             e.record(stream)
-            torch.cuda.synchronize()
-            tot += s.elapsed_time(e)
+        torch.cuda.synchronize()
+        tot = sum(s.elapsed_time(e) for s, e in ev)
         nk, kms = fa.fa_timing_read(0)
         for kid in range(1, 5):
             fa.fa_timing_read(kid)

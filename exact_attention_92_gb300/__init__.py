@@ -21,9 +21,11 @@ from ._binding import (  # noqa: F401
     declared_symbols,
     fa_abi_version,
     fa_bwd,
+    fa_bwd_gqa,
     fa_bwd_noalloc,
     fa_fwd,
     fa_fwd_ex,
+    fa_fwd_gqa,
     fa_poll_status,
     fa_selftest_wait_timeout,
     fa_set_wait_timeout_ns,

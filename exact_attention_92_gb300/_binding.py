@@ -47,7 +47,9 @@ _u64 = ctypes.c_uint64
 _SIGNATURES = {
     "fa_fwd": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp], _i),
     "fa_fwd_ex": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp], _i),
+    "fa_fwd_gqa": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp], _i),
     "fa_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp], _i),
+    "fa_bwd_gqa": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp], _i),
     "fa_bwd_noalloc": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp], _i),
     "fa_poll_status": ([_vp], _i),
     "fa_set_wait_timeout_ns": ([_u64], _u64),
@@ -150,6 +152,42 @@ def fa_fwd_ex(q, k, v, o, lse, causal=False, scale=None, num_splits=0, stream=No
     st = lib.fa_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, 1 if causal else 0,
                        _scale(scale, d), int(num_splits), _stream_ptr(stream, q.device))
     _check(st, "fa_fwd_ex")
+
+
+def fa_fwd_gqa(q, k, v, o, lse, causal=False, scale=None, num_splits=0, stream=None):
+    """C fa_fwd_gqa: grouped-query attention; q, o [B, H, N, d], k, v
+    [B, Hkv, N, d] with Hkv dividing H (query head h reads key/value head
+    h // (H // Hkv))."""
+    _check_bhnd("q", q)
+    B, H, N, d = q.shape
+    _check_bhnd("k", k)
+    Hkv = k.shape[1]
+    _check_bhnd("k", k, (B, Hkv, N, d))
+    _check_bhnd("v", v, (B, Hkv, N, d))
+    _check_bhnd("o", o, q.shape)
+    _check_lse(lse, (B, H, N))
+    lib = load()
+    st = lib.fa_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, N, d, 1 if causal else 0,
+                        _scale(scale, d), int(num_splits), _stream_ptr(stream, q.device))
+    _check(st, "fa_fwd_gqa")
+
+
+def fa_bwd_gqa(q, k, v, o, lse, dout, dq, dk, dv, causal=False, scale=None, stream=None):
+    """C fa_bwd_gqa: gradients for grouped-query attention; dk, dv have the
+    shape of k, v ([B, Hkv, N, d]) and hold the sums over each group."""
+    _check_bhnd("q", q)
+    B, H, N, d = q.shape
+    _check_bhnd("k", k)
+    Hkv = k.shape[1]
+    for name, t in (("k", k), ("v", v), ("dk", dk), ("dv", dv)):
+        _check_bhnd(name, t, (B, Hkv, N, d))
+    for name, t in (("o", o), ("dout", dout), ("dq", dq)):
+        _check_bhnd(name, t, q.shape)
+    _check_lse(lse, (B, H, N))
+    lib = load()
+    st = lib.fa_bwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                        B, H, Hkv, N, d, 1 if causal else 0, _scale(scale, d), _stream_ptr(stream, q.device))
+    _check(st, "fa_bwd_gqa")
 
 
 def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, causal=False, scale=None, stream=None):

@@ -293,12 +293,13 @@ int fa_selftest_wait_timeout(uint64_t timeout_ns, void* stream) {
              : FA_ERR_CUDA;
 }
 
-int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
-              int causal, float scale, int num_splits, void* stream) {
+int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv, int N,
+               int d, int causal, float scale, int num_splits, void* stream) {
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return FA_ERR_INVALID_ARG;
   int e = validate(B, H, N, d, scale);
   if (e) return e;
+  if (Hkv < 1 || H % Hkv != 0) return FA_ERR_INVALID_ARG;
   if (num_splits < 0) return FA_ERR_INVALID_ARG;
   DeviceState* s = nullptr;
   e = device_state(&s);
@@ -313,13 +314,14 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
   S = (nkv + per_split - 1) / per_split;  // no empty split
 
   CUtensorMap tq, tk, tv;
-  if (encode_bhnd(&tq, q, BH, N, d) || encode_bhnd(&tk, k, BH, N, d) || encode_bhnd(&tv, v, BH, N, d))
+  if (encode_bhnd(&tq, q, BH, N, d) || encode_bhnd(&tk, k, B * Hkv, N, d) || encode_bhnd(&tv, v, B * Hkv, N, d))
     return FA_ERR_CUDA;
 
   FwdParams p;
   std::memset(&p, 0, sizeof(p));
   p.B = B;
   p.H = H;
+  p.Hkv = Hkv;
   p.N = N;
   p.causal = causal ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
@@ -360,18 +362,25 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
   return ce == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
-           int causal, float scale, void* stream) {
-  return fa_fwd_ex(q, k, v, o, lse, B, H, N, d, causal, scale, 0, stream);
+int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+              int causal, float scale, int num_splits, void* stream) {
+  return fa_fwd_gqa(q, k, v, o, lse, B, H, H, N, d, causal, scale, num_splits, stream);
 }
 
-int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
-           void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale, void* stream) {
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+           int causal, float scale, void* stream) {
+  return fa_fwd_gqa(q, k, v, o, lse, B, H, H, N, d, causal, scale, 0, stream);
+}
+
+int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+               void* dq, void* dk, void* dv, int B, int H, int Hkv, int N, int d, int causal, float scale,
+               void* stream) {
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dout) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return FA_ERR_INVALID_ARG;
   int e = validate(B, H, N, d, scale);
   if (e) return e;
+  if (Hkv < 1 || H % Hkv != 0) return FA_ERR_INVALID_ARG;
   DeviceState* s = nullptr;
   e = device_state(&s);
   if (e) return e;
@@ -380,7 +389,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
   const size_t rows = (size_t)BH * N;
 
   CUtensorMap tq, tk, tv, tdo;
-  if (encode_bhnd(&tq, q, BH, N, d) || encode_bhnd(&tk, k, BH, N, d) || encode_bhnd(&tv, v, BH, N, d) ||
+  if (encode_bhnd(&tq, q, BH, N, d) || encode_bhnd(&tk, k, B * Hkv, N, d) || encode_bhnd(&tv, v, B * Hkv, N, d) ||
       encode_bhnd(&tdo, dout, BH, N, d))
     return FA_ERR_CUDA;
 
@@ -397,6 +406,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
   std::memset(&p, 0, sizeof(p));
   p.B = B;
   p.H = H;
+  p.Hkv = Hkv;
   p.N = N;
   p.causal = causal ? 1 : 0;
   p.scale = scale;
@@ -410,18 +420,26 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
                 reinterpret_cast<uintptr_t>(dv)) & 31u) == 0 ? 1 : 0;
   p.num_tiles = (N + 127) / 128;
   p.num_units = BH * p.num_tiles;
+  p.num_units_kv = B * Hkv * p.num_tiles;
+  p.group = H / Hkv;
   p.status = s->status;
   p.timeout_ns = g_timeout_ns.load();
 
-  const int grid = p.num_units < s->sm_count ? p.num_units : s->sm_count;
+  const int grid_q = p.num_units < s->sm_count ? p.num_units : s->sm_count;
+  const int grid_kv = p.num_units_kv < s->sm_count ? p.num_units_kv : s->sm_count;
   cudaError_t ce =
       timed(FA_KERNEL_BWD_PRE, st, [&] { return fa::launch_bwd_preprocess(d, o, dout, dvec, (int)rows, st); });
   if (ce == cudaSuccess)
-    ce = timed(FA_KERNEL_BWD, st, [&] { return fa::launch_bwd_dkdv(d, tq, tk, tv, tdo, p, grid, st); });
+    ce = timed(FA_KERNEL_BWD, st, [&] { return fa::launch_bwd_dkdv(d, tq, tk, tv, tdo, p, grid_kv, st); });
   if (ce == cudaSuccess)
-    ce = timed(FA_KERNEL_BWD_DQ, st, [&] { return fa::launch_bwd_dq(d, tq, tk, tv, tdo, p, grid, st); });
+    ce = timed(FA_KERNEL_BWD_DQ, st, [&] { return fa::launch_bwd_dq(d, tq, tk, tv, tdo, p, grid_q, st); });
   cudaFreeAsync(ws, st);
   return ce == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+           void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale, void* stream) {
+  return fa_bwd_gqa(q, k, v, o, lse, dout, dq, dk, dv, B, H, H, N, d, causal, scale, stream);
 }
 
 }  // extern "C"

@@ -93,21 +93,27 @@ __device__ __forceinline__ uint32_t packed_col(int kk, bool second) {
 }
 
 struct BwdUnit {
-  int bh;
+  int bh;     // the head: key/value head (dK/dV kernel), query head (dQ kernel)
   int t;      // the tile this CTA owns (key tile / query tile)
   int first;  // first tile of the other operand
-  int count;  // number of tiles of the other operand
+  int count;  // steps: tiles of the other operand, times the query heads that
+              // share the key/value head in the dK/dV kernel
+  int per;    // steps per query head (dK/dV kernel; = count in the dQ kernel)
 };
 
 // dK/dV units: with the causal mask, low key tiles see the most query tiles,
 // so they come first.
+// A dK/dV unit is one key/value tile of one key/value head; its steps walk
+// the visible query tiles of every query head that reads that key/value head
+// (one head, for plain multi-head attention), so dK and dV sum over them.
 __device__ __forceinline__ BwdUnit decode_dkdv(const BwdParams& p, int u) {
   BwdUnit w;
-  const int BH = p.B * p.H;
+  const int BH = p.B * p.Hkv;
   w.bh = u % BH;
   w.t = u / BH;
   w.first = p.causal ? w.t : 0;
-  w.count = p.num_tiles - w.first;
+  w.per = p.num_tiles - w.first;
+  w.count = w.per * p.group;
   return w;
 }
 
@@ -119,6 +125,7 @@ __device__ __forceinline__ BwdUnit decode_dq(const BwdParams& p, int u) {
   w.t = p.causal ? p.num_tiles - 1 - u / BH : u / BH;
   w.first = 0;
   w.count = p.causal ? w.t + 1 : p.num_tiles;
+  w.per = w.count;
   return w;
 }
 
@@ -171,7 +178,10 @@ __device__ __forceinline__ void p64_rowL(uint32_t* s, float L, float sl2, int q,
   }
 }
 
-template <int D>
+// GQA: key/value heads shared by several query heads (the steps of a unit
+// then run over (query head, query tile) pairs); the multi-head instance
+// keeps the plain per-tile indexing.
+template <int D, bool GQA>
 __global__ void __launch_bounds__(384, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -255,11 +265,10 @@ __global__ void __launch_bounds__(384, 1)
     reg_dealloc<R::kRegsCtl>();
     uint32_t kc = 0, qc = 0;
     bool ok = true;
-    for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units; ++rnd) {
+    for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units_kv; ++rnd) {
       const int u = snake_unit(rnd);
-      if (u >= p.num_units) continue;
+      if (u >= p.num_units_kv) continue;
       const BwdUnit w = decode_dkdv(p, u);
-      const size_t head = (size_t)w.bh * p.N;
       ok = __all_sync(0xffffffffu, mbar_wait(k_empty, (kc & 1) ^ 1, ctl, kWaitBwdLoad));
       if (!ok) break;
       if (lane == 0) {
@@ -267,8 +276,21 @@ __global__ void __launch_bounds__(384, 1)
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_3d(smem + C::kOffK + c * C::kChunkBytes, &tm_k, k_full, c * 64, w.t * kTileN, w.bh);
       }
+      // Step ii: query tile first + ii % per of the (ii / per)-th query head
+      // that reads this key/value head (with GQA, kept as running counters).
+      int qh = GQA ? q_head_of(w.bh, 0, p.H, p.Hkv) : w.bh;
+      int qt = w.first;
       for (int ii = 0; ok && ii < w.count; ++ii, ++qc) {
-        const int row = (w.first + ii) * kTileM;
+        if constexpr (GQA) {
+          if (ii > 0 && ++qt == w.first + w.per) {
+            qt = w.first;
+            ++qh;
+          }
+        } else {
+          qt = w.first + ii;
+        }
+        const int row = qt * kTileM;
+        const size_t head = (size_t)qh * p.N;
         // Q_i with L_i (log2 units; rows past N get +inf so their weights
         // vanish).  The values are written before the arrive that completes
         // the stage together with the copy.
@@ -290,7 +312,7 @@ __global__ void __launch_bounds__(384, 1)
           mbar_arrive_expect_tx(&q_full[sq], C::kTileBytes);
           for (int c = 0; c < C::kChunks; ++c)
             tma_load_3d(smem + C::kOffQ + sq * C::kTileBytes + c * C::kChunkBytes, &tm_q, &q_full[sq], c * 64,
-                        row, w.bh);
+                        row, qh);
         }
         // dO_i with D_i.
         const uint32_t sd = qc % C::kDoStages;
@@ -311,7 +333,7 @@ __global__ void __launch_bounds__(384, 1)
           mbar_arrive_expect_tx(&do_full[sd], C::kTileBytes);
           for (int c = 0; c < C::kChunks; ++c)
             tma_load_3d(smem + C::kOffDO + sd * C::kTileBytes + c * C::kChunkBytes, &tm_do, &do_full[sd],
-                        c * 64, row, w.bh);
+                        c * 64, row, qh);
         }
         if (ii == 0) {
           // V_j, needed by the first dP^T, after the first step's Q and dO.
@@ -369,9 +391,9 @@ __global__ void __launch_bounds__(384, 1)
     };
     auto seek = [&](Cur& c, int rnd, int un) {
       c.valid = false;
-      for (; rnd * (int)gridDim.x < p.num_units; ++rnd) {
+      for (; rnd * (int)gridDim.x < p.num_units_kv; ++rnd) {
         const int u = snake_unit(rnd);
-        if (u < p.num_units) {
+        if (u < p.num_units_kv) {
           c.rnd = rnd;
           c.ii = 0;
           c.un = un;
@@ -542,14 +564,20 @@ __global__ void __launch_bounds__(384, 1)
     };
     int pend_kr = -1;  // the unit whose dK / dV are still in TMEM
     size_t pend_head = 0;
-    for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units; ++rnd) {
+    for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units_kv; ++rnd) {
       const int u = snake_unit(rnd);
-      if (u >= p.num_units) continue;
+      if (u >= p.num_units_kv) continue;
       const BwdUnit w = decode_dkdv(p, u);
       const int kr = w.t * kTileN + r_key;  // key index
       const size_t head = (size_t)w.bh * p.N;
+      int qt = w.first;
       for (int ii = 0; ok && ii < w.count; ++ii, ++qc) {
-        const int q0 = (w.first + ii) * kTileM;
+        if constexpr (GQA) {
+          if (ii > 0 && ++qt == w.first + w.per) qt = w.first;  // query tile of step ii
+        } else {
+          qt = w.first + ii;
+        }
+        const int q0 = qt * kTileM;
         const uint32_t reg = qc & 1;
         const uint32_t tZ = tmem + lane_off + C::col_r(reg) + 64 * hc;
         const uint32_t sq = qc % C::kQStages;
@@ -743,6 +771,7 @@ __global__ void __launch_bounds__(384, 1)
         const int u = snake_unit(rnd);
         if (u >= p.num_units) continue;
         const BwdUnit w = decode_dq(p, u);
+        const int kvbh = p.Hkv == p.H ? w.bh : kv_head_of(w.bh, p.H, p.Hkv);  // K, V head
         ok = mbar_wait(q_empty, (uc & 1) ^ 1, ctl, kWaitBwdLoad);
         if (!ok) break;
         mbar_arrive_expect_tx(q_full, C::kTileBytes);
@@ -756,7 +785,7 @@ __global__ void __launch_bounds__(384, 1)
           mbar_arrive_expect_tx(&k_full[sk], C::kTileBytes);
           for (int c = 0; c < C::kChunks; ++c)
             tma_load_3d(smem + C::kOffK + sk * C::kTileBytes + c * C::kChunkBytes, &tm_k, &k_full[sk], c * 64, key0,
-                        w.bh);
+                        kvbh);
           if (jj == 0) {
             // dO_i, needed by the first dP, after the first K.
             ok = mbar_wait(do_empty, (uc & 1) ^ 1, ctl, kWaitBwdLoad);
@@ -771,7 +800,7 @@ __global__ void __launch_bounds__(384, 1)
           mbar_arrive_expect_tx(&v_full[sv], C::kTileBytes);
           for (int c = 0; c < C::kChunks; ++c)
             tma_load_3d(smem + C::kOffV + sv * C::kTileBytes + c * C::kChunkBytes, &tm_v, &v_full[sv], c * 64, key0,
-                        w.bh);
+                        kvbh);
         }
         ++uc;
       }
@@ -1073,14 +1102,14 @@ __global__ void fa_selftest_wait_kernel(unsigned int* status, unsigned long long
 
 // ------------------------------------------------------------------ launch
 
-template <int D>
+template <int D, bool GQA>
 static cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                  const CUtensorMap& tdo, const BwdParams& p, int grid, cudaStream_t stream) {
   using C = DkdvCfg<D>;
-  cudaError_t e =
-      cudaFuncSetAttribute(fa_bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(fa_bwd_dkdv_kernel<D, GQA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  fa_bwd_dkdv_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, p);
+  fa_bwd_dkdv_kernel<D, GQA><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, p);
   return cudaGetLastError();
 }
 
@@ -1097,8 +1126,11 @@ static cudaError_t launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, con
 
 cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const BwdParams& p, int grid, cudaStream_t stream) {
-  return d == 64 ? launch_dkdv_t<64>(tq, tk, tv, tdo, p, grid, stream)
-                 : launch_dkdv_t<128>(tq, tk, tv, tdo, p, grid, stream);
+  if (p.Hkv != p.H)
+    return d == 64 ? launch_dkdv_t<64, true>(tq, tk, tv, tdo, p, grid, stream)
+                   : launch_dkdv_t<128, true>(tq, tk, tv, tdo, p, grid, stream);
+  return d == 64 ? launch_dkdv_t<64, false>(tq, tk, tv, tdo, p, grid, stream)
+                 : launch_dkdv_t<128, false>(tq, tk, tv, tdo, p, grid, stream);
 }
 
 cudaError_t launch_bwd_dq(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -198,6 +198,7 @@ __global__ void __launch_bounds__(384, 1)
         const int u = snake_unit(rnd);
         if (u >= p.num_units) continue;
         const Unit w = decode_unit(p, u);
+        const int kvbh = p.Hkv == p.H ? w.bh : kv_head_of(w.bh, p.H, p.Hkv);  // K, V head
         for (int t = 0; ok && t < 2; ++t) {
           if (w.n[t] == 0) continue;
           ok = mbar_wait(&q_empty[t], (qc[t] & 1) ^ 1, ctl, kWaitQEmpty);
@@ -218,7 +219,7 @@ __global__ void __launch_bounds__(384, 1)
             const CUtensorMap* m = which ? &tm_v : &tm_k;
             for (int c = 0; c < C::kChunks; ++c)
               tma_load_3d(sKV + slot * C::kTileBytes + c * C::kChunkBytes, m, &kv_full[slot], c * 64,
-                          (w.kvb + j) * kTileN, w.bh);
+                          (w.kvb + j) * kTileN, kvbh);
             ++rc;
           }
         }

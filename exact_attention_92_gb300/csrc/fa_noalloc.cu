@@ -99,6 +99,7 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
   std::memset(&p, 0, sizeof(p));
   p.B = B;
   p.H = H;
+  p.Hkv = H;
   p.N = N;
   p.causal = causal ? 1 : 0;
   p.scale = scale;
@@ -112,6 +113,8 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
                 reinterpret_cast<uintptr_t>(dv)) & 31u) == 0 ? 1 : 0;
   p.num_tiles = (N + 127) / 128;
   p.num_units = BH * p.num_tiles;
+  p.num_units_kv = p.num_units;
+  p.group = 1;
   p.status = status;
   p.timeout_ns = fa::internal_wait_timeout_ns();
 

@@ -40,7 +40,7 @@
 extern "C" {
 #endif
 
-#define FA_ABI_VERSION 2
+#define FA_ABI_VERSION 3
 
 typedef enum {
   FA_OK = 0,
@@ -78,6 +78,19 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
               int causal, float scale, int num_splits, void* stream);
 
 /*
+ * Forward pass with grouped-query attention (GQA; MQA when Hkv = 1): the H
+ * query heads of a batch share Hkv key/value heads, query head h reading
+ * key/value head h / (H / Hkv).  The pages list this variant as not
+ * evaluated; it is the same computation per query head with K and V taken
+ * from that head's key/value head.
+ *   q, o    : bf16 [B,H,N,d];  k, v : bf16 [B,Hkv,N,d];  lse : fp32 [B,H,N]
+ *   Hkv     : >= 1 and divides H (FA_ERR_INVALID_ARG otherwise)
+ * Other arguments as fa_fwd_ex; Hkv = H is fa_fwd_ex.
+ */
+int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv, int N,
+               int d, int causal, float scale, int num_splits, void* stream);
+
+/*
  * Backward pass.  "FlashAttention V2 in depth", section 7: P recomputed from
  * the saved logsumexp (section 7.1), D_i = rowsum(dO_i * O_i) from a separate
  * preprocess kernel (section 7.3), dK and dV with key/value tiles in the
@@ -95,6 +108,21 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
  */
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
            void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale, void* stream);
+
+/*
+ * Backward pass with grouped-query attention (see fa_fwd_gqa): dK and dV of
+ * a key/value head are the sums over the query heads that read it.  A dK/dV
+ * CTA owns one key/value tile of one key/value head and walks the visible
+ * query tiles of all of those query heads, so the sums stay in tensor memory
+ * (no atomics; results bitwise reproducible from run to run).
+ *   q, o, dout, dq : bf16 [B,H,N,d];  k, v, dk, dv : bf16 [B,Hkv,N,d]
+ *   lse            : fp32 [B,H,N]
+ *   Hkv            : >= 1 and divides H (FA_ERR_INVALID_ARG otherwise)
+ * Workspace and other arguments as fa_bwd; Hkv = H is fa_bwd.
+ */
+int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+               void* dq, void* dk, void* dv, int B, int H, int Hkv, int N, int d, int causal, float scale,
+               void* stream);
 
 /*
  * Backward pass that allocates no device memory.  The paper has no

@@ -214,3 +214,41 @@ def forward_head_keys(q, k, v, scale, causal, key_lo, key_hi):
         o[ok] = (e @ v) / l[:, None]
         L[ok] = _lse(m, l)
     return o, L
+
+
+# ------------------------------------------------- grouped-query attention
+# Grouped-query attention is listed on the pages as not evaluated; it is the
+# same computation per query head with K and V shared: the H query heads of
+# a batch read Hkv key/value heads, query head h reading key/value head
+# h // (H // Hkv).  The oracle writes that definition out by repeating each
+# key/value head over its group and reusing the functions above; dK and dV of
+# a shared head are the sums over the query heads that read it (the
+# derivative of a sum of per-query-head terms).
+
+def expand_kv(x, H):
+    """[B, Hkv, N, d] -> [B, H, N, d]: head h of the result is head
+    h // (H // Hkv) of x."""
+    Hkv = x.shape[1]
+    assert H % Hkv == 0
+    return np.repeat(x, H // Hkv, axis=1)
+
+
+def reduce_kv(g, Hkv):
+    """[B, H, N, d] gradient w.r.t. the expanded K or V -> [B, Hkv, N, d],
+    summed over each group of H // Hkv query heads."""
+    B, H, N, d = g.shape
+    assert H % Hkv == 0
+    return g.reshape(B, Hkv, H // Hkv, N, d).sum(axis=2)
+
+
+def forward_gqa(q, k, v, scale, causal):
+    """O [B,H,N,d] and L [B,H,N] with k, v of Hkv heads."""
+    H = q.shape[1]
+    return forward(q, expand_kv(k, H), expand_kv(v, H), scale, causal)
+
+
+def backward_gqa(q, k, v, do, scale, causal):
+    """dQ [B,H,N,d] and dK, dV [B,Hkv,N,d] with k, v of Hkv heads."""
+    H, Hkv = q.shape[1], k.shape[1]
+    dq, dk, dv = backward(q, expand_kv(k, H), expand_kv(v, H), do, scale, causal)
+    return dq, reduce_kv(dk, Hkv), reduce_kv(dv, Hkv)

@@ -236,6 +236,64 @@ def pin_merge(att):
         assert np.allclose(O, Of, atol=1e-14) and np.allclose(L, Lf, atol=1e-14)
 
 
+def pin_gqa_routing(att):
+    """Grouped-query attention, closed form: with V = 0 on key/value head 0
+    and V = 1 on head 1, every softmax row sums to one, so O is exactly 0 for
+    the query heads of the first group and exactly 1 for those of the second
+    (H = 6, Hkv = 2)."""
+    rng = np.random.default_rng(7)
+    B, H, Hkv, N, d = 1, 6, 2, 9, 4
+    q = rng.standard_normal((B, H, N, d))
+    k = rng.standard_normal((B, Hkv, N, d))
+    v = np.zeros((B, Hkv, N, d))
+    v[:, 1] = 1.0
+    for causal in (False, True):
+        o, _ = att.forward_gqa(q, k, v, 0.5, causal)
+        assert np.array_equal(o[:, :3], np.zeros((B, 3, N, d)))
+        assert np.allclose(o[:, 3:], 1.0, rtol=0, atol=1e-15)
+
+
+def pin_gqa_finite_differences(att):
+    """Grouped-query attention: dQ, dK, dV against central differences of the
+    forward loss sum(O * dO); a dropped group member or a wrong head in the
+    sum of a shared head's gradient moves it by a whole term."""
+    rng = np.random.default_rng(11)
+    B, H, Hkv, N, d = 1, 4, 2, 5, 3
+    q = rng.standard_normal((B, H, N, d))
+    k = rng.standard_normal((B, Hkv, N, d))
+    v = rng.standard_normal((B, Hkv, N, d))
+    do = rng.standard_normal((B, H, N, d))
+    scale = 0.7
+    for causal in (False, True):
+        dq, dk, dv = att.backward_gqa(q, k, v, do, scale, causal)
+        assert dk.shape == k.shape and dv.shape == v.shape and dq.shape == q.shape
+
+        def loss(q_, k_, v_):
+            return float(np.sum(att.forward_gqa(q_, k_, v_, scale, causal)[0] * do))
+
+        eps = 1e-6
+        for name, x, g in (("k", k, dk), ("v", v, dv), ("q", q, dq)):
+            for ix in [(0, 0, 1, 2), (0, 1, 4, 0), (0, x.shape[1] - 1, 2, 1)]:
+                xp, xm = x.copy(), x.copy()
+                xp[ix] += eps
+                xm[ix] -= eps
+                args_p = {"q": (xp, k, v), "k": (q, xp, v), "v": (q, k, xp)}[name]
+                args_m = {"q": (xm, k, v), "k": (q, xm, v), "v": (q, k, xm)}[name]
+                fd = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+                assert abs(fd - g[ix]) <= 1e-6 * max(1.0, abs(fd)), (name, causal, ix, fd, g[ix])
+
+
+def pin_gqa_one_group_per_head(att):
+    """Hkv = H: the grouped functions give the multi-head results."""
+    rng = np.random.default_rng(3)
+    q, k, v, do = (rng.standard_normal((2, 3, 7, 4)) for _ in range(4))
+    o1, l1 = att.forward_gqa(q, k, v, 0.5, True)
+    o2, l2 = att.forward(q, k, v, 0.5, True)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    for a, b in zip(att.backward_gqa(q, k, v, do, 0.5, True), att.backward(q, k, v, do, 0.5, True)):
+        assert np.array_equal(a, b)
+
+
 ALL_PINS = [
     pin_brute_force,
     pin_rows_sum_to_one,
@@ -248,4 +306,7 @@ ALL_PINS = [
     pin_backward_finite_differences,
     pin_d_identity,
     pin_merge,
+    pin_gqa_routing,
+    pin_gqa_finite_differences,
+    pin_gqa_one_group_per_head,
 ]

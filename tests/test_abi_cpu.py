@@ -37,7 +37,7 @@ def test_no_driver_dependency():
 
 
 def test_version_and_strerror(lib):
-    assert fa.fa_abi_version() == 2
+    assert fa.fa_abi_version() == 3
     for code in range(6):
         assert fa.fa_strerror(code).startswith("FA_")
     assert "unknown" in fa.fa_strerror(99)
@@ -64,6 +64,17 @@ def test_fwd_argument_errors(lib):
     assert _fwd(lib, splits=-1) == fa.FA_ERR_INVALID_ARG
     assert _fwd(lib, d=96) == fa.FA_ERR_UNSUPPORTED
     assert _fwd(lib, d=256) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_gqa_argument_errors(lib):
+    """Key/value head counts that do not divide the query heads are refused
+    before anything touches a device."""
+    ptrs = [P(0x1000 * (i + 1)) for i in range(9)]
+    for hkv in (0, -1, 3, 5):
+        assert lib.fa_fwd_gqa(*ptrs[:5], 2, 8, hkv, 256, 64, 1, 0.125, 0, None) == fa.FA_ERR_INVALID_ARG
+        assert lib.fa_bwd_gqa(*ptrs, 2, 8, hkv, 256, 64, 1, 0.125, None) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_fwd_gqa(P(0), *ptrs[1:5], 2, 8, 2, 256, 64, 1, 0.125, 0, None) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_bwd_gqa(*ptrs[:8], P(0x9008), 2, 8, 2, 256, 64, 1, 0.125, None) == fa.FA_ERR_INVALID_ARG
 
 
 def test_bwd_argument_errors(lib):

@@ -118,3 +118,4 @@ def test_inputs_seeded_and_degenerate():
 def test_flop_counts():
     assert inputs.fwd_flops(8, 32, 4096, 128, True) == 4 * 8 * 32 * 4096 ** 2 * 128 / 2
     assert inputs.bwd_flops(2, 16, 4096, 128, True) == 2.5 * inputs.fwd_flops(2, 16, 4096, 128, True)
+

@@ -34,6 +34,12 @@ MUTANTS = {
     # backward
     "d_dropped": ("_d_vector", lambda do, o: np.zeros(do.shape[0])),
     "d_wrong_axis": ("_d_vector", lambda do, o: np.sum(do * o, axis=1)[::-1].copy()),
+    # grouped-query attention
+    "gqa_heads_interleaved": ("expand_kv", lambda x, H: np.tile(x, (1, H // x.shape[1], 1, 1))),
+    "gqa_sum_interleaved": ("reduce_kv", lambda g, Hkv: g.reshape(g.shape[0], g.shape[1] // Hkv, Hkv,
+                                                                  *g.shape[2:]).sum(axis=1)),
+    "gqa_mean_not_sum": ("reduce_kv", lambda g, Hkv: g.reshape(g.shape[0], Hkv, g.shape[1] // Hkv,
+                                                               *g.shape[2:]).mean(axis=2)),
 }
 
 
