@@ -19,6 +19,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -65,13 +66,24 @@ KERNEL_SOURCES = {
 }
 
 
+# C/C++ comments and string/char literals (literals are kept as they are).
+_C_TOKENS = re.compile(r'//[^\n]*|/\*.*?\*/|"(?:\\.|[^"\\])*"|\'(?:\\.|[^\'\\])*\'', re.S)
+
+
+def _code_only(text):
+    """Source text without comments and blank lines: what the compiler sees."""
+    text = _C_TOKENS.sub(lambda m: "" if m.group(0).startswith("/") else m.group(0), text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_source_hash(kernel):
-    """Hash of the source files a kernel is compiled from."""
+    """Hash of the code (comments left out) of the source files a kernel is
+    compiled from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_attention_92_gb300", "csrc")
     for name in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(csrc, name), "rb") as fh:
-            h.update(name.encode() + fh.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as fh:
+            h.update(name.encode() + _code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

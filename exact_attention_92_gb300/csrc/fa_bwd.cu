@@ -371,7 +371,7 @@ __global__ void __launch_bounds__(384, 1)
     // so dP^T, which the element-wise warps wait for next, enters the tensor
     // pipe behind a single product (dV of the step before) rather than
     // behind dV, dK and S^T.  S^T(g+1) goes into the region dK(g-1) has just
-    // read (the pipe runs one thread's products in issue order).  At the
+    // read (the pipe runs one warp's products in issue order).  At the
     // first step of a unit, V_j is new and may still be loading: dK(g-1) and
     // S^T(g+1) go first.
     reg_dealloc<R::kRegsCtl>();

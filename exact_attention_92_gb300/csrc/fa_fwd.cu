@@ -9,8 +9,10 @@
 //              A Q buffer is refilled as soon as the last S product that
 //              reads it has completed, so the next unit's Q, K and V arrive
 //              while the current unit's last steps run.
-//   warp 8     MMA issuer (one thread): S_t = Q_t K_j^T and O_t += P_t V_j
-//              with tcgen05 into tensor memory (TMEM).
+//   warp 8     MMA issuer (the whole warp walks the schedule, one elected
+//              lane issues): S_t = Q_t K_j^T and O_t += P_t V_j with tcgen05
+//              into tensor memory (TMEM).  With grouped-query attention the
+//              K, V tiles are those of the query head's key/value head.
 //   warps 0-3  softmax of query tile 0, warps 4-7 of tile 1: each thread owns
 //              one query row (the "split along Q" of section 4.2), so row max
 //              and row sum need no communication.  They also write O and L
