@@ -2,16 +2,18 @@
 """Throughput of exact attention (forward + backward) on GB300.
 
 One step = the whole hot path on one batch: fa_fwd (forward kernel, causal
-tile skip, O and LSE) followed by fa_bwd (D preprocess, backward kernel, dQ
-convert) on B=2, H=16, N=4096, d=128, causal, seeded N(0,1) bf16 inputs.
+tile skip, O and LSE) followed by fa_bwd (D preprocess, dK/dV kernel, dQ
+kernel) on B=2, H=16, N=4096, d=128, causal, seeded N(0,1) bf16 inputs.
 Throughput counts 4*B*H*N^2*d forward FLOPs (halved for causal) plus 2.5x
 that for the backward pass.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-With N > 1 (torchrun, one rank per GPU) each rank runs its own heads of a
-batch N times larger (weak scaling; no data-path collective).  Rank 0 prints
-one JSON line.  ``--impl reference`` times the fp64 CPU oracle instead, on a
+With N > 1 each rank (one per GPU) runs its own heads of a batch N times
+larger (weak scaling; no data-path collective).  Started without a
+torch.distributed environment, ``--gpus N`` launches the N ranks itself
+through torch.distributed.run; under torchrun it joins the ranks it was
+started with.  Rank 0 prints one JSON line.  ``--impl reference`` times the fp64 CPU oracle instead, on a
 bounded sample of the same workload, on the host cores.
 """
 
@@ -354,6 +356,7 @@ def run_ours(args, world, rank, local):
     extra = fwd_targets(fa, device, peaks, args) if (rank == 0 and not args.no_extra) else None
     extra_bwd = bwd_targets(fa, device, peaks, args) if (rank == 0 and not args.no_extra) else None
     extra_gqa = gqa_targets(fa, device, peaks, args) if (rank == 0 and not args.no_extra) else None
+    extra_short = short_targets(fa, device, peaks, args) if (rank == 0 and not args.no_extra) else None
 
     if rank != 0:
         return None
@@ -390,6 +393,8 @@ def run_ours(args, world, rank, local):
         line["bwd_targets"] = extra_bwd
     if extra_gqa is not None:
         line["gqa_targets"] = extra_gqa
+    if extra_short is not None:
+        line["short_targets"] = extra_short
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tf, dt, desc = oracle_sample()
         line["cpu_baseline"] = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
@@ -519,6 +524,78 @@ def bwd_targets(fa, device, peaks, args):
     return out
 
 
+def short_targets(fa, device, peaks, args):
+    """The short-sequence half of the sweep, where the data, not the tensor
+    cores, bound the time: the single head B=1 H=1 N=128 d=64 (launch
+    latency, microseconds per call), B=4 H=16 N=1024 d=64, and the 16K-token
+    sweep at d=64 (every N) and at d=128 for N <= 2048.  Each case reports the
+    forward's TFLOP/s and its algorithmic HBM bytes per second (Q, K, V read
+    and O written as bf16, LSE as fp32) against the measured copy bandwidth;
+    the N=1024 d=64 and N=512 cases also time the backward (Q, K, V, O, dO
+    read, dQ, dK, dV written as bf16, LSE and D as fp32)."""
+    import torch
+
+    from exact_attention_92_gb300 import inputs
+
+    cases = [(1, 1, 128, 64), (4, 16, 1024, 64)]
+    for d in (64, 128):
+        for N in (512, 1024, 2048, 4096, 8192, 16384):
+            if d == 128 and N > 2048:
+                continue
+            cases.append((16384 // N, 2048 // d, N, d))
+    with_bwd = {(4, 16, 1024, 64), (32, 32, 512, 64), (32, 16, 512, 128)}
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    hbm = peaks["hbm_gbs"]
+    out = []
+
+    def timed(fn, reps=20):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for st, en in ev:  # queued before one synchronise (host time stays out)
+            flush.zero_()
+            st.record(stream)
+            fn()
+            en.record(stream)
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in ev) / reps
+
+    for (B, H, N, d) in cases:
+        for causal in (False, True):
+            g = torch.Generator(device=device)
+            g.manual_seed(3000)
+            shape = (B, H, N, d)
+            q, k, v, do = (torch.randn(shape, generator=g, device=device).to(torch.bfloat16) for _ in range(4))
+            o = torch.empty_like(q)
+            lse = torch.empty(shape[:3], dtype=torch.float32, device=device)
+            ms = timed(lambda: fa.fa_fwd(q, k, v, o, lse, causal))
+            fl = inputs.fwd_flops(B, H, N, d, causal)
+            nbytes = 8 * B * H * N * d + 4 * B * H * N
+            gbs = nbytes / ms / 1e6
+            rec = {"case": f"B={B} H={H} N={N} d={d} {'causal' if causal else 'non-causal'} forward",
+                   "us": round(ms * 1e3, 2), "tflops": round(fl / ms / 1e9, 1),
+                   "frac_tensor": round(fl / ms / 1e9 / peaks["bf16_tflops"], 4),
+                   "hbm_gbs": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4), "bytes": nbytes}
+            out.append(rec)
+            if (B, H, N, d) in with_bwd:
+                dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+                ms_b = timed(lambda: fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, causal))
+                nb = 16 * B * H * N * d + 8 * B * H * N
+                gb = nb / ms_b / 1e6
+                out.append({"case": f"B={B} H={H} N={N} d={d} {'causal' if causal else 'non-causal'} backward",
+                            "us": round(ms_b * 1e3, 2), "tflops": round(2.5 * fl / ms_b / 1e9, 1),
+                            "frac_tensor": round(2.5 * fl / ms_b / 1e9 / peaks["bf16_tflops"], 4),
+                            "hbm_gbs": round(gb, 1), "frac_hbm": round(gb / hbm, 4), "bytes": nb})
+                del dq, dk, dv
+            del q, k, v, do, o, lse
+    st = fa.fa_poll_status()
+    if st != 0:
+        raise RuntimeError(f"device status after the short-sequence cases: {fa.fa_strerror(st)}")
+    return out
+
+
 def gqa_targets(fa, device, peaks, args):
     """Grouped-query attention (fa_fwd_gqa, fa_bwd_gqa): 32 query heads over 8
     key/value heads, B=2, N=4096, d=128, causal; FLOPs counted per query head
@@ -621,8 +698,10 @@ def fwd_targets(fa, device, peaks, args):
 
 def run_profile(case):
     """Two warm-up launches, then one launch, of the forward kernel on the GPT
-    layer (B=8 H=32 N=4096 d=128 causal) or of the backward on the fwd+bwd
-    workload, for ``ncu -s 2 -c 1`` captures (inputs 0.1-1 GB, above L2)."""
+    layer (B=8 H=32 N=4096 d=128 causal) or on B=4 H=16 N=1024 d=64
+    non-causal (``fwd_short``, 33.6 MB: the DRAM figures there are those of
+    a problem below the L2 size), or of the backward on the fwd+bwd workload,
+    for ``ncu -s 2 -c 1`` captures."""
     import torch
 
     import exact_attention_92_gb300 as fa
@@ -637,6 +716,8 @@ def run_profile(case):
     g.manual_seed(1)
     if case == "fwd":
         shape, causal = (8, 32, 4096, 128), True
+    elif case == "fwd_short":
+        shape, causal = (4, 16, 1024, 64), False
     else:
         w = WORKLOAD
         shape, causal = (w["B"], w["H"], w["N"], w["d"]), w["causal"]
@@ -647,7 +728,7 @@ def run_profile(case):
     if case == "bwd":
         fa.fa_fwd(q, k, v, o, lse, causal)
     for _ in range(3):
-        if case == "fwd":
+        if case in ("fwd", "fwd_short"):
             fa.fa_fwd_ex(q, k, v, o, lse, causal, None, 1)
         else:
             fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, causal)
@@ -699,6 +780,23 @@ def run_reference(args, world, rank):
     }
 
 
+def free_port():
+    import socket
+
+    with socket.socket(socket.AF_INET, socket.SOCK_STREAM) as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def launch_ranks(n, argv):
+    """Run this script as ``n`` ranks on this node (torch.distributed.run,
+    rendezvous on 127.0.0.1) with the same arguments; returns the launcher's
+    exit status."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr=127.0.0.1", f"--master-port={free_port()}", os.path.abspath(__file__), *argv]
+    return subprocess.call(cmd)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -707,13 +805,15 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true", help="skip the forward-only and backward-only target cases")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip timing the CPU oracle")
-    ap.add_argument("--profile", choices=["fwd", "bwd"], help="3 launches of one kernel, for ncu")
+    ap.add_argument("--profile", choices=["fwd", "fwd_short", "bwd"], help="3 launches of one kernel, for ncu")
     args = ap.parse_args(argv)
     if args.profile:
         run_profile(args.profile)
         return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        raise SystemExit(launch_ranks(args.gpus, sys.argv[1:] if argv is None else list(argv)))
     world, rank, local = dist_setup()
     if args.impl == "reference":
         line = run_reference(args, world, rank)

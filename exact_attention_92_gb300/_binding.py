@@ -120,6 +120,12 @@ def _check_bhnd(name, t, shape=None):
         raise ValueError(f"{name} must be a contiguous [B, H, N, d] tensor")
     if shape is not None and tuple(t.shape) != tuple(shape):
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    # The library works on the current CUDA device (its status word, its
+    # scratch and its launches); a tensor on another device would be read
+    # through the wrong device's context.
+    if t.device.index is not None and t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name} is on {t.device}, but the current CUDA device is "
+                         f"cuda:{torch.cuda.current_device()} (use torch.cuda.device)")
 
 
 def _check_lse(t, shape):

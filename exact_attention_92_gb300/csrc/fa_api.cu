@@ -38,8 +38,8 @@ using fa::FwdParams;
 constexpr int kMaxDevices = 64;
 
 struct DeviceState {
-  std::once_flag once;
-  int err = 0;  // fa_status of the set-up
+  std::mutex mu;
+  bool ready = false;
   int sm_count = 0;
   unsigned int* status = nullptr;  // device address of g_fa_status_word
 };
@@ -59,33 +59,36 @@ void load_encode() {
     g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
 }
 
-// Set-up of the current device, once: compute capability check, SM count and
-// the address of the status word.
+// Set-up of the current device: compute capability check, SM count and the
+// address of the status word (cleared).  It is kept once it has succeeded; a
+// set-up that failed (for instance inside a stream capture, where the
+// clearing memset is not allowed) is tried again by the next call.  A device
+// that is not an sm_103 part is refused every time.
 int device_state(DeviceState** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
   DeviceState& s = g_dev[dev];
-  std::call_once(s.once, [&s, dev]() {
-    cudaDeviceProp prop;
-    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) {
-      s.err = FA_ERR_CUDA;
-      return;
+  {
+    std::lock_guard<std::mutex> g(s.mu);
+    if (!s.ready) {
+      cudaDeviceProp prop;
+      if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return FA_ERR_CUDA;
+      if (!(prop.major == 10 && prop.minor == 3)) return FA_ERR_UNSUPPORTED;
+      void* addr = nullptr;
+      if (cudaGetSymbolAddress(&addr, g_fa_status_word) != cudaSuccess || addr == nullptr) {
+        cudaGetLastError();
+        return FA_ERR_CUDA;
+      }
+      if (cudaMemset(addr, 0, sizeof(unsigned int)) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_CUDA;
+      }
+      s.sm_count = prop.multiProcessorCount;
+      s.status = static_cast<unsigned int*>(addr);
+      s.ready = true;
     }
-    if (!(prop.major == 10 && prop.minor == 3)) {
-      s.err = FA_ERR_UNSUPPORTED;
-      return;
-    }
-    s.sm_count = prop.multiProcessorCount;
-    void* addr = nullptr;
-    if (cudaGetSymbolAddress(&addr, g_fa_status_word) != cudaSuccess) {
-      s.err = FA_ERR_CUDA;
-      return;
-    }
-    s.status = static_cast<unsigned int*>(addr);
-    if (cudaMemset(s.status, 0, sizeof(unsigned int)) != cudaSuccess) s.err = FA_ERR_CUDA;
-  });
-  if (s.err) return s.err;
+  }
   std::call_once(g_encode_once, load_encode);
   if (!g_encode) return FA_ERR_CUDA;
   *out = &s;
@@ -206,7 +209,11 @@ int internal_encode_bhnd(CUtensorMap* m, const void* ptr, int BH, int N, int d) 
   return encode_bhnd(m, ptr, BH, N, d);
 }
 unsigned long long internal_wait_timeout_ns() { return g_timeout_ns.load(); }
-void internal_count_launch(int kernel) { g_launches[kernel].fetch_add(1, std::memory_order_relaxed); }
+// A launch of library kernel `kernel` by another file of the library, counted
+// and (while timing is on) bracketed by events like the launches here.
+cudaError_t internal_timed_launch(int kernel, cudaStream_t stream, cudaError_t (*launch)(void*), void* ctx) {
+  return timed(kernel, stream, [&] { return launch(ctx); });
+}
 }  // namespace fa
 
 extern "C" {

@@ -23,7 +23,9 @@
 // Online softmax (section 6.1): the running max m and sum l live in registers
 // of the row's thread, O~ stays unnormalised in TMEM and is divided by l
 // once at the end; L = m + log l is written for the backward pass.  P is
-// rounded to bf16 for the PV MMA; l sums the fp32 weights.  The
+// rounded to bf16 for the PV MMA, and O~ is divided by the sum of those
+// rounded weights, so O is an exact weighted mean of the rows of V under the
+// weights the MMA used; L takes the sum of the unrounded fp32 weights.  The
 // exp(m_old - m_new) correction of O~ is applied only when a row's max grows
 // by more than 2^8 over the reference the row's O~ and l are kept at;
 // otherwise the old reference stays.  O~ and l always share one reference,
@@ -344,7 +346,8 @@ __global__ void __launch_bounds__(384, 1)
         continue;
       }
       float m_ref = -INFINITY;  // reference max of this row, log2 units
-      float l = 0.f;  // sum of the fp32 weights
+      float l = 0.f;     // sum of the fp32 weights: L = m + log l
+      float l_bf = 0.f;  // sum of the bf16-rounded weights the PV MMA takes: O = O~ / l_bf
       for (int j = 0; j < w.n[t]; ++j) {
         ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t], sc & 1, ctl, kWaitSFull));
         ++sc;
@@ -382,15 +385,18 @@ __global__ void __launch_bounds__(384, 1)
           const float m_new = fmaxf(m_ref, m_tile);
           f = ex2_approx(m_ref - m_new);
           l *= f;
+          l_bf *= f;
           m_ref = m_new;
           rescale = true;
         }
         // P = exp2(S * scale * log2(e) - m_ref), 32 columns at a time, packed
         // to bf16 over the already-read S columns; pairs of columns share the
-        // packed fp32x2 FMA and adds.
+        // packed fp32x2 FMA and adds.  The rounded weights are summed from
+        // the packed pairs (each half converted exactly to fp32).
         const float2 sl2v = make_float2(sl2, sl2);
         const float2 negv = make_float2(-m_ref, -m_ref);
         float2 ls0 = make_float2(0.f, 0.f), ls1 = ls0;
+        float lr0 = 0.f, lr1 = 0.f, lr2 = 0.f, lr3 = 0.f;
 #pragma unroll
         for (int h = 0; h < kTileN / 32; ++h) {
           uint32_t pk[16];
@@ -399,15 +405,22 @@ __global__ void __launch_bounds__(384, 1)
             const float2 a = __ffma2_rn(make_float2(x[32 * h + e], x[32 * h + e + 1]), sl2v, negv);
             const float p0 = ex2_approx(a.x);
             const float p1 = ex2_approx(a.y);
-            if ((e >> 1) & 1)
+            const uint32_t pp = pack_bf16(p0, p1);
+            if ((e >> 1) & 1) {
               ls1 = __fadd2_rn(ls1, make_float2(p0, p1));
-            else
+              lr2 = add_bf16_lo(lr2, pp);
+              lr3 = add_bf16_hi(lr3, pp);
+            } else {
               ls0 = __fadd2_rn(ls0, make_float2(p0, p1));
-            pk[e / 2] = pack_bf16(p0, p1);
+              lr0 = add_bf16_lo(lr0, pp);
+              lr1 = add_bf16_hi(lr1, pp);
+            }
+            pk[e / 2] = pp;
           }
           tmem_st16(tS + 16 * h, pk);
         }
         l += (ls0.x + ls0.y) + (ls1.x + ls1.y);
+        l_bf += (lr0 + lr1) + (lr2 + lr3);
         if (rescale) {
           // O~ <- exp2(m_old - m_new) O~; the previous PV MMA has completed
           // (it was issued before this S tile's MMA) and the next one waits
@@ -436,7 +449,7 @@ __global__ void __launch_bounds__(384, 1)
       ++oc;
       if (!ok) break;
       tc_fence_after();
-      const float inv_l = 1.0f / l;
+      const float inv_l = 1.0f / l_bf;
       const float lse = (m_ref + lg2_approx(l)) * 0.69314718055994530942f;
       if (p.num_splits == 1) {
         // O = O~ / l in bf16, 64 columns (128 bytes of the row) at a time,

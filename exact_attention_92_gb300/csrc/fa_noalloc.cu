@@ -21,7 +21,7 @@ int internal_device_setup(unsigned int** status, int* sm_count);
 int internal_validate(int B, int H, int N, int d, float scale);
 int internal_encode_bhnd(CUtensorMap* m, const void* ptr, int BH, int N, int d);
 unsigned long long internal_wait_timeout_ns();
-void internal_count_launch(int kernel);
+cudaError_t internal_timed_launch(int kernel, cudaStream_t stream, cudaError_t (*launch)(void*), void* ctx);
 cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const BwdParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_bwd_dq(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
@@ -35,30 +35,56 @@ namespace {
 constexpr int kMaxDevices = 64;
 
 struct ScratchState {
-  std::once_flag once;
-  int err = 0;
-  unsigned char* ptr = nullptr;  // device address of g_fa_bwd_scratch
+  std::mutex mu;
+  unsigned char* ptr = nullptr;  // device address of g_fa_bwd_scratch, once known
 };
 ScratchState g_scratch[kMaxDevices];
 
-// Device address of the scratch array on the current device (set up once).
+// Device address of the scratch array on the current device.  The lookup is
+// kept once it has succeeded; a failed one is tried again by the next call.
 int scratch_address(unsigned char** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
   ScratchState& s = g_scratch[dev];
-  std::call_once(s.once, [&s]() {
+  std::lock_guard<std::mutex> g(s.mu);
+  if (s.ptr == nullptr) {
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_fa_bwd_scratch);
     if (e != cudaSuccess || p == nullptr) {
-      s.err = FA_ERR_CUDA;
-      return;
+      cudaGetLastError();
+      return FA_ERR_CUDA;
     }
     s.ptr = static_cast<unsigned char*>(p);
-  });
-  if (s.err) return s.err;
+  }
   *out = s.ptr;
   return FA_OK;
+}
+
+// The three launches of the backward pass, each through the library's
+// launch counter and per-kernel timing.
+struct Launch {
+  int d;
+  const void* o;
+  const void* dout;
+  float* dvec;
+  int rows;
+  const CUtensorMap *tq, *tk, *tv, *tdo;
+  const fa::BwdParams* p;
+  int grid;
+  cudaStream_t st;
+};
+cudaError_t run_pre(void* c) {
+  const Launch& l = *static_cast<const Launch*>(c);
+  return fa::launch_bwd_preprocess(l.d, l.o, l.dout, l.dvec, l.rows, l.st);
+}
+cudaError_t run_dkdv(void* c) {
+  const Launch& l = *static_cast<const Launch*>(c);
+  return fa::launch_bwd_dkdv(l.d, *l.tq, *l.tk, *l.tv, *l.tdo, *l.p, l.grid, l.st);
+}
+cudaError_t run_dq(void* c) {
+  const Launch& l = *static_cast<const Launch*>(c);
+  return fa::launch_bwd_dq(l.d, *l.tq, *l.tk, *l.tv, *l.tdo, *l.p, l.grid, l.st);
 }
 
 bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -119,15 +145,9 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
   p.timeout_ns = fa::internal_wait_timeout_ns();
 
   const int grid = p.num_units < sm_count ? p.num_units : sm_count;
-  cudaError_t ce = fa::launch_bwd_preprocess(d, o, dout, dvec, (int)rows, st);
-  if (ce == cudaSuccess) {
-    fa::internal_count_launch(FA_KERNEL_BWD_PRE);
-    ce = fa::launch_bwd_dkdv(d, tq, tk, tv, tdo, p, grid, st);
-  }
-  if (ce == cudaSuccess) {
-    fa::internal_count_launch(FA_KERNEL_BWD);
-    ce = fa::launch_bwd_dq(d, tq, tk, tv, tdo, p, grid, st);
-  }
-  if (ce == cudaSuccess) fa::internal_count_launch(FA_KERNEL_BWD_DQ);
+  Launch l{d, o, dout, dvec, (int)rows, &tq, &tk, &tv, &tdo, &p, grid, st};
+  cudaError_t ce = fa::internal_timed_launch(FA_KERNEL_BWD_PRE, st, run_pre, &l);
+  if (ce == cudaSuccess) ce = fa::internal_timed_launch(FA_KERNEL_BWD, st, run_dkdv, &l);
+  if (ce == cudaSuccess) ce = fa::internal_timed_launch(FA_KERNEL_BWD_DQ, st, run_dq, &l);
   return ce == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }

@@ -365,6 +365,24 @@ __device__ __forceinline__ void store_rows(uint8_t* row_ptr, size_t stride, int 
   }
 }
 
+// acc + the low / high bf16 half of a packed pair: the half is converted to
+// fp32 exactly and added with round-to-nearest (the mixed-precision add of
+// sm_100 and later).
+__device__ __forceinline__ float add_bf16_lo(float acc, uint32_t pk) {
+  float r;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.bf16 %0, lo, %2;\n\t}"
+      : "=f"(r)
+      : "r"(pk), "f"(acc));
+  return r;
+}
+__device__ __forceinline__ float add_bf16_hi(float acc, uint32_t pk) {
+  float r;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.bf16 %0, hi, %2;\n\t}"
+      : "=f"(r)
+      : "r"(pk), "f"(acc));
+  return r;
+}
+
 // Two floats to packed bf16 (round to nearest even); `lo` in bits [0,16).
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   uint32_t r;

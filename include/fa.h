@@ -24,9 +24,10 @@
  *  - Calls are asynchronous on `stream` (a cudaStream_t; 0 = legacy default
  *    stream) and never synchronise it, except fa_poll_status.
  *  - The caller owns every buffer it passes; the library never frees or keeps
- *    them.  Temporary device workspace (split-KV partials, the fp32 dQ
- *    accumulator) is taken with cudaMallocAsync on `stream` and returned with
- *    cudaFreeAsync on the same stream, so it is stream-ordered.
+ *    them.  Temporary device workspace (the fp32 split-KV partials of the
+ *    forward pass, the fp32 D vector of the backward pass) is taken with
+ *    cudaMallocAsync on `stream` and returned with cudaFreeAsync on the same
+ *    stream, so it is stream-ordered.
  *  - Return value: FA_OK, or an fa_status code.  Argument errors are detected
  *    on the host before anything is launched.  A device-side wait that gives
  *    up (see fa_set_wait_timeout_ns) is reported later by fa_poll_status.
@@ -129,14 +130,16 @@ int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const
  * counterpart: this is a library convenience.
  *
  * fa_bwd takes its fp32 workspace (D, B*H*N*4 bytes) from cudaMallocAsync
- * on every call.  Some callers cannot allow
- * that: a caller capturing a CUDA graph that must contain no memory-
- * allocation nodes, and a caller that has handed nearly all device memory
- * to its own pool up front (weights, KV caches) and cannot have a library
- * take megabytes in the middle of a step.  fa_bwd_noalloc runs the same
- * three kernels as fa_bwd, with the workspace in one static device
- * array of FA_BWD_NOALLOC_SCRATCH_BYTES, which every device that sets this
- * entry point up keeps until the process exits.
+ * on every call.  Some callers cannot allow that: a caller that has handed
+ * nearly all device memory to its own pool up front (weights, KV caches,
+ * activations) and cannot have a library take memory in the middle of a
+ * step, or one whose memory budget is fixed when it starts.  fa_bwd_noalloc
+ * runs the same three kernels as fa_bwd, with the workspace in one static
+ * device array of FA_BWD_NOALLOC_SCRATCH_BYTES (64 MiB).  The array belongs
+ * to the library's module: it is reserved on every device where that module
+ * is loaded (at the first use of the library on the device with lazy module
+ * loading, the CUDA default; when the context is created with
+ * CUDA_MODULE_LOADING=EAGER), and it stays reserved until the process exits.
  *
  *  - Arguments, layouts and ownership as fa_bwd; the caller still passes
  *    (and owns) every input and output.
@@ -144,7 +147,8 @@ int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const
  *    B*H*N*4 exceeds FA_BWD_NOALLOC_SCRATCH_BYTES.
  *  - The first call on a device sets up that device (with it current): it
  *    looks up the array's device address, and the library's status word,
- *    once.  Make that first call before any stream capture.
+ *    and keeps them.  Make that first call before any stream capture; a
+ *    set-up that fails is not kept, and the next call tries again.
  *  - It calls no cudaMalloc/cudaMallocAsync/cudaFree and no allocating
  *    routine of any other library.
  *  - All calls on a device share the one array, and it keeps the last
@@ -152,6 +156,8 @@ int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const
  *    reading it.  Two calls whose kernels overlap on the GPU
  *    (different streams, or different host threads) race on the array and
  *    give wrong gradients: serialise them.
+ *  - Its launches are counted by fa_launch_count and timed by
+ *    fa_timing_enable / fa_timing_read like those of fa_bwd.
  */
 #define FA_BWD_NOALLOC_SCRATCH_BYTES (64u << 20)
 int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,

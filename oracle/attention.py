@@ -178,6 +178,30 @@ def backward_dq_rows_head(q, k, v, do, scale, causal, rows):
     return scale * (ds @ k)
 
 
+def backward_dkdv_rows_head(q, k, v, do, scale, causal, key_rows):
+    """dK and dV on selected key rows of one head.
+
+    dV_j = sum_i P_ij dO_i and dK_j = scale sum_i dS_ij Q_i take column j of P
+    and of dS over every query row i.  P_ij = exp(S_ij - L_i) with the row's
+    logsumexp L_i (section 7.1), and D_i = rowsum(dO_i * O_i) needs the row's
+    output (section 7.3), so the whole forward pass (forward_head) runs first;
+    then only the selected columns of S, P, dP and dS are formed.
+    """
+    key_rows = np.asarray(key_rows)
+    n = q.shape[0]
+    o, L = forward_head(q, k, v, scale, causal)
+    s = scale * (q @ k[key_rows].T)
+    if causal:
+        s = np.where(_visible(np.arange(n), k.shape[0])[:, key_rows], s, -np.inf)
+    p = np.exp(s - L[:, None])
+    dp = do @ v[key_rows].T
+    D = _d_vector(do, o)
+    ds = p * (dp - D[:, None])
+    dv = p.T @ do
+    dk = scale * (ds.T @ q)
+    return dk, dv
+
+
 def merge_partials(o_parts, L_parts):
     """Merge attention results computed over disjoint key subsets.
 

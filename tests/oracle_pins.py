@@ -201,6 +201,9 @@ def pin_backward_finite_differences(att):
             rows = np.array([0, N // 2, N - 1])
             dqr = att.backward_dq_rows_head(q, k, v, do, scale, causal, rows)
             assert np.max(np.abs(dqr - gq[rows])) <= 1e-7 * max(1.0, np.max(np.abs(gq)))
+            dkr, dvr = att.backward_dkdv_rows_head(q, k, v, do, scale, causal, rows)
+            assert np.max(np.abs(dkr - gk[rows])) <= 1e-7 * max(1.0, np.max(np.abs(gk)))
+            assert np.max(np.abs(dvr - gv[rows])) <= 1e-7 * max(1.0, np.max(np.abs(gv)))
 
 
 def pin_d_identity(att):

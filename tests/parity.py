@@ -6,13 +6,15 @@ Tolerances (attention forward / backward on bf16 inputs):
          sit half an ulp away from the fp64 value, more than 1e-2 once
          |O| > 5); and mean |O_gpu - bf16(O_ref)| <= 1e-3.
          An element above that flat bound must still lie within the bound
-         the arithmetic gives: the PV product takes the softmax weights
-         rounded to bf16 (relative error <= u = 2^-8 each) and divides by
-         the fp32 sum of the unrounded weights, so
-           |dO_ic| <= 0.5 ulp(O_ic) + u * sum_j P_ij |V_jc| + 1e-4,
+         that follows from the precisions the method is read to use (P
+         rounded to bf16 for the P V product, O the weighted mean under those
+         weights): each weight has relative error <= u = 2^-8, so the rounded
+         weights renormalised differ from P_ij by at most 2u P_ij and
+           |dO_ic| <= 0.5 ulp(O_ic) + 2u * sum_j P_ij |V_jc - O_ic| + 1e-4,
          computed from the oracle's weights for that row.  Such elements may
-         be at most 1 in 10^4 (rows where a few large weights carry values of
-         magnitude > 2); the raw maximum is reported either way.
+         be at most 1 in 10^6 of the elements checked (none in a check of
+         fewer than 10^6 elements); how many there were is
+         recorded per case (O_EXCEPTIONS) and printed at the end of the run.
   LSE  : |L_gpu - L_ref| <= 1e-4 * max(1, |L_ref|) (relative error, with an
          absolute floor where L is near 0, e.g. causal row 0).
   grads: max |g_gpu - g_ref| <= 5e-2 * max |g_ref|, per tensor.
@@ -41,6 +43,11 @@ def round_bf16(x):
 
 
 U_BF16 = 2.0 ** -8
+O_EXCEPTION_BUDGET = 10 ** -6
+
+# (what, elements checked, elements above the flat bound) of every check_o
+# call of the session; the test session prints it as a summary.
+O_EXCEPTIONS = []
 
 
 def check_o(o_gpu, o_ref, what="", row_weights=None):
@@ -52,16 +59,17 @@ def check_o(o_gpu, o_ref, what="", row_weights=None):
     allowed = np.maximum(O_MAX_ABS, bf16_ulp(o_ref))
     bad = err > allowed
     assert not np.isnan(o_gpu).any(), f"{what}: NaN in O"
+    O_EXCEPTIONS.append((what, int(err.size), int(bad.sum())))
     if bad.any():
         idx = np.argwhere(bad)
         msg = (f"{what}: O max-abs error {err.max():.3e} over the flat bound at {idx[:5].tolist()} "
                f"(ref {o_ref[bad][:5]}, gpu {o_gpu[bad][:5]})")
-        assert row_weights is not None and len(idx) <= max(1, err.size // 10 ** 4), msg
+        assert row_weights is not None and len(idx) <= int(err.size * O_EXCEPTION_BUDGET), msg
         for ix in idx:
             P, V = row_weights(tuple(ix[:-1]))
             c = ix[-1]
             ref = o_ref[tuple(ix)]
-            derived = 0.5 * bf16_ulp(ref) + U_BF16 * float(np.sum(P * np.abs(V[:, c]))) + 1e-4
+            derived = 0.5 * bf16_ulp(ref) + 2 * U_BF16 * float(np.sum(P * np.abs(V[:, c] - ref))) + 1e-4
             assert err[tuple(ix)] <= derived, f"{msg}; derived bound {derived:.3e} at {ix.tolist()}"
     mean = float(np.mean(np.abs(o_gpu - round_bf16(o_ref))))
     assert mean <= O_MEAN_ABS, f"{what}: O mean-abs error {mean:.3e} > {O_MEAN_ABS}"

@@ -127,3 +127,68 @@ def test_many_heads_many_units_per_cta(fa):
         check_grad(dq[b, h], rq, "dQ", what)
         check_grad(dk[b, h], rk, "dK", what)
         check_grad(dv[b, h], rv, "dV", what)
+
+
+def _sweep_case(N, d, causal):
+    """The 16K-token sweep case with these sizes (its seed), with dO."""
+    c = next(c for c in inputs.workload_cases()[3] if (c["N"], c["d"], c["causal"]) == (N, d, causal))
+    return inputs.make_case(**c, with_do=True)
+
+
+def _check_dq_rows(case, dq):
+    q, k, v, do = case.f64("q"), case.f64("k"), case.f64("v"), case.f64("do")
+    rows = inputs.sample_rows_per_head(case.seed, case.B, case.H, case.N)
+    for b in range(case.B):
+        for h in range(case.H):
+            ref = att.backward_dq_rows_head(q[b, h], k[b, h], v[b, h], do[b, h], case.scale, case.causal, rows[b, h])
+            check_grad(dq[b, h, rows[b, h]], ref, "dQ", f"head {(b, h)} sampled rows")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_b4_h16_n4096_d128(fa, causal):
+    """The backward the bench times at N = 4096: dK, dV in full on 4 seeded
+    heads, dQ on 1024 seeded rows of every head."""
+    case = _sweep_case(4096, 128, causal)
+    dq, dk, dv = run(fa, case)
+    q, k, v, do = case.f64("q"), case.f64("k"), case.f64("v"), case.f64("do")
+    rng = np.random.default_rng(case.seed + 11)
+    heads = [(int(i) // case.H, int(i) % case.H) for i in rng.choice(case.B * case.H, 4, replace=False)]
+    rq, rk, rv = att.backward(q, k, v, do, case.scale, causal, heads=heads)
+    for b, h in heads:
+        check_grad(dk[b, h], rk[b, h], "dK", f"head {(b, h)}")
+        check_grad(dv[b, h], rv[b, h], "dV", f"head {(b, h)}")
+    _check_dq_rows(case, dq)
+    assert np.isfinite(dq).all() and np.isfinite(dk).all() and np.isfinite(dv).all()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_b1_h16_n16384_d128(fa, causal):
+    """The backward the bench times at N = 16384: dK, dV on 1024 seeded key
+    rows of 4 seeded heads, dQ on 1024 seeded rows of every head."""
+    case = _sweep_case(16384, 128, causal)
+    dq, dk, dv = run(fa, case)
+    q, k, v, do = case.f64("q"), case.f64("k"), case.f64("v"), case.f64("do")
+    rng = np.random.default_rng(case.seed + 11)
+    for i in rng.choice(case.B * case.H, 4, replace=False):
+        b, h = int(i) // case.H, int(i) % case.H
+        keys = np.sort(rng.choice(case.N, inputs.SAMPLE_ROWS, replace=False))
+        rk, rv = att.backward_dkdv_rows_head(q[b, h], k[b, h], v[b, h], do[b, h], case.scale, causal, keys)
+        check_grad(dk[b, h, keys], rk, "dK", f"head {(b, h)} sampled key rows")
+        check_grad(dv[b, h, keys], rv, "dV", f"head {(b, h)} sampled key rows")
+    _check_dq_rows(case, dq)
+    assert np.isfinite(dq).all() and np.isfinite(dk).all() and np.isfinite(dv).all()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_b4_h16_n1024_d64(fa, causal):
+    """Backward at the B=4 H=16 N=1024 d=64 shape, every head in full."""
+    c = next(c for c in inputs.workload_cases()[2] if c["causal"] == causal and "degenerate" not in c)
+    case = inputs.make_case(**c, with_do=True)
+    dq, dk, dv = run(fa, case)
+    rq, rk, rv = att.backward(case.f64("q"), case.f64("k"), case.f64("v"), case.f64("do"), case.scale, causal)
+    for b in range(case.B):
+        for h in range(case.H):
+            what = f"head {(b, h)} causal={causal}"
+            check_grad(dq[b, h], rq[b, h], "dQ", what)
+            check_grad(dk[b, h], rk[b, h], "dK", what)
+            check_grad(dv[b, h], rv[b, h], "dV", what)

@@ -57,3 +57,24 @@ def test_single_rank_reduce_is_identity():
     assert bench.reduce_max_sum(1, [1.5, 2.0], [3.0], None) == ([1.5, 2.0], [3.0])
     s = bench.shard_heads(2, 16, 1, 0)
     assert s["batch_offset"] == 0 and s["B"] == 2
+
+
+def test_gpus_flag_starts_that_many_ranks():
+    """``bench.py --gpus 2`` started without a torch.distributed environment
+    launches two ranks itself (torch.distributed.run on 127.0.0.1, gloo on a
+    machine without CUDA); rank 0 alone prints the JSON line, with n_gpus 2.
+    The reference arm runs here since it needs no GPU."""
+    import json
+    import subprocess
+    import sys
+
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    r = subprocess.run([sys.executable, os.path.join(os.path.dirname(bench.__file__), "bench.py"), "--gpus", "2",
+                        "--impl", "reference", "--steps", "1", "--warmup", "3"],
+                       capture_output=True, text=True, env=env, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2
