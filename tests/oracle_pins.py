@@ -297,6 +297,93 @@ def pin_gqa_one_group_per_head(att):
         assert np.array_equal(a, b)
 
 
+# --------------------------------------------------------------------------
+# Queries and keys of different lengths.  Each alignment is pinned through
+# the square causal case (Nq = Nk, pinned by brute force above) and closed
+# forms, not by restating its mask:
+#  * bottom-right: the Nq rows are the last Nq rows of a causal self-attention
+#    over all Nk positions (what a decoder computes for the newest Nq tokens);
+#    rows that no position of that self-attention corresponds to (Nq > Nk)
+#    see no key: O = 0, L = -inf;
+#  * top-left: the Nq rows are the first rows of a causal self-attention over
+#    the keys, and rows past the last key see every key (no mask);
+#  * one query row: bottom-right sees every key (the unmasked result),
+#    top-left sees key 0 alone (O = V_0, L = scale q . k_0).
+# --------------------------------------------------------------------------
+
+def _square_causal_rows(att, q_rows, k, v, scale, rows):
+    """Rows ``rows`` of causal self-attention over len(k) positions whose
+    queries at those rows are q_rows (other queries do not matter)."""
+    nk, d = k.shape
+    qq = np.zeros((nk, d))
+    qq[rows] = q_rows
+    O, L = att.forward_head(qq, k, v, scale, True)
+    return O[rows], L[rows]
+
+
+def pin_unequal_lengths_alignments(att):
+    d, scale = 4, 0.5
+    for nq, nk in ((1, 9), (3, 9), (9, 9), (5, 2), (12, 7), (1, 1), (4, 1)):
+        seed = 100 * nq + nk
+        q = _rng_f64(seed, (nq, d))
+        k = _rng_f64(seed + 1, (nk, d))
+        v = _rng_f64(seed + 2, (nk, d))
+        # bottom-right
+        off = att.causal_offset(nq, nk, "bottom_right")
+        O, L = att.forward_head(q, k, v, scale, True, offset=off)
+        empty = max(0, nq - nk)
+        assert np.all(O[:empty] == 0.0) and np.all(L[:empty] == -np.inf), (nq, nk)
+        rows = np.arange(nk - (nq - empty), nk)
+        Ow, Lw = _square_causal_rows(att, q[empty:], k, v, scale, rows)
+        assert np.allclose(O[empty:], Ow, atol=1e-12) and np.allclose(L[empty:], Lw, atol=1e-12), (nq, nk)
+        # top-left
+        off = att.causal_offset(nq, nk, "top_left")
+        O, L = att.forward_head(q, k, v, scale, True, offset=off)
+        m = min(nq, nk)
+        Ow, Lw = _square_causal_rows(att, q[:m], k, v, scale, np.arange(m))
+        assert np.allclose(O[:m], Ow, atol=1e-12) and np.allclose(L[:m], Lw, atol=1e-12), (nq, nk)
+        if nq > nk:
+            Of, Lf = att.forward_head(q[nk:], k, v, scale, False)
+            assert np.allclose(O[nk:], Of, atol=1e-12) and np.allclose(L[nk:], Lf, atol=1e-12), (nq, nk)
+        if nq == 1:
+            Ob, Lb = att.forward_head(q, k, v, scale, True, offset=att.causal_offset(1, nk, "bottom_right"))
+            Of, Lf = brute_force_head(q.tolist() + [[0.0] * d] * (nk - 1), k.tolist(), v.tolist(), scale, False)
+            assert np.allclose(Ob, Of[:1], atol=1e-12) and np.allclose(Lb, Lf[:1], atol=1e-12)
+            assert np.allclose(O[0], v[0], atol=1e-14) and abs(L[0] - scale * float(q[0] @ k[0])) < 1e-12
+
+
+def pin_unequal_lengths_finite_differences(att):
+    """Gradients with Nq != Nk, both alignments (rows that see no key
+    included), against central differences of the forward pass."""
+    d, scale = 3, 0.6
+    for nq, nk, align in ((3, 7, "bottom_right"), (6, 4, "bottom_right"), (6, 4, "top_left"),
+                          (2, 5, "top_left")):
+        seed = 7 * nq + nk
+        q = _rng_f64(seed, (nq, d))
+        k = _rng_f64(seed + 1, (nk, d))
+        v = _rng_f64(seed + 2, (nk, d))
+        do = _rng_f64(seed + 3, (nq, d))
+        off = att.causal_offset(nq, nk, align)
+
+        def loss(qq, kk, vv):
+            O, _ = att.forward_head(qq, kk, vv, scale, True, offset=off)
+            return float(np.sum(do * O))
+
+        gq = _fd_grad(lambda x: loss(x, k, v), q)
+        gk = _fd_grad(lambda x: loss(q, x, v), k)
+        gv = _fd_grad(lambda x: loss(q, k, x), v)
+        dq, dk, dv = att.backward_head(q, k, v, do, scale, True, offset=off)
+        for g, a in ((gq, dq), (gk, dk), (gv, dv)):
+            assert np.max(np.abs(g - a)) <= 1e-7 * max(1.0, np.max(np.abs(g))), (nq, nk, align)
+        rows = np.arange(nq)
+        dqr = att.backward_dq_rows_head(q, k, v, do, scale, True, rows, offset=off)
+        assert np.max(np.abs(dqr - gq)) <= 1e-7 * max(1.0, np.max(np.abs(gq)))
+        keys = np.arange(nk)
+        dkr, dvr = att.backward_dkdv_rows_head(q, k, v, do, scale, True, keys, offset=off)
+        assert np.max(np.abs(dkr - gk)) <= 1e-7 * max(1.0, np.max(np.abs(gk)))
+        assert np.max(np.abs(dvr - gv)) <= 1e-7 * max(1.0, np.max(np.abs(gv)))
+
+
 ALL_PINS = [
     pin_brute_force,
     pin_rows_sum_to_one,
@@ -312,4 +399,6 @@ ALL_PINS = [
     pin_gqa_routing,
     pin_gqa_finite_differences,
     pin_gqa_one_group_per_head,
+    pin_unequal_lengths_alignments,
+    pin_unequal_lengths_finite_differences,
 ]

@@ -25,9 +25,16 @@ MUTANTS = {
     # forward
     "scale_dropped": ("_scores", lambda q, k, scale: q @ k.T),
     "operands_transposed": ("_scores", lambda q, k, scale: scale * (k @ q.T)),
-    "mask_flipped": ("_visible", lambda rows, n_k: np.arange(n_k)[None, :] >= rows[:, None]),
-    "mask_strict": ("_visible", lambda rows, n_k: np.arange(n_k)[None, :] < rows[:, None]),
-    "mask_off_by_one": ("_visible", lambda rows, n_k: np.arange(n_k)[None, :] <= rows[:, None] + 1),
+    "mask_flipped": ("_visible", lambda rows, n_k, off=0: np.arange(n_k)[None, :] >= rows[:, None] + off),
+    "mask_strict": ("_visible", lambda rows, n_k, off=0: np.arange(n_k)[None, :] < rows[:, None] + off),
+    "mask_off_by_one": ("_visible", lambda rows, n_k, off=0: np.arange(n_k)[None, :] <= rows[:, None] + off + 1),
+    # queries and keys of different lengths
+    "offset_ignored": ("_visible", lambda rows, n_k, off=0: np.arange(n_k)[None, :] <= rows[:, None]),
+    "offset_negated": ("_visible", lambda rows, n_k, off=0: np.arange(n_k)[None, :] <= rows[:, None] - off),
+    "bottom_right_as_top_left": ("causal_offset", lambda n_q, n_k, align: 0),
+    "bottom_right_reversed": ("causal_offset", lambda n_q, n_k, align: 0 if align == "top_left" else n_q - n_k),
+    "empty_rows_uniform": ("_normalise", lambda p, l: p / np.where(l > 0, l, 1.0)[:, None]
+                           + (l == 0)[:, None] / p.shape[1]),
     "max_sign": ("_softmax_stats", lambda s: (lambda m: (m, np.exp(s + m[:, None]), np.sum(np.exp(s + m[:, None]), axis=1)))(np.max(s, axis=1))),
     "lse_without_max": ("_lse", lambda m, l: np.log(l)),
     "lse_log2": ("_lse", lambda m, l: m + np.log2(l)),
