@@ -11,6 +11,9 @@ from ._binding import (  # noqa: F401
     FA_ERR_CUDA,
     FA_ERR_INVALID_ARG,
     FA_BWD_NOALLOC_SCRATCH_BYTES,
+    FA_CAUSAL_BOTTOM_RIGHT,
+    FA_CAUSAL_NONE,
+    FA_CAUSAL_TOP_LEFT,
     FA_ERR_NO_MEMORY,
     FA_ERR_SCRATCH_TOO_SMALL,
     FA_ERR_TIMEOUT,
@@ -21,10 +24,12 @@ from ._binding import (  # noqa: F401
     declared_symbols,
     fa_abi_version,
     fa_bwd,
+    fa_bwd_general,
     fa_bwd_gqa,
     fa_bwd_noalloc,
     fa_fwd,
     fa_fwd_ex,
+    fa_fwd_general,
     fa_fwd_gqa,
     fa_poll_status,
     fa_selftest_wait_timeout,

@@ -27,6 +27,10 @@ FA_ERR_NO_MEMORY = 4
 FA_ERR_TIMEOUT = 5
 FA_ERR_SCRATCH_TOO_SMALL = 6
 FA_BWD_NOALLOC_SCRATCH_BYTES = 64 << 20
+FA_CAUSAL_NONE = 0
+FA_CAUSAL_TOP_LEFT = 1
+FA_CAUSAL_BOTTOM_RIGHT = 2
+_CAUSAL_NAMES = {"none": FA_CAUSAL_NONE, "top_left": FA_CAUSAL_TOP_LEFT, "bottom_right": FA_CAUSAL_BOTTOM_RIGHT}
 
 
 class FaError(RuntimeError):
@@ -51,6 +55,8 @@ _SIGNATURES = {
     "fa_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp], _i),
     "fa_bwd_gqa": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp], _i),
     "fa_bwd_noalloc": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp], _i),
+    "fa_fwd_general": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _i, _vp], _i),
+    "fa_bwd_general": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _vp], _i),
     "fa_poll_status": ([_vp], _i),
     "fa_set_wait_timeout_ns": ([_u64], _u64),
     "fa_selftest_wait_timeout": ([_u64, _vp], _i),
@@ -178,6 +184,54 @@ def fa_fwd_gqa(q, k, v, o, lse, causal=False, scale=None, num_splits=0, stream=N
     _check(st, "fa_fwd_gqa")
 
 
+def _causal_code(causal):
+    """False/True (top-left), or a FA_CAUSAL_* code, or its name."""
+    if isinstance(causal, str):
+        if causal not in _CAUSAL_NAMES:
+            raise ValueError(f"causal must be one of {sorted(_CAUSAL_NAMES)}, got {causal!r}")
+        return _CAUSAL_NAMES[causal]
+    if isinstance(causal, bool):
+        return FA_CAUSAL_TOP_LEFT if causal else FA_CAUSAL_NONE
+    return int(causal)
+
+
+def fa_fwd_general(q, k, v, o, lse, causal=False, scale=None, num_splits=0, stream=None):
+    """C fa_fwd_general: q, o [B, H, Nq, d], k, v [B, Hkv, Nk, d];
+    causal False / True (top-left) / "top_left" / "bottom_right" or a
+    FA_CAUSAL_* code."""
+    _check_bhnd("q", q)
+    B, H, Nq, d = q.shape
+    _check_bhnd("k", k)
+    Hkv, Nk = k.shape[1], k.shape[2]
+    _check_bhnd("k", k, (B, Hkv, Nk, d))
+    _check_bhnd("v", v, (B, Hkv, Nk, d))
+    _check_bhnd("o", o, q.shape)
+    _check_lse(lse, (B, H, Nq))
+    lib = load()
+    st = lib.fa_fwd_general(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, Nq, Nk, d,
+                            _causal_code(causal), _scale(scale, d), int(num_splits), _stream_ptr(stream, q.device))
+    _check(st, "fa_fwd_general")
+
+
+def fa_bwd_general(q, k, v, o, lse, dout, dq, dk, dv, causal=False, scale=None, stream=None):
+    """C fa_bwd_general: gradients for fa_fwd_general (same shapes and
+    causal argument); dk, dv have the shape of k, v."""
+    _check_bhnd("q", q)
+    B, H, Nq, d = q.shape
+    _check_bhnd("k", k)
+    Hkv, Nk = k.shape[1], k.shape[2]
+    for name, t in (("k", k), ("v", v), ("dk", dk), ("dv", dv)):
+        _check_bhnd(name, t, (B, Hkv, Nk, d))
+    for name, t in (("o", o), ("dout", dout), ("dq", dq)):
+        _check_bhnd(name, t, q.shape)
+    _check_lse(lse, (B, H, Nq))
+    lib = load()
+    st = lib.fa_bwd_general(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+                            _ptr(dv), B, H, Hkv, Nq, Nk, d, _causal_code(causal), _scale(scale, d),
+                            _stream_ptr(stream, q.device))
+    _check(st, "fa_bwd_general")
+
+
 def fa_bwd_gqa(q, k, v, o, lse, dout, dq, dk, dv, causal=False, scale=None, stream=None):
     """C fa_bwd_gqa: gradients for grouped-query attention; dk, dv have the
     shape of k, v ([B, Hkv, N, d]) and hold the sums over each group."""
@@ -272,22 +326,31 @@ def fa_launch_count(kernel: int) -> int:
 # ------------------------------------------------------- convenience calls
 
 def forward(q, k, v, causal=False, scale=None, num_splits=0):
-    """Allocate O and LSE and run fa_fwd_ex; returns (o, lse)."""
+    """Allocate O and LSE and run the forward pass; returns (o, lse).  k, v
+    may have fewer heads (grouped-query) or another length than q
+    (fa_fwd_general; causal may then be "top_left" or "bottom_right")."""
     import torch
 
     B, H, N, d = q.shape
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    fa_fwd_ex(q, k, v, o, lse, causal, scale, num_splits)
+    if tuple(k.shape) == tuple(q.shape) and not isinstance(causal, str):
+        fa_fwd_ex(q, k, v, o, lse, causal, scale, num_splits)
+    else:
+        fa_fwd_general(q, k, v, o, lse, causal, scale, num_splits)
     return o, lse
 
 
 def backward(q, k, v, o, lse, dout, causal=False, scale=None):
-    """Allocate dQ, dK, dV and run fa_bwd; returns (dq, dk, dv)."""
+    """Allocate dQ, dK, dV and run the backward pass; returns (dq, dk, dv)
+    (shapes and causal argument as for ``forward``)."""
     import torch
 
     dq = torch.empty_like(q)
     dk = torch.empty_like(k)
     dv = torch.empty_like(v)
-    fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, causal, scale)
+    if tuple(k.shape) == tuple(q.shape) and not isinstance(causal, str):
+        fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, causal, scale)
+    else:
+        fa_bwd_general(q, k, v, o, lse, dout, dq, dk, dv, causal, scale)
     return dq, dk, dv

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -97,20 +98,25 @@ int device_state(DeviceState** out) {
 
 bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int validate(int B, int H, int N, int d, float scale) {
-  if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+int validate(int B, int H, int Nq, int Nk, int d, float scale) {
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return FA_ERR_INVALID_ARG;
   if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-  const long double elems = (long double)B * H * N * d;
-  if (elems >= 9.0e18L) return FA_ERR_INVALID_ARG;
-  if ((long long)B * H > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
-  if ((long long)B * H * ((N + 255) / 256) * 64 > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 96 && d != 128) return FA_ERR_UNSUPPORTED;
+  const long double n = Nq > Nk ? Nq : Nk;
+  if ((long double)B * H * n * d >= 9.0e18L) return FA_ERR_INVALID_ARG;
+  // Row and unit indices are 32-bit: B*H*Nq rows, (query block, split) units.
+  if ((long long)B * H * Nq > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  if ((long long)B * H * ((Nq + 255) / 256) * 64 > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  if ((long long)B * H * ((Nk + 127) / 128) > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
   return FA_OK;
 }
 
+// Mask offset of the causal code: query row i sees keys j <= i + offset.
+int causal_offset(int causal, int Nq, int Nk) { return causal == FA_CAUSAL_BOTTOM_RIGHT ? Nk - Nq : 0; }
+
 // [B*H, N, d] bf16 viewed as a 3-D tensor (d innermost); boxes of 64 x 128 x 1
-// with the 128-byte swizzle the MMA descriptors expect.  Rows past N read as
-// zero.
+// with the 128-byte swizzle the MMA descriptors expect.  Rows past N, and the
+// columns of the second 64-column box past d = 96, read as zero.
 int encode_bhnd(CUtensorMap* m, const void* ptr, int BH, int N, int d) {
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
@@ -125,9 +131,9 @@ int encode_bhnd(CUtensorMap* m, const void* ptr, int BH, int N, int d) {
 // Number of key splits: only when the (batch*head, query block) units cannot
 // fill the GPU.  Picks the split count with the best last-wave occupancy,
 // keeping at least 4 key tiles per split.
-int choose_splits(int BH, int N, int sm_count) {
-  const int qblocks = (N + 255) / 256;
-  const int nkv = (N + 127) / 128;
+int choose_splits(int BH, int Nq, int Nk, int sm_count) {
+  const int qblocks = (Nq + 255) / 256;
+  const int nkv = (Nk + 127) / 128;
   const long long units = (long long)BH * qblocks;
   if (units >= 2LL * sm_count) return 1;
   int best = 1;
@@ -204,7 +210,7 @@ int internal_device_setup(unsigned int** status, int* sm_count) {
   *sm_count = s->sm_count;
   return FA_OK;
 }
-int internal_validate(int B, int H, int N, int d, float scale) { return validate(B, H, N, d, scale); }
+int internal_validate(int B, int H, int N, int d, float scale) { return validate(B, H, N, N, d, scale); }
 int internal_encode_bhnd(CUtensorMap* m, const void* ptr, int BH, int N, int d) {
   return encode_bhnd(m, ptr, BH, N, d);
 }
@@ -267,7 +273,7 @@ const char* fa_strerror(int status) {
   switch (status) {
     case FA_OK: return "FA_OK";
     case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: null or misaligned pointer, bad size or scale";
-    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: head dim must be 64 or 128 on an sm_103 GPU";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: head dim must be 64, 96 or 128 on an sm_103 GPU";
     case FA_ERR_CUDA: return "FA_ERR_CUDA: CUDA runtime or launch failure";
     case FA_ERR_NO_MEMORY: return "FA_ERR_NO_MEMORY: workspace allocation failed";
     case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a device-side wait gave up";
@@ -300,28 +306,30 @@ int fa_selftest_wait_timeout(uint64_t timeout_ns, void* stream) {
              : FA_ERR_CUDA;
 }
 
-int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv, int N,
-               int d, int causal, float scale, int num_splits, void* stream) {
+int fa_fwd_general(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv,
+                   int Nq, int Nk, int d, int causal, float scale, int num_splits, void* stream) {
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return FA_ERR_INVALID_ARG;
-  int e = validate(B, H, N, d, scale);
+  int e = validate(B, H, Nq, Nk, d, scale);
   if (e) return e;
   if (Hkv < 1 || H % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (causal < FA_CAUSAL_NONE || causal > FA_CAUSAL_BOTTOM_RIGHT) return FA_ERR_INVALID_ARG;
   if (num_splits < 0) return FA_ERR_INVALID_ARG;
   DeviceState* s = nullptr;
   e = device_state(&s);
   if (e) return e;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int BH = B * H;
-  const int nkv = (N + 127) / 128;
-  int S = num_splits == 0 ? choose_splits(BH, N, s->sm_count) : num_splits;
+  const int nkv = (Nk + 127) / 128;
+  int S = num_splits == 0 ? choose_splits(BH, Nq, Nk, s->sm_count) : num_splits;
   if (S > nkv) S = nkv;
   if (S < 1) S = 1;
   const int per_split = (nkv + S - 1) / S;
   S = (nkv + per_split - 1) / per_split;  // no empty split
 
   CUtensorMap tq, tk, tv;
-  if (encode_bhnd(&tq, q, BH, N, d) || encode_bhnd(&tk, k, B * Hkv, N, d) || encode_bhnd(&tv, v, B * Hkv, N, d))
+  if (encode_bhnd(&tq, q, BH, Nq, d) || encode_bhnd(&tk, k, B * Hkv, Nk, d) ||
+      encode_bhnd(&tv, v, B * Hkv, Nk, d))
     return FA_ERR_CUDA;
 
   FwdParams p;
@@ -329,12 +337,14 @@ int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
   p.B = B;
   p.H = H;
   p.Hkv = Hkv;
-  p.N = N;
-  p.causal = causal ? 1 : 0;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.causal = causal != FA_CAUSAL_NONE ? 1 : 0;
+  p.causal_off = causal_offset(causal, Nq, Nk);
   p.scale_log2 = scale * 1.4426950408889634f;
   p.num_splits = S;
   p.kv_tiles_per_split = per_split;
-  p.num_q_blocks = (N + 255) / 256;
+  p.num_q_blocks = (Nq + 255) / 256;
   p.num_units = BH * p.num_q_blocks * S;
   p.o = o;
   p.lse = lse;
@@ -343,7 +353,7 @@ int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
   p.timeout_ns = g_timeout_ns.load();
 
   void* ws = nullptr;
-  const size_t rows = (size_t)BH * N;
+  const size_t rows = (size_t)BH * Nq;
   if (S > 1) {
     const size_t bytes = (size_t)S * rows * ((size_t)d + 1) * sizeof(float);
     if (cudaMallocAsync(&ws, bytes, st) != cudaSuccess) {
@@ -369,6 +379,12 @@ int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
   return ce == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv, int N,
+               int d, int causal, float scale, int num_splits, void* stream) {
+  return fa_fwd_general(q, k, v, o, lse, B, H, Hkv, N, N, d, causal ? FA_CAUSAL_TOP_LEFT : FA_CAUSAL_NONE, scale,
+                        num_splits, stream);
+}
+
 int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
               int causal, float scale, int num_splits, void* stream) {
   return fa_fwd_gqa(q, k, v, o, lse, B, H, H, N, d, causal, scale, num_splits, stream);
@@ -379,69 +395,102 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   return fa_fwd_gqa(q, k, v, o, lse, B, H, H, N, d, causal, scale, 0, stream);
 }
 
-int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
-               void* dq, void* dk, void* dv, int B, int H, int Hkv, int N, int d, int causal, float scale,
-               void* stream) {
+int fa_bwd_general(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                   const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int Nq, int Nk, int d,
+                   int causal, float scale, void* stream) {
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dout) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return FA_ERR_INVALID_ARG;
-  int e = validate(B, H, N, d, scale);
+  int e = validate(B, H, Nq, Nk, d, scale);
   if (e) return e;
   if (Hkv < 1 || H % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (causal < FA_CAUSAL_NONE || causal > FA_CAUSAL_BOTTOM_RIGHT) return FA_ERR_INVALID_ARG;
   DeviceState* s = nullptr;
   e = device_state(&s);
   if (e) return e;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int BH = B * H;
-  const size_t rows = (size_t)BH * N;
+  const size_t rows = (size_t)BH * Nq;
 
   CUtensorMap tq, tk, tv, tdo;
-  if (encode_bhnd(&tq, q, BH, N, d) || encode_bhnd(&tk, k, B * Hkv, N, d) || encode_bhnd(&tv, v, B * Hkv, N, d) ||
-      encode_bhnd(&tdo, dout, BH, N, d))
+  if (encode_bhnd(&tq, q, BH, Nq, d) || encode_bhnd(&tk, k, B * Hkv, Nk, d) ||
+      encode_bhnd(&tv, v, B * Hkv, Nk, d) || encode_bhnd(&tdo, dout, BH, Nq, d))
     return FA_ERR_CUDA;
-
-  // Workspace: D [rows].
-  void* ws = nullptr;
-  const size_t bytes = rows * sizeof(float);
-  if (cudaMallocAsync(&ws, bytes, st) != cudaSuccess) {
-    cudaGetLastError();
-    return FA_ERR_NO_MEMORY;
-  }
-  float* dvec = static_cast<float*>(ws);
 
   fa::BwdParams p;
   std::memset(&p, 0, sizeof(p));
   p.B = B;
   p.H = H;
   p.Hkv = Hkv;
-  p.N = N;
-  p.causal = causal ? 1 : 0;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.causal = causal != FA_CAUSAL_NONE ? 1 : 0;
+  p.causal_off = causal_offset(causal, Nq, Nk);
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.lse = lse;
-  p.dvec = dvec;
   p.dq = dq;
   p.dk = dk;
   p.dv = dv;
   p.store32 = ((reinterpret_cast<uintptr_t>(dq) | reinterpret_cast<uintptr_t>(dk) |
                 reinterpret_cast<uintptr_t>(dv)) & 31u) == 0 ? 1 : 0;
-  p.num_tiles = (N + 127) / 128;
-  p.num_units = BH * p.num_tiles;
-  p.num_units_kv = B * Hkv * p.num_tiles;
+  p.num_q_tiles = (Nq + 127) / 128;
+  p.num_k_tiles = (Nk + 127) / 128;
+  // With the causal mask: key tiles past the last key the last query row
+  // sees, and query tiles whose rows all see no key (a negative offset),
+  // take no part; their gradient rows are zero.
+  p.kv_tiles_used = p.num_k_tiles;
+  p.q_tile_first = 0;
+  if (p.causal) {
+    const int last_key = Nq - 1 + p.causal_off;  // >= 0 for both alignments
+    p.kv_tiles_used = std::min(p.num_k_tiles, last_key / 128 + 1);
+    if (p.causal_off < 0) p.q_tile_first = (-p.causal_off) / 128;
+  }
+  p.num_units = BH * (p.num_q_tiles - p.q_tile_first);
+  p.num_units_kv = B * Hkv * p.kv_tiles_used;
   p.group = H / Hkv;
   p.status = s->status;
   p.timeout_ns = g_timeout_ns.load();
 
+  // Workspace: D [rows].
+  void* ws = nullptr;
+  if (cudaMallocAsync(&ws, rows * sizeof(float), st) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_NO_MEMORY;
+  }
+  float* dvec = static_cast<float*>(ws);
+  p.dvec = dvec;
+
+  cudaError_t ce = cudaSuccess;
+  const size_t row_bytes = (size_t)d * 2;
+  if (p.kv_tiles_used < p.num_k_tiles) {
+    const size_t r0 = (size_t)p.kv_tiles_used * 128;
+    for (void* g : {dk, dv})
+      if (ce == cudaSuccess)
+        ce = cudaMemset2DAsync(static_cast<uint8_t*>(g) + r0 * row_bytes, (size_t)Nk * row_bytes, 0,
+                               ((size_t)Nk - r0) * row_bytes, (size_t)B * Hkv, st);
+  }
+  if (ce == cudaSuccess && p.q_tile_first > 0) {
+    const size_t r1 = std::min((size_t)Nq, (size_t)p.q_tile_first * 128);
+    ce = cudaMemset2DAsync(dq, (size_t)Nq * row_bytes, 0, r1 * row_bytes, (size_t)BH, st);
+  }
   const int grid_q = p.num_units < s->sm_count ? p.num_units : s->sm_count;
   const int grid_kv = p.num_units_kv < s->sm_count ? p.num_units_kv : s->sm_count;
-  cudaError_t ce =
-      timed(FA_KERNEL_BWD_PRE, st, [&] { return fa::launch_bwd_preprocess(d, o, dout, dvec, (int)rows, st); });
+  if (ce == cudaSuccess)
+    ce = timed(FA_KERNEL_BWD_PRE, st, [&] { return fa::launch_bwd_preprocess(d, o, dout, dvec, (int)rows, st); });
   if (ce == cudaSuccess)
     ce = timed(FA_KERNEL_BWD, st, [&] { return fa::launch_bwd_dkdv(d, tq, tk, tv, tdo, p, grid_kv, st); });
   if (ce == cudaSuccess)
     ce = timed(FA_KERNEL_BWD_DQ, st, [&] { return fa::launch_bwd_dq(d, tq, tk, tv, tdo, p, grid_q, st); });
   cudaFreeAsync(ws, st);
   return ce == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+               void* dq, void* dk, void* dv, int B, int H, int Hkv, int N, int d, int causal, float scale,
+               void* stream) {
+  return fa_bwd_general(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, N, N, d,
+                        causal ? FA_CAUSAL_TOP_LEFT : FA_CAUSAL_NONE, scale, stream);
 }
 
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,

@@ -33,12 +33,24 @@
 // thread; warps w and w+4 split the 128 columns of a tile) and write the
 // results.
 //
+// Queries and keys may differ in length (Nq, Nk); with the causal mask query
+// row i sees keys j <= i + causal_off.  The dK/dV kernel runs over the key
+// tiles some query row sees, the dQ kernel over the query tiles that see
+// some key; the host zeroes the gradient rows of the others.  A query row
+// that sees no key has L = -inf, which the kernels read as +inf (all of its
+// weights are 0).
+//
+// Head dims 64, 96 and 128; a 96-wide row is staged in the 128-wide layout
+// (TMA zero-fills columns 96..127) and the products use K = 96 / N = 96.
+//
 // Pipelining.  The element-wise warps read a tile of S into registers and
 // compute P from it while the tensor core runs other products; they read dP
 // when it lands, and P^T / dS^T (dK/dV kernel) or dS (dQ kernel) go back to
 // TMEM as bf16 pairs over columns the same warp has already read, where the
 // next products take them as the TMEM operand.
 #include <cuda_runtime.h>
+
+#include <type_traits>
 
 #include "sm103_primitives.cuh"
 
@@ -58,11 +70,36 @@ struct BwdRegs {
 
 // ---------------------------------------------------------------- dK / dV
 
+// Columns of a D-wide gradient row handled by the element-wise warps with
+// hc = 0 (the warps with hc = 1 take the rest): halves of D, or the first 64
+// of 96 so that both parts are whole 32-byte units in power-of-two groups.
+template <int D>
+struct RowSplit {
+  static constexpr int kLo = (D == 96) ? 64 : D / 2;
+  static constexpr int kHi = D - kLo;
+};
+
+// Rows of 32 consecutive TMEM columns, NC columns from `taddr`, scaled and
+// packed to bf16 pairs into w[NC / 2].
+template <int NC>
+__device__ __forceinline__ void tmem_read_pack(uint32_t taddr, float sc, uint32_t* w) {
+#pragma unroll
+  for (int c = 0; c < NC / 32; ++c) {
+    uint32_t a[32];
+    tmem_ld32(taddr + 32 * c, a);
+    tmem_ld_wait<32>(a);
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      w[16 * c + i] = pack_bf16(__uint_as_float(a[2 * i]) * sc, __uint_as_float(a[2 * i + 1]) * sc);
+  }
+}
+
 template <int D>
 struct DkdvCfg {
-  static constexpr int kChunks = D / 64;
+  static_assert(D == 64 || D == 96 || D == 128, "head dim");
+  static constexpr int kChunks = (D + 63) / 64;
   static constexpr int kChunkBytes = kTileM * 128;
-  static constexpr int kTileBytes = kTileM * D * 2;
+  static constexpr int kTileBytes = kChunks * kChunkBytes;
   static constexpr int kQStages = 3;  // the next step's S^T needs Q early
   static constexpr int kDoStages = 2;
   static constexpr int kThreads = 384;
@@ -70,7 +107,7 @@ struct DkdvCfg {
   // P^T | dS^T packed.
   __host__ __device__ static constexpr uint32_t col_r(uint32_t r) { return 128u * r; }
   static constexpr uint32_t kColDV = 256;
-  static constexpr uint32_t kColDK = 256 + D;
+  static constexpr uint32_t kColDK = 256 + 64 * kChunks;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kTileBytes;
@@ -111,27 +148,37 @@ __device__ __forceinline__ BwdUnit decode_dkdv(const BwdParams& p, int u) {
   const int BH = p.B * p.Hkv;
   w.bh = u % BH;
   w.t = u / BH;
-  w.first = p.causal ? w.t : 0;
-  w.per = p.num_tiles - w.first;
+  // With the causal mask the first query row that sees key 128 t is
+  // 128 t - causal_off; units cover only key tiles some row sees.
+  const int first_row = w.t * kTileN - p.causal_off;
+  w.first = (p.causal && first_row > 0) ? first_row / kTileM : 0;
+  w.per = p.num_q_tiles - w.first;
   w.count = w.per * p.group;
   return w;
 }
 
 // dQ units: with the causal mask, high query tiles see the most key tiles.
+// Units cover only query tiles [q_tile_first, num_q_tiles), which see keys.
 __device__ __forceinline__ BwdUnit decode_dq(const BwdParams& p, int u) {
   BwdUnit w;
   const int BH = p.B * p.H;
   w.bh = u % BH;
-  w.t = p.causal ? p.num_tiles - 1 - u / BH : u / BH;
+  w.t = p.causal ? p.num_q_tiles - 1 - u / BH : p.q_tile_first + u / BH;
   w.first = 0;
-  w.count = p.causal ? w.t + 1 : p.num_tiles;
+  if (p.causal) {
+    const int last_key = min(p.Nq, (w.t + 1) * kTileM) - 1 + p.causal_off;  // >= 0 for these tiles
+    w.count = min(p.num_k_tiles, last_key / kTileN + 1);
+  } else {
+    w.count = p.num_k_tiles;
+  }
   w.per = w.count;
   return w;
 }
 
 // P^T of 64 query columns [q_first, q_first + 64) of key row kr, in place:
 // p = exp2(s * sl2 - L_q) with L per column.  MASK zeroes the weights the
-// causal mask hides (key > query) and those of a key row past N.
+// causal mask hides (kr > query; the caller passes the key row less the
+// causal offset) and those of a key row past Nk (dead).
 template <bool MASK>
 __device__ __forceinline__ void p64_colL(uint32_t* s, const float* bl, float sl2, int kr, int q_first, bool dead,
                                          bool causal) {
@@ -159,7 +206,8 @@ __device__ __forceinline__ void p64_colL(uint32_t* s, const float* bl, float sl2
 
 // P of 64 key columns [k_first, k_first + 64) of query row q, in place:
 // p = exp2(s * sl2 - L) with one L for the row.  MASK zeroes keys past N and,
-// with the causal mask, keys after the query.
+// with the causal mask, keys after q (the caller passes the query row plus
+// the causal offset).
 template <bool MASK>
 __device__ __forceinline__ void p64_rowL(uint32_t* s, float L, float sl2, int q, int k_first, int N, bool causal) {
   const float2 sv = make_float2(sl2, sl2);
@@ -290,10 +338,10 @@ __global__ void __launch_bounds__(384, 1)
           qt = w.first + ii;
         }
         const int row = qt * kTileM;
-        const size_t head = (size_t)qh * p.N;
-        // Q_i with L_i (log2 units; rows past N get +inf so their weights
-        // vanish).  The values are written before the arrive that completes
-        // the stage together with the copy.
+        const size_t head = (size_t)qh * p.Nq;
+        // Q_i with L_i (log2 units; rows past Nq and rows that see no key
+        // get +inf so their weights vanish).  The values are written before
+        // the arrive that completes the stage together with the copy.
         const uint32_t sq = qc % C::kQStages;
         ok = __all_sync(0xffffffffu, mbar_wait(&q_empty[sq], ((qc / C::kQStages) & 1) ^ 1, ctl, kWaitBwdLoad));
         if (!ok) break;
@@ -303,7 +351,8 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int qr = row + 4 * lane + e;
-            lp[e] = qr < p.N ? p.lse[head + qr] * 1.4426950408889634f : INFINITY;
+            const float L = qr < p.Nq ? p.lse[head + qr] : INFINITY;
+            lp[e] = L == -INFINITY ? INFINITY : L * 1.4426950408889634f;
           }
           reinterpret_cast<float4*>(sLse + sq * 128)[lane] = l4;
         }
@@ -324,7 +373,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int qr = row + 4 * lane + e;
-            dp[e] = qr < p.N ? p.dvec[head + qr] : 0.f;
+            dp[e] = qr < p.Nq ? p.dvec[head + qr] : 0.f;
           }
           reinterpret_cast<float4*>(sDv + sd * 128)[lane] = d4;
         }
@@ -529,37 +578,33 @@ __global__ void __launch_bounds__(384, 1)
     uint32_t uc = 0, qc = 0;
     bool ok = true;
     // dK_j = scale * sum dS^T Q and dV_j = sum P^T dO of unit (kr, head);
-    // this warp writes head-dim columns [D/2 hc, D/2 hc + D/2).  Run after
-    // the next unit's first P^T, while its dP^T is computed.
-    auto write_dkdv = [&](int kr, size_t head) -> bool {
-      if (!__all_sync(0xffffffffu, mbar_wait(dkv_full, uc & 1, ctl, kWaitBwdSoftmax))) return false;
-      ++uc;
-      tc_fence_after();
-      // This warp's half row (D/2 columns) of dV and of dK, packed to bf16
-      // and released from TMEM before any store is issued, so that the next
-      // unit's accumulation does not wait behind the stores.
-      uint32_t w[2][D / 4];
-#pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const uint32_t col = (which ? C::kColDK : C::kColDV) + (D / 2) * hc;
-        const float sc = which ? p.scale : 1.f;
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          uint32_t a[32];
-          tmem_ld32(tmem + lane_off + col + 32 * c, a);
-          tmem_ld_wait<32>(a);
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            w[which][16 * c + i] = pack_bf16(__uint_as_float(a[2 * i]) * sc, __uint_as_float(a[2 * i + 1]) * sc);
-        }
-      }
+    // this warp writes head-dim columns [c0, c0 + NC) (RowSplit).  Run after
+    // the next unit's first P^T, while its dP^T is computed.  The warp's
+    // part of the row of dV and of dK is packed to bf16 and released from
+    // TMEM before any store is issued, so that the next unit's accumulation
+    // does not wait behind the stores.
+    auto write_part = [&](auto nc_tag, int kr, size_t head) {
+      constexpr int NC = decltype(nc_tag)::value;
+      const int c0 = hc ? RowSplit<D>::kLo : 0;
+      uint32_t w[2][NC / 2];
+      tmem_read_pack<NC>(tmem + lane_off + C::kColDV + c0, 1.f, w[0]);
+      tmem_read_pack<NC>(tmem + lane_off + C::kColDK + c0, p.scale, w[1]);
       tc_fence_before();
       mbar_arrive_warp(dkv_empty);
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
-        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(which ? p.dk : p.dv) + (head + kr) * D + (D / 2) * hc;
-        store_rows<D / 32>(reinterpret_cast<uint8_t*>(dst), (size_t)D * 2, kr, p.N, w[which], p.store32 != 0);
+        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(which ? p.dk : p.dv) + (head + kr) * D + c0;
+        store_rows<NC / 16>(reinterpret_cast<uint8_t*>(dst), (size_t)D * 2, kr, p.Nk, w[which], p.store32 != 0);
       }
+    };
+    auto write_dkdv = [&](int kr, size_t head) -> bool {
+      if (!__all_sync(0xffffffffu, mbar_wait(dkv_full, uc & 1, ctl, kWaitBwdSoftmax))) return false;
+      ++uc;
+      tc_fence_after();
+      if (hc == 0)
+        write_part(std::integral_constant<int, RowSplit<D>::kLo>{}, kr, head);
+      else
+        write_part(std::integral_constant<int, RowSplit<D>::kHi>{}, kr, head);
       return true;
     };
     int pend_kr = -1;  // the unit whose dK / dV are still in TMEM
@@ -569,7 +614,7 @@ __global__ void __launch_bounds__(384, 1)
       if (u >= p.num_units_kv) continue;
       const BwdUnit w = decode_dkdv(p, u);
       const int kr = w.t * kTileN + r_key;  // key index
-      const size_t head = (size_t)w.bh * p.N;
+      const size_t head = (size_t)w.bh * p.Nk;
       int qt = w.first;
       for (int ii = 0; ok && ii < w.count; ++ii, ++qc) {
         if constexpr (GQA) {
@@ -597,8 +642,8 @@ __global__ void __launch_bounds__(384, 1)
         {
           const float* bl = sLse + sq * 128 + 64 * hc;
           const int qf = q0 + 64 * hc;
-          if ((kr >= p.N) || (p.causal && kr > qf))
-            p64_colL<true>(pv, bl, sl2, kr, qf, kr >= p.N, p.causal != 0);
+          if ((kr >= p.Nk) || (p.causal && kr > qf + p.causal_off))
+            p64_colL<true>(pv, bl, sl2, kr - p.causal_off, qf, kr >= p.Nk, p.causal != 0);
           else
             p64_colL<false>(pv, bl, sl2, kr, qf, false, false);
         }
@@ -665,9 +710,10 @@ __global__ void __launch_bounds__(384, 1)
 
 template <int D>
 struct DqCfg {
-  static constexpr int kChunks = D / 64;
+  static_assert(D == 64 || D == 96 || D == 128, "head dim");
+  static constexpr int kChunks = (D + 63) / 64;
   static constexpr int kChunkBytes = kTileM * 128;
-  static constexpr int kTileBytes = kTileM * D * 2;
+  static constexpr int kTileBytes = kChunks * kChunkBytes;
   static constexpr int kKStages = 3;  // S two steps ahead needs K early
   static constexpr int kVStages = 2;
   static constexpr int kThreads = 384;
@@ -936,37 +982,45 @@ __global__ void __launch_bounds__(384, 1)
     // dQ_i = scale * sum dS K of a unit: lane = query row q of head `head`,
     // this warp writes head-dim columns [D/2 hc, D/2 hc + D/2).  Run after
     // the next unit's first P, while its dP is computed.
+    // This warp's columns [c0, c0 + NC) of the row (RowSplit), read out of
+    // TMEM, released, then scaled, packed and stored.  One row per lane
+    // here: the dQ stores follow the TMEM release and overlap the next
+    // unit's first steps, and the shuffles of store_rows measured slower
+    // than the scattered lines they save.
+    auto write_part = [&](auto nc_tag, int q, size_t head) {
+      constexpr int NC = decltype(nc_tag)::value;
+      const int c0 = hc ? RowSplit<D>::kLo : 0;
+      uint32_t v[NC];
+#pragma unroll
+      for (int c = 0; c < NC / 32; ++c) tmem_ld32(tmem + lane_off + C::kColDQ + c0 + 32 * c, v + 32 * c);
+      tmem_ld_wait<NC>(v);
+      tc_fence_before();
+      mbar_arrive_warp(dq_empty);
+      __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.dq) + (head + q) * D + c0;
+      const float sc = p.scale;
+      uint32_t w[NC / 2];
+#pragma unroll
+      for (int i = 0; i < NC / 2; ++i)
+        w[i] = pack_bf16(__uint_as_float(v[2 * i]) * sc, __uint_as_float(v[2 * i + 1]) * sc);
+      if (q < p.Nq) {
+        if (p.store32) {
+#pragma unroll
+          for (int i = 0; i < NC / 16; ++i) st_global_v8(dst + 16 * i, w + 8 * i);
+        } else {
+#pragma unroll
+          for (int i = 0; i < NC / 8; ++i)
+            reinterpret_cast<uint4*>(dst)[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        }
+      }
+    };
     auto write_dq = [&](int q, size_t head) -> bool {
       if (!__all_sync(0xffffffffu, mbar_wait(dq_full, uc & 1, ctl, kWaitBwdDq))) return false;
       ++uc;
       tc_fence_after();
-      uint32_t v[D / 2];
-      tmem_ld32(tmem + lane_off + C::kColDQ + (D / 2) * hc, v);
-      if constexpr (D == 128) tmem_ld32(tmem + lane_off + C::kColDQ + (D / 2) * hc + 32, v + 32);
-      tmem_ld_wait<D / 2>(v);
-      tc_fence_before();
-      mbar_arrive_warp(dq_empty);
-      {
-        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.dq) + (head + q) * D + (D / 2) * hc;
-        const float sc = p.scale;
-        uint32_t w[D / 4];
-#pragma unroll
-        for (int i = 0; i < D / 4; ++i)
-          w[i] = pack_bf16(__uint_as_float(v[2 * i]) * sc, __uint_as_float(v[2 * i + 1]) * sc);
-        // One row per lane here: the dQ stores follow the TMEM release and
-        // overlap the next unit's first steps, and the shuffles of
-        // store_rows measured slower than the scattered lines they save.
-        if (q < p.N) {
-          if (p.store32) {
-#pragma unroll
-            for (int i = 0; i < D / 32; ++i) st_global_v8(dst + 16 * i, w + 8 * i);
-          } else {
-#pragma unroll
-            for (int i = 0; i < D / 16; ++i)
-              reinterpret_cast<uint4*>(dst)[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-          }
-        }
-      }
+      if (hc == 0)
+        write_part(std::integral_constant<int, RowSplit<D>::kLo>{}, q, head);
+      else
+        write_part(std::integral_constant<int, RowSplit<D>::kHi>{}, q, head);
       return true;
     };
     int pend_q = -1;  // the unit whose dQ is still in TMEM
@@ -975,10 +1029,11 @@ __global__ void __launch_bounds__(384, 1)
       const int u = snake_unit(rnd);
       if (u >= p.num_units) continue;
       const BwdUnit w = decode_dq(p, u);
-      const size_t head = (size_t)w.bh * p.N;
+      const size_t head = (size_t)w.bh * p.Nq;
       const int q = w.t * kTileM + 32 * g + lane;  // query row
-      const float L = q < p.N ? p.lse[head + q] * 1.4426950408889634f : INFINITY;
-      const float Dq = q < p.N ? p.dvec[head + q] : 0.f;
+      const float Lraw = q < p.Nq ? p.lse[head + q] : INFINITY;
+      const float L = Lraw == -INFINITY ? INFINITY : Lraw * 1.4426950408889634f;  // no key seen: weights 0
+      const float Dq = q < p.Nq ? p.dvec[head + q] : 0.f;
       const int q_lo = w.t * kTileM + 32 * g;  // first query of this warp
       for (int jj = 0; ok && jj < w.count; ++jj, ++kc) {
         const uint32_t tS = tmem + lane_off + ((kc & 1) ? C::kColS1 : C::kColS0) + 64 * hc;
@@ -990,10 +1045,10 @@ __global__ void __launch_bounds__(384, 1)
         tmem_ld32(tS, pv);
         tmem_ld32(tS + 32, pv + 32);
         tmem_ld_wait<64>(pv);
-        if (k_first + 63 >= p.N || (p.causal && k_first + 63 > q_lo))
-          p64_rowL<true>(pv, L, sl2, q, k_first, p.N, p.causal != 0);
+        if (k_first + 63 >= p.Nk || (p.causal && k_first + 63 > q_lo + p.causal_off))
+          p64_rowL<true>(pv, L, sl2, q + p.causal_off, k_first, p.Nk, p.causal != 0);
         else
-          p64_rowL<false>(pv, L, sl2, q, k_first, p.N, false);
+          p64_rowL<false>(pv, L, sl2, q, k_first, p.Nk, false);
         if (jj == 0 && pend_q >= 0) {
           ok = write_dq(pend_q, pend_head);
           if (!ok) break;
@@ -1051,35 +1106,42 @@ template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_preprocess(const __nv_bfloat16* __restrict__ o,
                                                          const __nv_bfloat16* __restrict__ dout,
                                                          float* __restrict__ dvec, int rows) {
-  constexpr int kLanes = D / 8;               // lanes per row
+  constexpr int kVec = (D == 96) ? 3 : 1;     // 16-byte pieces per lane (lanes per row a power of two)
+  constexpr int kLanes = D / (8 * kVec);      // lanes per row
   constexpr int kSlots = 256 / kLanes;        // rows per pass
   constexpr int kRowsPerThread = 4;           // passes
   const int part = threadIdx.x % kLanes;
   const int slot = threadIdx.x / kLanes;
   const int base = blockIdx.x * kSlots * kRowsPerThread;
-  uint4 a[kRowsPerThread], b[kRowsPerThread];
+  uint4 a[kRowsPerThread][kVec], b[kRowsPerThread][kVec];
 #pragma unroll
   for (int r = 0; r < kRowsPerThread; ++r) {
     const int row = base + r * kSlots + slot;
-    if (row < rows) {
-      a[r] = reinterpret_cast<const uint4*>(o + (size_t)row * D)[part];
-      b[r] = reinterpret_cast<const uint4*>(dout + (size_t)row * D)[part];
-    } else {
-      a[r] = make_uint4(0u, 0u, 0u, 0u);
-      b[r] = a[r];
+#pragma unroll
+    for (int v = 0; v < kVec; ++v) {
+      if (row < rows) {
+        a[r][v] = reinterpret_cast<const uint4*>(o + (size_t)row * D)[part * kVec + v];
+        b[r][v] = reinterpret_cast<const uint4*>(dout + (size_t)row * D)[part * kVec + v];
+      } else {
+        a[r][v] = make_uint4(0u, 0u, 0u, 0u);
+        b[r][v] = a[r][v];
+      }
     }
   }
 #pragma unroll
   for (int r = 0; r < kRowsPerThread; ++r) {
-    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a[r]);
-    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b[r]);
     float acc = 0.f;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 x = __bfloat1622float2(a2[i]);
-      const float2 y = __bfloat1622float2(b2[i]);
-      acc = fmaf(x.x, y.x, acc);
-      acc = fmaf(x.y, y.y, acc);
+    for (int v = 0; v < kVec; ++v) {
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a[r][v]);
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b[r][v]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 x = __bfloat1622float2(a2[i]);
+        const float2 y = __bfloat1622float2(b2[i]);
+        acc = fmaf(x.x, y.x, acc);
+        acc = fmaf(x.y, y.y, acc);
+      }
     }
 #pragma unroll
     for (int off = kLanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
@@ -1126,30 +1188,49 @@ static cudaError_t launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, con
 
 cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const BwdParams& p, int grid, cudaStream_t stream) {
-  if (p.Hkv != p.H)
-    return d == 64 ? launch_dkdv_t<64, true>(tq, tk, tv, tdo, p, grid, stream)
-                   : launch_dkdv_t<128, true>(tq, tk, tv, tdo, p, grid, stream);
-  return d == 64 ? launch_dkdv_t<64, false>(tq, tk, tv, tdo, p, grid, stream)
+  const bool gqa = p.Hkv != p.H;
+  switch (d) {
+    case 64:
+      return gqa ? launch_dkdv_t<64, true>(tq, tk, tv, tdo, p, grid, stream)
+                 : launch_dkdv_t<64, false>(tq, tk, tv, tdo, p, grid, stream);
+    case 96:
+      return gqa ? launch_dkdv_t<96, true>(tq, tk, tv, tdo, p, grid, stream)
+                 : launch_dkdv_t<96, false>(tq, tk, tv, tdo, p, grid, stream);
+    case 128:
+      return gqa ? launch_dkdv_t<128, true>(tq, tk, tv, tdo, p, grid, stream)
                  : launch_dkdv_t<128, false>(tq, tk, tv, tdo, p, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_bwd_dq(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tdo, const BwdParams& p, int grid, cudaStream_t stream) {
-  return d == 64 ? launch_dq_t<64>(tq, tk, tv, tdo, p, grid, stream)
-                 : launch_dq_t<128>(tq, tk, tv, tdo, p, grid, stream);
+  switch (d) {
+    case 64: return launch_dq_t<64>(tq, tk, tv, tdo, p, grid, stream);
+    case 96: return launch_dq_t<96>(tq, tk, tv, tdo, p, grid, stream);
+    case 128: return launch_dq_t<128>(tq, tk, tv, tdo, p, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <int D>
+static cudaError_t launch_pre_t(const void* o, const void* dout, float* dvec, int rows, cudaStream_t stream) {
+  constexpr int kVec = (D == 96) ? 3 : 1;
+  const int per_block = (256 / (D / (8 * kVec))) * 4;  // rows per 256-thread block (4 passes)
+  const int grid = (rows + per_block - 1) / per_block;
+  fa_bwd_preprocess<D><<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(o),
+                                                  static_cast<const __nv_bfloat16*>(dout), dvec, rows);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_preprocess(int d, const void* o, const void* dout, float* dvec, int rows,
                                   cudaStream_t stream) {
-  const int per_block = (256 / (d / 8)) * 4;  // rows per 256-thread block (4 passes)
-  const int grid = (rows + per_block - 1) / per_block;
-  const auto* po = static_cast<const __nv_bfloat16*>(o);
-  const auto* pd = static_cast<const __nv_bfloat16*>(dout);
-  if (d == 64)
-    fa_bwd_preprocess<64><<<grid, 256, 0, stream>>>(po, pd, dvec, rows);
-  else
-    fa_bwd_preprocess<128><<<grid, 256, 0, stream>>>(po, pd, dvec, rows);
-  return cudaGetLastError();
+  switch (d) {
+    case 64: return launch_pre_t<64>(o, dout, dvec, rows, stream);
+    case 96: return launch_pre_t<96>(o, dout, dvec, rows, stream);
+    case 128: return launch_pre_t<128>(o, dout, dvec, rows, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_selftest_wait(unsigned int* status, unsigned long long timeout_ns, cudaStream_t stream) {

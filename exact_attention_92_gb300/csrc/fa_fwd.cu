@@ -33,7 +33,13 @@
 //
 // Causal mask (section 5): key tiles past a query tile's last row are never
 // loaded or multiplied; only tiles crossing the diagonal (and the ragged last
-// key tile) are masked element by element.
+// key tile) are masked element by element.  Queries and keys may differ in
+// length; row i then sees keys j <= i + causal_off (0: top-left alignment,
+// Nk - Nq: bottom-right).  A row that sees no key writes O = 0, L = -inf.
+//
+// Head dims 64, 96 and 128.  A 96-wide row is staged in the 128-wide layout
+// (two 64-column blocks; TMA fills columns 96..127 with zeros) while the
+// products use K = 96 (S) and N = 96 (O) exactly.
 #include <cuda_runtime.h>
 
 #include "sm103_primitives.cuh"
@@ -44,15 +50,17 @@ using namespace dev;
 
 template <int D>
 struct FwdCfg {
-  static constexpr int kChunks = D / 64;               // 128-byte column blocks per row
+  static_assert(D == 64 || D == 96 || D == 128, "head dim");
+  static constexpr int kChunks = (D + 63) / 64;        // 128-byte column blocks per row
   static constexpr int kChunkBytes = kTileM * 128;     // one 128-row x 64-column block
-  static constexpr int kTileBytes = kTileM * D * 2;    // one 128 x D bf16 tile
-  static constexpr int kStages = (D == 128) ? 4 : 8;   // K/V ring slots
+  static constexpr int kTileBytes = kChunks * kChunkBytes;  // one 128-row tile (padded to 64 columns)
+  static constexpr int kStages = (D == 64) ? 8 : 4;    // K/V ring slots
+  static constexpr int kOCols = kChunks * 64;          // TMEM columns given to one O tile
   // Three warpgroups: 0-1 softmax (one 128-row Q tile each), 2 the MMA
   // issuer (warp 8), the TMA producer (warp 9) and two idle warps.
   static constexpr int kThreads = 384;
   __host__ __device__ static constexpr uint32_t col_s(int t) { return 128u * t; }
-  __host__ __device__ static constexpr uint32_t col_o(int t) { return 256u + (uint32_t)D * t; }
+  __host__ __device__ static constexpr uint32_t col_o(int t) { return 256u + (uint32_t)kOCols * t; }
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = 2 * kTileBytes;
@@ -90,7 +98,7 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
   // carry the most key tiles, so they start first (longest job first).
   const int qb = p.num_q_blocks - 1 - r / BH;
   w.q0 = qb * (kTileM * kQTilesPerCta);
-  const int nkv = (p.N + kTileN - 1) / kTileN;
+  const int nkv = (p.Nk + kTileN - 1) / kTileN;
   const int lo = split * p.kv_tiles_per_split;
   const int hi = min(nkv, lo + p.kv_tiles_per_split);
   w.kvb = lo;
@@ -98,11 +106,15 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     const int row0 = w.q0 + kTileM * t;
-    if (row0 >= p.N) {
+    if (row0 >= p.Nq) {
       w.n[t] = 0;
     } else {
-      const int last = min(p.N, row0 + kTileM) - 1;
-      const int h = p.causal ? min(hi, last / kTileN + 1) : hi;
+      int h = hi;
+      if (p.causal) {
+        // The last key any row of the tile sees; none if it is negative.
+        const int last_key = min(p.Nq, row0 + kTileM) - 1 + p.causal_off;
+        h = last_key < 0 ? 0 : min(hi, last_key / kTileN + 1);
+      }
       w.n[t] = max(0, h - lo);
     }
   }
@@ -336,12 +348,19 @@ __global__ void __launch_bounds__(384, 1)
       const int row = row0 + r_in_tile;
       const int split = w.split;
       if (w.n[t] == 0) {
-        // No visible key in this split: an empty partial (O = 0, L = -inf).
-        if (p.num_splits > 1 && row < p.N) {
-          const size_t prow = ((size_t)split * p.B * p.H + w.bh) * p.N + row;
-          float4* dst = reinterpret_cast<float4*>(p.o_part + prow * D);
-          for (int c = 0; c < D / 4; ++c) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-          p.lse_part[prow] = -INFINITY;
+        // No row of the tile sees a key (of this split): O = 0, L = -inf
+        // (an empty partial when the keys are split).
+        if (row < p.Nq) {
+          if (p.num_splits > 1) {
+            const size_t prow = ((size_t)split * p.B * p.H + w.bh) * p.Nq + row;
+            float4* dst = reinterpret_cast<float4*>(p.o_part + prow * D);
+            for (int c = 0; c < D / 4; ++c) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+            p.lse_part[prow] = -INFINITY;
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.o) + ((size_t)w.bh * p.Nq + row) * (D * 2));
+            for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+            p.lse[(size_t)w.bh * p.Nq + row] = -INFINITY;
+          }
         }
         continue;
       }
@@ -361,9 +380,9 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
         for (int c = 0; c < kTileN; ++c) x[c] = __uint_as_float(s[c]);
         const int kv0 = (w.kvb + j) * kTileN;
-        const bool need_mask = (kv0 + kTileN > p.N) || (p.causal && kv0 + kTileN - 1 > row0);
+        const bool need_mask = (kv0 + kTileN > p.Nk) || (p.causal && kv0 + kTileN - 1 > row0 + p.causal_off);
         if (need_mask) {
-          const int lim = p.causal ? min(p.N - 1, row) : p.N - 1;  // last visible key
+          const int lim = p.causal ? min(p.Nk - 1, row + p.causal_off) : p.Nk - 1;  // last visible key
 #pragma unroll
           for (int c = 0; c < kTileN; ++c)
             if (kv0 + c > lim) x[c] = -INFINITY;
@@ -377,24 +396,27 @@ __global__ void __launch_bounds__(384, 1)
           mx3 = fmax3(mx3, x[c + 6], x[c + 7]);
         }
         const float m_tile = fmax3(fmaxf(mx0, mx1), mx2, mx3) * sl2;
+        // m_ref stays -inf while the row has seen no key; the first key it
+        // sees then takes the rescale path with f = 0 (l and O~ are 0).
         float f = 1.f;
         bool rescale = false;
         if (j == 0) {
-          m_ref = (m_tile == -INFINITY) ? 0.f : m_tile;
+          m_ref = m_tile;
         } else if (__any_sync(0xffffffffu, m_tile > m_ref + C::kRescaleThreshold)) {
           const float m_new = fmaxf(m_ref, m_tile);
-          f = ex2_approx(m_ref - m_new);
+          f = (m_new == -INFINITY) ? 1.f : ex2_approx(m_ref - m_new);
           l *= f;
           l_bf *= f;
           m_ref = m_new;
           rescale = true;
         }
+        const float m_exp = (m_ref == -INFINITY) ? 0.f : m_ref;  // exponent reference (all weights 0 if -inf)
         // P = exp2(S * scale * log2(e) - m_ref), 32 columns at a time, packed
         // to bf16 over the already-read S columns; pairs of columns share the
         // packed fp32x2 FMA and adds.  The rounded weights are summed from
         // the packed pairs (each half converted exactly to fp32).
         const float2 sl2v = make_float2(sl2, sl2);
-        const float2 negv = make_float2(-m_ref, -m_ref);
+        const float2 negv = make_float2(-m_exp, -m_exp);
         float2 ls0 = make_float2(0.f, 0.f), ls1 = ls0;
         float lr0 = 0.f, lr1 = 0.f, lr2 = 0.f, lr3 = 0.f;
 #pragma unroll
@@ -449,13 +471,14 @@ __global__ void __launch_bounds__(384, 1)
       ++oc;
       if (!ok) break;
       tc_fence_after();
-      const float inv_l = 1.0f / l_bf;
-      const float lse = (m_ref + lg2_approx(l)) * 0.69314718055994530942f;
+      // A row that saw no key has l = 0: O = 0, L = -inf.
+      const float inv_l = l_bf > 0.f ? 1.0f / l_bf : 0.f;
+      const float lse = l > 0.f ? (m_ref + lg2_approx(l)) * 0.69314718055994530942f : -INFINITY;
       if (p.num_splits == 1) {
         // O = O~ / l in bf16, 64 columns (128 bytes of the row) at a time,
         // stored with whole row segments per warp store; rows past N are
         // skipped.
-        uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) + ((size_t)w.bh * p.N + row) * (D * 2);
+        uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) + ((size_t)w.bh * p.Nq + row) * (D * 2);
         const float2 il = make_float2(inv_l, inv_l);
 #pragma unroll 1
         for (int hb = 0; hb < D / 64; ++hb) {
@@ -471,18 +494,30 @@ __global__ void __launch_bounds__(384, 1)
               ob[16 * c + i] = pack_bf16(a.x, a.y);
             }
           }
-          store_rows<4>(orow + 128 * hb, (size_t)D * 2, row, p.N, ob, p.store32 != 0);
+          store_rows<4>(orow + 128 * hb, (size_t)D * 2, row, p.Nq, ob, p.store32 != 0);
         }
-        if (row < p.N) p.lse[(size_t)w.bh * p.N + row] = lse;
+        if constexpr (D % 64 == 32) {
+          // The last 32 columns (64 bytes of the row).
+          uint32_t o[32], ob[16];
+          tmem_ld32(tO + 64 * (D / 64), o);
+          tmem_ld_wait<32>(o);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float2 a = __fmul2_rn(make_float2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), il);
+            ob[i] = pack_bf16(a.x, a.y);
+          }
+          store_rows<2>(orow + 128 * (D / 64), (size_t)D * 2, row, p.Nq, ob, p.store32 != 0);
+        }
+        if (row < p.Nq) p.lse[(size_t)w.bh * p.Nq + row] = lse;
       } else {
-        const size_t prow = ((size_t)split * p.B * p.H + w.bh) * p.N + row;
+        const size_t prow = ((size_t)split * p.B * p.H + w.bh) * p.Nq + row;
         float4* dst = reinterpret_cast<float4*>(p.o_part + prow * D);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
           tmem_ld32(tO + 32 * c, o);
           tmem_ld_wait<32>(o);
-          if (row < p.N) {
+          if (row < p.Nq) {
 #pragma unroll
             for (int i = 0; i < 8; ++i)
               dst[c * 8 + i] = make_float4(__uint_as_float(o[4 * i]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
@@ -490,7 +525,7 @@ __global__ void __launch_bounds__(384, 1)
                                            __uint_as_float(o[4 * i + 3]) * inv_l);
           }
         }
-        if (row < p.N) p.lse_part[prow] = lse;
+        if (row < p.Nq) p.lse_part[prow] = lse;
       }
     }
     __syncwarp();
@@ -528,17 +563,21 @@ __global__ void __launch_bounds__(256) fa_combine_kernel(const CombineParams p) 
 #pragma unroll
     for (int i = 0; i < kPer; ++i) acc[i] = fmaf(wgt, src[i], acc[i]);
   }
-  const float inv = 1.0f / tot;
+  // A row that sees no key in any split: O = 0, L = -inf.
+  const float inv = tot > 0.f ? 1.0f / tot : 0.f;
   __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.o) + (size_t)row * D + lane * kPer;
   if constexpr (kPer == 2) {
     *reinterpret_cast<uint32_t*>(o) = pack_bf16(acc[0] * inv, acc[1] * inv);
-  } else {
+  } else if constexpr (kPer == 4) {
     uint2 v;
     v.x = pack_bf16(acc[0] * inv, acc[1] * inv);
     v.y = pack_bf16(acc[2] * inv, acc[3] * inv);
     *reinterpret_cast<uint2*>(o) = v;
+  } else {
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) o[i] = __float2bfloat16_rn(acc[i] * inv);
   }
-  if (lane == 0) p.lse[row] = mx + logf(tot);
+  if (lane == 0) p.lse[row] = tot > 0.f ? mx + logf(tot) : -INFINITY;
 }
 
 // ------------------------------------------------------------------ launch
@@ -555,15 +594,22 @@ static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
 
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdParams& p, int grid, cudaStream_t stream) {
-  return d == 64 ? launch_fwd_t<64>(tq, tk, tv, p, grid, stream) : launch_fwd_t<128>(tq, tk, tv, p, grid, stream);
+  switch (d) {
+    case 64: return launch_fwd_t<64>(tq, tk, tv, p, grid, stream);
+    case 96: return launch_fwd_t<96>(tq, tk, tv, p, grid, stream);
+    case 128: return launch_fwd_t<128>(tq, tk, tv, p, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_combine(int d, const CombineParams& p, cudaStream_t stream) {
   const int grid = (p.rows + 7) / 8;
-  if (d == 64)
-    fa_combine_kernel<64><<<grid, 256, 0, stream>>>(p);
-  else
-    fa_combine_kernel<128><<<grid, 256, 0, stream>>>(p);
+  switch (d) {
+    case 64: fa_combine_kernel<64><<<grid, 256, 0, stream>>>(p); break;
+    case 96: fa_combine_kernel<96><<<grid, 256, 0, stream>>>(p); break;
+    case 128: fa_combine_kernel<128><<<grid, 256, 0, stream>>>(p); break;
+    default: return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 

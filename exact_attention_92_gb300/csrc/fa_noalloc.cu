@@ -126,8 +126,10 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
   p.B = B;
   p.H = H;
   p.Hkv = H;
-  p.N = N;
+  p.Nq = N;
+  p.Nk = N;
   p.causal = causal ? 1 : 0;
+  p.causal_off = 0;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.lse = lse;
@@ -137,8 +139,11 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
   p.dv = dv;
   p.store32 = ((reinterpret_cast<uintptr_t>(dq) | reinterpret_cast<uintptr_t>(dk) |
                 reinterpret_cast<uintptr_t>(dv)) & 31u) == 0 ? 1 : 0;
-  p.num_tiles = (N + 127) / 128;
-  p.num_units = BH * p.num_tiles;
+  p.num_q_tiles = (N + 127) / 128;
+  p.num_k_tiles = p.num_q_tiles;
+  p.kv_tiles_used = p.num_k_tiles;
+  p.q_tile_first = 0;
+  p.num_units = BH * p.num_q_tiles;
   p.num_units_kv = p.num_units;
   p.group = 1;
   p.status = status;

@@ -15,8 +15,9 @@
  *    dO, dQ, dK, dV are bf16, shape [B, H, N, d], contiguous row-major (d is
  *    the fastest index).  LSE is fp32, shape [B, H, N], natural logarithm.
  *  - Pointers must be non-null and 16-byte aligned.
- *  - d must be 64 or 128.  B, H, N >= 1.  Queries and keys have the same
- *    length N; N need not be a multiple of the tile size.
+ *  - d must be 64, 96 or 128 (FA_ERR_UNSUPPORTED otherwise).  B, H, N >= 1.
+ *    N need not be a multiple of the tile size.  Queries and keys have the
+ *    same length N, except in fa_fwd_general / fa_bwd_general.
  *  - causal != 0 applies the mask of "FlashAttention V2 in depth" section 5.1:
  *    query row i sees key j iff j <= i (top-left aligned).
  *  - scale multiplies Q K^T before the softmax; pass 1/sqrt(d) for the usual
@@ -41,12 +42,12 @@
 extern "C" {
 #endif
 
-#define FA_ABI_VERSION 3
+#define FA_ABI_VERSION 4
 
 typedef enum {
   FA_OK = 0,
   FA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size or scale      */
-  FA_ERR_UNSUPPORTED = 2, /* head dim not 64/128, or device is not sm_103    */
+  FA_ERR_UNSUPPORTED = 2, /* head dim not 64/96/128, or not an sm_103 GPU   */
   FA_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed     */
   FA_ERR_NO_MEMORY = 4,   /* workspace allocation failed                     */
   FA_ERR_TIMEOUT = 5,     /* a device-side wait gave up (fa_poll_status)     */
@@ -92,6 +93,38 @@ int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
                int d, int causal, float scale, int num_splits, void* stream);
 
 /*
+ * Causal codes of fa_fwd_general / fa_bwd_general.  The pages define the
+ * mask for queries and keys of one length N (query row i sees keys j <= i);
+ * with Nq query rows and Nk key rows the alignment has to be chosen:
+ *   FA_CAUSAL_TOP_LEFT     row i sees keys j <= i
+ *   FA_CAUSAL_BOTTOM_RIGHT row i sees keys j <= i + Nk - Nq (the last query
+ *                          row sees every key: the newest Nq positions of a
+ *                          sequence of Nk, as when decoding)
+ * Both equal the pages' mask when Nq = Nk.  A query row that sees no key
+ * (bottom-right with Nq > Nk: rows i < Nq - Nk) gets O = 0, L = -inf, and
+ * zero gradients; keys no row sees get dK = dV = 0.
+ */
+#define FA_CAUSAL_NONE 0
+#define FA_CAUSAL_TOP_LEFT 1
+#define FA_CAUSAL_BOTTOM_RIGHT 2
+
+/*
+ * Forward pass with queries and keys of different lengths (and grouped-query
+ * attention).  The computation of fa_fwd ("FlashAttention V2 in depth",
+ * section 6.1) per query row over the keys it sees; short query blocks over
+ * long keys (decoding) are split along the keys as in fa_fwd_ex
+ * (FlashAttention-2 abstract, point (2)).
+ *   q, o    : bf16 [B,H,Nq,d];  k, v : bf16 [B,Hkv,Nk,d];  lse : fp32 [B,H,Nq]
+ *   Nq, Nk  : >= 1
+ *   Hkv     : >= 1 and divides H (FA_ERR_INVALID_ARG otherwise)
+ *   causal  : FA_CAUSAL_NONE, FA_CAUSAL_TOP_LEFT or FA_CAUSAL_BOTTOM_RIGHT
+ *             (FA_ERR_INVALID_ARG otherwise)
+ * Other arguments as fa_fwd_ex.  fa_fwd_gqa is this call with Nq = Nk.
+ */
+int fa_fwd_general(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv,
+                   int Nq, int Nk, int d, int causal, float scale, int num_splits, void* stream);
+
+/*
  * Backward pass.  "FlashAttention V2 in depth", section 7: P recomputed from
  * the saved logsumexp (section 7.1), D_i = rowsum(dO_i * O_i) from a separate
  * preprocess kernel (section 7.3), dK and dV with key/value tiles in the
@@ -124,6 +157,19 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
 int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
                void* dq, void* dk, void* dv, int B, int H, int Hkv, int N, int d, int causal, float scale,
                void* stream);
+
+/*
+ * Backward pass with queries and keys of different lengths (see
+ * fa_fwd_general for the causal codes), and grouped-query attention.
+ *   q, o, dout, dq : bf16 [B,H,Nq,d];  k, v, dk, dv : bf16 [B,Hkv,Nk,d]
+ *   lse            : fp32 [B,H,Nq] (from fa_fwd_general with the same causal code)
+ * Gradient rows of query tiles that see no key, and of key tiles that no
+ * query row sees, are zeroed with cudaMemset2DAsync on `stream`.  Workspace
+ * and other arguments as fa_bwd; fa_bwd_gqa is this call with Nq = Nk.
+ */
+int fa_bwd_general(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                   const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int Nq, int Nk, int d,
+                   int causal, float scale, void* stream);
 
 /*
  * Backward pass that allocates no device memory.  The paper has no

@@ -77,10 +77,18 @@ def check_o(o_gpu, o_ref, what="", row_weights=None):
 
 
 def check_lse(l_gpu, l_ref, what=""):
+    """A row that sees no key has L = -inf in the oracle; the GPU must give
+    exactly -inf there and finite values elsewhere."""
     l_gpu = np.asarray(l_gpu, dtype=np.float64)
+    l_ref = np.asarray(l_ref, dtype=np.float64)
+    assert not np.isnan(l_gpu).any(), f"{what}: NaN in LSE"
+    empty = np.isneginf(l_ref)
+    assert np.array_equal(np.isneginf(l_gpu), empty), (
+        f"{what}: LSE -inf at {np.argwhere(np.isneginf(l_gpu) != empty)[:5].tolist()} disagrees with the oracle")
+    l_gpu = np.where(empty, 0.0, l_gpu)
+    l_ref = np.where(empty, 0.0, l_ref)
     err = np.abs(l_gpu - l_ref)
     bound = LSE_REL * np.maximum(1.0, np.abs(l_ref))
-    assert not np.isnan(l_gpu).any(), f"{what}: NaN in LSE"
     bad = err > bound
     assert not bad.any(), (f"{what}: LSE error {err.max():.3e} at {np.argwhere(bad)[:5].tolist()} "
                            f"(ref {l_ref[bad][:5]}, gpu {l_gpu[bad][:5]})")

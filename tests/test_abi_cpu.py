@@ -37,7 +37,7 @@ def test_no_driver_dependency():
 
 
 def test_version_and_strerror(lib):
-    assert fa.fa_abi_version() == 3
+    assert fa.fa_abi_version() == 4
     for code in range(6):
         assert fa.fa_strerror(code).startswith("FA_")
     assert "unknown" in fa.fa_strerror(99)
@@ -62,8 +62,34 @@ def test_fwd_argument_errors(lib):
     assert _fwd(lib, scale=float("inf")) == fa.FA_ERR_INVALID_ARG
     assert _fwd(lib, scale=-1.0) == fa.FA_ERR_INVALID_ARG
     assert _fwd(lib, splits=-1) == fa.FA_ERR_INVALID_ARG
-    assert _fwd(lib, d=96) == fa.FA_ERR_UNSUPPORTED
+    assert _fwd(lib, d=32) == fa.FA_ERR_UNSUPPORTED
+    assert _fwd(lib, d=80) == fa.FA_ERR_UNSUPPORTED
     assert _fwd(lib, d=256) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_general_argument_errors(lib):
+    """fa_fwd_general / fa_bwd_general: lengths, causal codes and head counts
+    are checked on the host before anything touches a device."""
+    ptrs = [P(0x1000 * (i + 1)) for i in range(9)]
+
+    def fwd(B=1, H=4, Hkv=2, Nq=100, Nk=300, d=96, causal=2, scale=0.1, splits=0):
+        return lib.fa_fwd_general(*ptrs[:5], B, H, Hkv, Nq, Nk, d, causal, scale, splits, None)
+
+    def bwd(B=1, H=4, Hkv=2, Nq=100, Nk=300, d=96, causal=2, scale=0.1):
+        return lib.fa_bwd_general(*ptrs, B, H, Hkv, Nq, Nk, d, causal, scale, None)
+
+    for call in (fwd, bwd):
+        assert call(Nq=0) == fa.FA_ERR_INVALID_ARG
+        assert call(Nk=0) == fa.FA_ERR_INVALID_ARG
+        assert call(causal=3) == fa.FA_ERR_INVALID_ARG
+        assert call(causal=-1) == fa.FA_ERR_INVALID_ARG
+        assert call(Hkv=3) == fa.FA_ERR_INVALID_ARG
+        assert call(d=48) == fa.FA_ERR_UNSUPPORTED
+        assert call(scale=0.0) == fa.FA_ERR_INVALID_ARG
+        assert call(B=1 << 16, H=1 << 10, Nq=1 << 10) == fa.FA_ERR_INVALID_ARG  # 2^36 query rows
+    assert fwd(splits=-2) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_fwd_general(*ptrs[:4], P(0x5004), 1, 4, 2, 100, 300, 96, 2, 0.1, 0, None) == fa.FA_ERR_INVALID_ARG
+    assert fa.FA_CAUSAL_NONE == 0 and fa.FA_CAUSAL_TOP_LEFT == 1 and fa.FA_CAUSAL_BOTTOM_RIGHT == 2
 
 
 def test_gqa_argument_errors(lib):

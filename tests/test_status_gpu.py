@@ -40,7 +40,7 @@ def test_context_usable_after_timeout(fa):
 
 def test_bad_arguments_raise_before_launch(fa):
     torch = torch_cuda()
-    q = torch.zeros(1, 1, 64, 96, dtype=torch.bfloat16, device="cuda")
+    q = torch.zeros(1, 1, 64, 80, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(fa.FaError) as e:
         fa.forward(q, q, q)
     assert e.value.status == fa.FA_ERR_UNSUPPORTED
