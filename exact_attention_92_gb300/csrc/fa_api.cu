@@ -19,6 +19,8 @@ namespace fa {
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_combine(int d, const CombineParams& p, cudaStream_t stream);
+cudaError_t launch_fwd256(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
+                          int grid, cudaStream_t stream);
 cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const BwdParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_bwd_dq(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
@@ -98,10 +100,15 @@ int device_state(DeviceState** out) {
 
 bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int validate(int B, int H, int Nq, int Nk, int d, float scale) {
+// Head dims of the forward pass (64, 96, 128, 256) and of the backward pass
+// (64, 96, 128).
+bool fwd_head_dim(int d) { return d == 64 || d == 96 || d == 128 || d == 256; }
+bool bwd_head_dim(int d) { return d == 64 || d == 96 || d == 128; }
+
+int validate(int B, int H, int Nq, int Nk, int d, float scale, bool backward = false) {
   if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return FA_ERR_INVALID_ARG;
   if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_INVALID_ARG;
-  if (d != 64 && d != 96 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (!(backward ? bwd_head_dim(d) : fwd_head_dim(d))) return FA_ERR_UNSUPPORTED;
   const long double n = Nq > Nk ? Nq : Nk;
   if ((long double)B * H * n * d >= 9.0e18L) return FA_ERR_INVALID_ARG;
   // Row and unit indices are 32-bit: B*H*Nq rows, (query block, split) units.
@@ -117,10 +124,10 @@ int causal_offset(int causal, int Nq, int Nk) { return causal == FA_CAUSAL_BOTTO
 // [B*H, N, d] bf16 viewed as a 3-D tensor (d innermost); boxes of 64 x 128 x 1
 // with the 128-byte swizzle the MMA descriptors expect.  Rows past N, and the
 // columns of the second 64-column box past d = 96, read as zero.
-int encode_bhnd(CUtensorMap* m, const void* ptr, int BH, int N, int d) {
+int encode_bhnd(CUtensorMap* m, const void* ptr, int BH, int N, int d, int box_rows = 128) {
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -131,15 +138,12 @@ int encode_bhnd(CUtensorMap* m, const void* ptr, int BH, int N, int d) {
 // Number of key splits: only when the (batch*head, query block) units cannot
 // fill the GPU.  Picks the split count with the best last-wave occupancy,
 // keeping at least 4 key tiles per split.
-int choose_splits(int BH, int Nq, int Nk, int sm_count) {
-  const int qblocks = (Nq + 255) / 256;
-  const int nkv = (Nk + 127) / 128;
-  const long long units = (long long)BH * qblocks;
+int choose_splits(long long units, int nkv, int min_tiles, int sm_count) {
   if (units >= 2LL * sm_count) return 1;
   int best = 1;
   double best_eff = 0.0;
   for (int s = 1; s <= 16; ++s) {
-    if (s > 1 && nkv / s < 4) break;
+    if (s > 1 && nkv / s < min_tiles) break;
     const long long u = units * s;
     const long long waves = (u + sm_count - 1) / sm_count;
     const double eff = (double)u / (double)(waves * sm_count) - 0.01 * (s - 1);
@@ -210,7 +214,7 @@ int internal_device_setup(unsigned int** status, int* sm_count) {
   *sm_count = s->sm_count;
   return FA_OK;
 }
-int internal_validate(int B, int H, int N, int d, float scale) { return validate(B, H, N, N, d, scale); }
+int internal_validate(int B, int H, int N, int d, float scale) { return validate(B, H, N, N, d, scale, true); }
 int internal_encode_bhnd(CUtensorMap* m, const void* ptr, int BH, int N, int d) {
   return encode_bhnd(m, ptr, BH, N, d);
 }
@@ -273,7 +277,8 @@ const char* fa_strerror(int status) {
   switch (status) {
     case FA_OK: return "FA_OK";
     case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: null or misaligned pointer, bad size or scale";
-    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: head dim must be 64, 96 or 128 on an sm_103 GPU";
+    case FA_ERR_UNSUPPORTED:
+      return "FA_ERR_UNSUPPORTED: head dim must be 64, 96, 128 (or 256, forward only) on an sm_103 GPU";
     case FA_ERR_CUDA: return "FA_ERR_CUDA: CUDA runtime or launch failure";
     case FA_ERR_NO_MEMORY: return "FA_ERR_NO_MEMORY: workspace allocation failed";
     case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a device-side wait gave up";
@@ -320,16 +325,23 @@ int fa_fwd_general(const void* q, const void* k, const void* v, void* o, float* 
   if (e) return e;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int BH = B * H;
-  const int nkv = (Nk + 127) / 128;
-  int S = num_splits == 0 ? choose_splits(BH, Nq, Nk, s->sm_count) : num_splits;
+  // Work units: (batch*head, query block, key split).  A query block is 256
+  // rows (two 128-row tiles) with 128-key tiles, or at d = 256 one 128-row
+  // tile with 64-key tiles.
+  const bool wide = d == 256;
+  const int q_block = wide ? 128 : 256;
+  const int key_tile = wide ? 64 : 128;
+  const int nkv = (Nk + key_tile - 1) / key_tile;
+  const int qblocks = (Nq + q_block - 1) / q_block;
+  int S = num_splits == 0 ? choose_splits((long long)BH * qblocks, nkv, wide ? 8 : 4, s->sm_count) : num_splits;
   if (S > nkv) S = nkv;
   if (S < 1) S = 1;
   const int per_split = (nkv + S - 1) / S;
   S = (nkv + per_split - 1) / per_split;  // no empty split
 
   CUtensorMap tq, tk, tv;
-  if (encode_bhnd(&tq, q, BH, Nq, d) || encode_bhnd(&tk, k, B * Hkv, Nk, d) ||
-      encode_bhnd(&tv, v, B * Hkv, Nk, d))
+  if (encode_bhnd(&tq, q, BH, Nq, d) || encode_bhnd(&tk, k, B * Hkv, Nk, d, key_tile) ||
+      encode_bhnd(&tv, v, B * Hkv, Nk, d, key_tile))
     return FA_ERR_CUDA;
 
   FwdParams p;
@@ -344,7 +356,7 @@ int fa_fwd_general(const void* q, const void* k, const void* v, void* o, float* 
   p.scale_log2 = scale * 1.4426950408889634f;
   p.num_splits = S;
   p.kv_tiles_per_split = per_split;
-  p.num_q_blocks = (Nq + 255) / 256;
+  p.num_q_blocks = qblocks;
   p.num_units = BH * p.num_q_blocks * S;
   p.o = o;
   p.lse = lse;
@@ -364,7 +376,9 @@ int fa_fwd_general(const void* q, const void* k, const void* v, void* o, float* 
     p.lse_part = p.o_part + (size_t)S * rows * d;
   }
   const int grid = p.num_units < s->sm_count ? p.num_units : s->sm_count;
-  cudaError_t ce = timed(FA_KERNEL_FWD, st, [&] { return fa::launch_fwd(d, tq, tk, tv, p, grid, st); });
+  cudaError_t ce = timed(FA_KERNEL_FWD, st, [&] {
+    return wide ? fa::launch_fwd256(tq, tk, tv, p, grid, st) : fa::launch_fwd(d, tq, tk, tv, p, grid, st);
+  });
   if (ce == cudaSuccess && S > 1) {
     fa::CombineParams c;
     c.rows = (int)rows;
@@ -401,7 +415,7 @@ int fa_bwd_general(const void* q, const void* k, const void* v, const void* o, c
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dout) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return FA_ERR_INVALID_ARG;
-  int e = validate(B, H, Nq, Nk, d, scale);
+  int e = validate(B, H, Nq, Nk, d, scale, true);
   if (e) return e;
   if (Hkv < 1 || H % Hkv != 0) return FA_ERR_INVALID_ARG;
   if (causal < FA_CAUSAL_NONE || causal > FA_CAUSAL_BOTTOM_RIGHT) return FA_ERR_INVALID_ARG;

@@ -15,7 +15,8 @@
  *    dO, dQ, dK, dV are bf16, shape [B, H, N, d], contiguous row-major (d is
  *    the fastest index).  LSE is fp32, shape [B, H, N], natural logarithm.
  *  - Pointers must be non-null and 16-byte aligned.
- *  - d must be 64, 96 or 128 (FA_ERR_UNSUPPORTED otherwise).  B, H, N >= 1.
+ *  - d must be 64, 96 or 128, and for the forward entry points may also be
+ *    256 (FA_ERR_UNSUPPORTED otherwise).  B, H, N >= 1.
  *    N need not be a multiple of the tile size.  Queries and keys have the
  *    same length N, except in fa_fwd_general / fa_bwd_general.
  *  - causal != 0 applies the mask of "FlashAttention V2 in depth" section 5.1:
@@ -47,7 +48,7 @@ extern "C" {
 typedef enum {
   FA_OK = 0,
   FA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size or scale      */
-  FA_ERR_UNSUPPORTED = 2, /* head dim not 64/96/128, or not an sm_103 GPU   */
+  FA_ERR_UNSUPPORTED = 2, /* head dim not supported, or not an sm_103 GPU   */
   FA_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed     */
   FA_ERR_NO_MEMORY = 4,   /* workspace allocation failed                     */
   FA_ERR_TIMEOUT = 5,     /* a device-side wait gave up (fa_poll_status)     */

@@ -79,6 +79,9 @@ FWD_SHAPES = [
     (1, 2, 2, 1000, 8192, 64), (1, 2, 2, 1000, 8192, 96), (2, 2, 2, 1, 8192, 96),
     (1, 1, 1, 300, 100, 128), (1, 2, 2, 257, 130, 64), (2, 3, 3, 200, 200, 96),
     (1, 1, 1, 1000, 1000, 96), (1, 4, 2, 200, 700, 96), (1, 4, 1, 129, 383, 64),
+    # head dim 256 (its own kernel: one query tile per CTA, 64-key tiles)
+    (1, 2, 2, 1, 8192, 256), (1, 2, 2, 128, 8192, 256), (1, 2, 2, 1000, 8192, 256),
+    (1, 1, 1, 300, 100, 256), (2, 3, 3, 200, 200, 256), (1, 4, 2, 200, 700, 256), (1, 1, 1, 63, 63, 256),
 ]
 
 
@@ -98,10 +101,11 @@ def test_forward(fa, shape, mode):
         assert np.all(o[:, :, :-off] == 0.0), what
 
 
+@pytest.mark.parametrize("d", [96, 256])
 @pytest.mark.parametrize("splits", [1, 3, 16])
 @pytest.mark.parametrize("mode", ["top_left", "bottom_right"])
-def test_forward_forced_splits(fa, mode, splits):
-    q, k, v, _ = make(1, 2, 2, 300, 4000, 96, seed=7100 + splits)
+def test_forward_forced_splits(fa, mode, splits, d):
+    q, k, v, _ = make(1, 2, 2, 300, 4000, d, seed=7100 + splits + d)
     o, lse, _ = run_fwd(fa, q, k, v, mode, splits)
     O, L, weights = oracle_fwd(q, k, v, mode)
     check_o(o, O, f"splits={splits} {mode}", weights)
@@ -109,13 +113,14 @@ def test_forward_forced_splits(fa, mode, splits):
 
 
 @pytest.mark.parametrize("mode", ["none", "top_left", "bottom_right"])
-@pytest.mark.parametrize("c", [dict(B=16384 // N, H=2048 // 96, N=N, d=96) for N in (1024, 4096)],
-                         ids=lambda c: f"B{c['B']}H{c['H']}N{c['N']}d96")
-def test_forward_d96_16k_tokens(fa, c, mode):
-    """Head dim 96 at the 16K-token sweep's sizes (hidden 2016 = 21 heads),
-    checked on 1024 seeded rows per head."""
+@pytest.mark.parametrize("c", [dict(B=16384 // N, H=2048 // d, N=N, d=d) for d in (96, 256) for N in (1024, 4096)],
+                         ids=lambda c: f"B{c['B']}H{c['H']}N{c['N']}d{c['d']}")
+def test_forward_16k_tokens_other_head_dims(fa, c, mode):
+    """Head dims 96 and 256 at the 16K-token sweep's sizes (hidden 2016 = 21
+    heads of 96, 2048 = 8 heads of 256), checked on 1024 seeded rows per
+    head."""
     B, H, N, d = c["B"], c["H"], c["N"], c["d"]
-    q, k, v, _ = make(B, H, H, N, N, d, seed=7200 + N)
+    q, k, v, _ = make(B, H, H, N, N, d, seed=7200 + N + d)
     o, lse, _ = run_fwd(fa, q, k, v, mode)
     rows = inputs.sample_rows(7200 + N, N)
     O, L, weights = oracle_fwd(q, k, v, mode, rows)
