@@ -61,6 +61,7 @@ def load_peaks():
 
 KERNEL_SOURCES = {
     "fa_fwd_kernel": ["fa_fwd.cu", "sm103_primitives.cuh", "fa_common.h"],
+    "fa_fwd256_kernel": ["fa_fwd256.cu", "sm103_primitives.cuh", "fa_common.h"],
     "fa_combine_kernel": ["fa_fwd.cu", "sm103_primitives.cuh", "fa_common.h"],
     "fa_bwd_dkdv_kernel": ["fa_bwd.cu", "sm103_primitives.cuh", "fa_common.h"],
     "fa_bwd_preprocess": ["fa_bwd.cu", "sm103_primitives.cuh", "fa_common.h"],
@@ -357,6 +358,7 @@ def run_ours(args, world, rank, local):
     extra_bwd = bwd_targets(fa, device, peaks, args) if (rank == 0 and not args.no_extra) else None
     extra_gqa = gqa_targets(fa, device, peaks, args) if (rank == 0 and not args.no_extra) else None
     extra_short = short_targets(fa, device, peaks, args) if (rank == 0 and not args.no_extra) else None
+    extra_general = general_targets(fa, device, peaks, args) if (rank == 0 and not args.no_extra) else None
 
     if rank != 0:
         return None
@@ -395,6 +397,8 @@ def run_ours(args, world, rank, local):
         line["gqa_targets"] = extra_gqa
     if extra_short is not None:
         line["short_targets"] = extra_short
+    if extra_general is not None:
+        line["general_targets"] = extra_general
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tf, dt, desc = oracle_sample()
         line["cpu_baseline"] = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
@@ -593,6 +597,83 @@ def short_targets(fa, device, peaks, args):
     st = fa.fa_poll_status()
     if st != 0:
         raise RuntimeError(f"device status after the short-sequence cases: {fa.fa_strerror(st)}")
+    return out
+
+
+def visible_pairs(Nq, Nk, causal, align):
+    """(query, key) pairs the mask lets through, per head."""
+    if not causal:
+        return Nq * Nk
+    off = 0 if align == "top_left" else Nk - Nq
+    # row i sees min(Nk, max(0, i + off + 1)) keys
+    tot = 0
+    for i in range(Nq):
+        tot += min(Nk, max(0, i + off + 1))
+    return tot
+
+
+def general_targets(fa, device, peaks, args):
+    """Head dims 96 and 256 (hidden 2016 / 2048 at 16K tokens), and queries
+    shorter than the keys with bottom-right causal alignment: a grouped-query
+    decode step (one query row per head over 8192 keys, HBM-bound: the K, V
+    reads are the traffic) and a 1024-row chunk over 8192 keys.  FLOPs are
+    4 d per visible (query, key) pair (2.5x for the backward)."""
+    import torch
+
+    cases = [
+        # (name, B, H, Hkv, Nq, Nk, d, causal, backward too)
+        ("d=96 B=8 H=21 N=2048 non-causal", 8, 21, 21, 2048, 2048, 96, False, True),
+        ("d=96 B=8 H=21 N=2048 causal", 8, 21, 21, 2048, 2048, 96, "top_left", True),
+        ("d=96 B=4 H=21 N=4096 causal", 4, 21, 21, 4096, 4096, 96, "top_left", True),
+        ("d=256 B=4 H=8 N=4096 non-causal", 4, 8, 8, 4096, 4096, 256, False, False),
+        ("d=256 B=4 H=8 N=4096 causal", 4, 8, 8, 4096, 4096, 256, "top_left", False),
+        ("d=256 B=1 H=8 N=16384 causal", 1, 8, 8, 16384, 16384, 256, "top_left", False),
+        ("decode GQA B=8 H=32 Hkv=8 Nq=1 Nk=8192 d=128 bottom-right", 8, 32, 8, 1, 8192, 128, "bottom_right", False),
+        ("chunk B=1 H=32 Nq=1024 Nk=8192 d=128 bottom-right", 1, 32, 32, 1024, 8192, 128, "bottom_right", True),
+    ]
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    out = []
+
+    def timed(fn, reps=10):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for st, en in ev:  # queued before one synchronise (host time stays out)
+            flush.zero_()
+            st.record(stream)
+            fn()
+            en.record(stream)
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in ev) / reps
+
+    for name, B, H, Hkv, Nq, Nk, d, causal, bwd in cases:
+        g = torch.Generator(device=device)
+        g.manual_seed(7000)
+        q, do = (torch.randn((B, H, Nq, d), generator=g, device=device).to(torch.bfloat16) for _ in range(2))
+        k, v = (torch.randn((B, Hkv, Nk, d), generator=g, device=device).to(torch.bfloat16) for _ in range(2))
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=device)
+        pairs = B * H * visible_pairs(Nq, Nk, bool(causal), causal if causal else "top_left")
+        fl = 4.0 * d * pairs
+        ms = timed(lambda: fa.fa_fwd_general(q, k, v, o, lse, causal))
+        nbytes = 2 * d * (2 * B * H * Nq + 2 * B * Hkv * Nk) + 4 * B * H * Nq
+        gbs = nbytes / ms / 1e6
+        out.append({"case": name + " forward", "us": round(ms * 1e3, 2), "tflops": round(fl / ms / 1e9, 1),
+                    "frac_tensor": round(fl / ms / 1e9 / peaks["bf16_tflops"], 4), "hbm_gbs": round(gbs, 1),
+                    "frac_hbm": round(gbs / peaks["hbm_gbs"], 4)})
+        if bwd:
+            dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+            ms_b = timed(lambda: fa.fa_bwd_general(q, k, v, o, lse, do, dq, dk, dv, causal))
+            out.append({"case": name + " backward", "us": round(ms_b * 1e3, 2),
+                        "tflops": round(2.5 * fl / ms_b / 1e9, 1),
+                        "frac_tensor": round(2.5 * fl / ms_b / 1e9 / peaks["bf16_tflops"], 4)})
+            del dq, dk, dv
+        del q, k, v, do, o, lse
+    st = fa.fa_poll_status()
+    if st != 0:
+        raise RuntimeError(f"device status after the general cases: {fa.fa_strerror(st)}")
     return out
 
 

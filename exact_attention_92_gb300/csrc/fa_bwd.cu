@@ -601,10 +601,14 @@ __global__ void __launch_bounds__(384, 1)
       if (!__all_sync(0xffffffffu, mbar_wait(dkv_full, uc & 1, ctl, kWaitBwdSoftmax))) return false;
       ++uc;
       tc_fence_after();
-      if (hc == 0)
+      if constexpr (RowSplit<D>::kLo == RowSplit<D>::kHi) {
         write_part(std::integral_constant<int, RowSplit<D>::kLo>{}, kr, head);
-      else
-        write_part(std::integral_constant<int, RowSplit<D>::kHi>{}, kr, head);
+      } else {
+        if (hc == 0)
+          write_part(std::integral_constant<int, RowSplit<D>::kLo>{}, kr, head);
+        else
+          write_part(std::integral_constant<int, RowSplit<D>::kHi>{}, kr, head);
+      }
       return true;
     };
     int pend_kr = -1;  // the unit whose dK / dV are still in TMEM
@@ -1017,10 +1021,14 @@ __global__ void __launch_bounds__(384, 1)
       if (!__all_sync(0xffffffffu, mbar_wait(dq_full, uc & 1, ctl, kWaitBwdDq))) return false;
       ++uc;
       tc_fence_after();
-      if (hc == 0)
+      if constexpr (RowSplit<D>::kLo == RowSplit<D>::kHi) {
         write_part(std::integral_constant<int, RowSplit<D>::kLo>{}, q, head);
-      else
-        write_part(std::integral_constant<int, RowSplit<D>::kHi>{}, q, head);
+      } else {
+        if (hc == 0)
+          write_part(std::integral_constant<int, RowSplit<D>::kLo>{}, q, head);
+        else
+          write_part(std::integral_constant<int, RowSplit<D>::kHi>{}, q, head);
+      }
       return true;
     };
     int pend_q = -1;  // the unit whose dQ is still in TMEM

@@ -542,7 +542,8 @@ __global__ void __launch_bounds__(384, 1)
 }
 
 // Merge of split-KV partial results: L = log sum_s exp(L_s),
-// O = sum_s exp(L_s - L) O_s.  One warp per query row.
+// O = sum_s exp(L_s - L) O_s.  One warp per query row (any head dim of the
+// forward kernels, 256 included).
 template <int D>
 __global__ void __launch_bounds__(256) fa_combine_kernel(const CombineParams p) {
   const int row = blockIdx.x * 8 + threadIdx.x / 32;
@@ -573,6 +574,13 @@ __global__ void __launch_bounds__(256) fa_combine_kernel(const CombineParams p) 
     v.x = pack_bf16(acc[0] * inv, acc[1] * inv);
     v.y = pack_bf16(acc[2] * inv, acc[3] * inv);
     *reinterpret_cast<uint2*>(o) = v;
+  } else if constexpr (kPer == 8) {
+    uint4 v;
+    v.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+    v.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+    v.z = pack_bf16(acc[4] * inv, acc[5] * inv);
+    v.w = pack_bf16(acc[6] * inv, acc[7] * inv);
+    *reinterpret_cast<uint4*>(o) = v;
   } else {
 #pragma unroll
     for (int i = 0; i < kPer; ++i) o[i] = __float2bfloat16_rn(acc[i] * inv);
@@ -608,6 +616,7 @@ cudaError_t launch_combine(int d, const CombineParams& p, cudaStream_t stream) {
     case 64: fa_combine_kernel<64><<<grid, 256, 0, stream>>>(p); break;
     case 96: fa_combine_kernel<96><<<grid, 256, 0, stream>>>(p); break;
     case 128: fa_combine_kernel<128><<<grid, 256, 0, stream>>>(p); break;
+    case 256: fa_combine_kernel<256><<<grid, 256, 0, stream>>>(p); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
