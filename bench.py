@@ -779,10 +779,12 @@ def fwd_targets(fa, device, peaks, args):
 
 def run_profile(case):
     """Two warm-up launches, then one launch, of the forward kernel on the GPT
-    layer (B=8 H=32 N=4096 d=128 causal) or on B=4 H=16 N=1024 d=64
+    layer (B=8 H=32 N=4096 d=128 causal), on B=4 H=16 N=1024 d=64
     non-causal (``fwd_short``, 33.6 MB: the DRAM figures there are those of
-    a problem below the L2 size), or of the backward on the fwd+bwd workload,
-    for ``ncu -s 2 -c 1`` captures."""
+    a problem below the L2 size) or on B=4 H=8 N=4096 d=256 causal
+    (``fwd256``); of the split-KV forward and its merge on one head of 65536
+    tokens (``splitkv``); or of the backward on the fwd+bwd workload; for
+    ``ncu -s 2 -c 1`` captures."""
     import torch
 
     import exact_attention_92_gb300 as fa
@@ -799,6 +801,10 @@ def run_profile(case):
         shape, causal = (8, 32, 4096, 128), True
     elif case == "fwd_short":
         shape, causal = (4, 16, 1024, 64), False
+    elif case == "splitkv":
+        shape, causal = (1, 1, 65536, 128), True
+    elif case == "fwd256":
+        shape, causal = (4, 8, 4096, 256), True
     else:
         w = WORKLOAD
         shape, causal = (w["B"], w["H"], w["N"], w["d"]), w["causal"]
@@ -809,8 +815,10 @@ def run_profile(case):
     if case == "bwd":
         fa.fa_fwd(q, k, v, o, lse, causal)
     for _ in range(3):
-        if case in ("fwd", "fwd_short"):
+        if case in ("fwd", "fwd_short", "fwd256"):
             fa.fa_fwd_ex(q, k, v, o, lse, causal, None, 1)
+        elif case == "splitkv":
+            fa.fa_fwd(q, k, v, o, lse, causal)
         else:
             fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, causal)
     torch.cuda.synchronize()
@@ -886,7 +894,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true", help="skip the forward-only and backward-only target cases")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip timing the CPU oracle")
-    ap.add_argument("--profile", choices=["fwd", "fwd_short", "bwd"], help="3 launches of one kernel, for ncu")
+    ap.add_argument("--profile", choices=["fwd", "fwd_short", "splitkv", "fwd256", "bwd"],
+                    help="3 launches of one kernel (or of the split-KV forward and its merge), for ncu")
     args = ap.parse_args(argv)
     if args.profile:
         run_profile(args.profile)

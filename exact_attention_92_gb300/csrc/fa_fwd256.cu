@@ -20,7 +20,7 @@
 // row's thread, O~ unnormalised in TMEM and divided once at the end by the
 // sum of the bf16-rounded weights the P V product used, L = m + log l from
 // the fp32 weights, and the O~ correction only when a row max grows by more
-// than 2^8.  Because the product that reads P_{j-1} may still be running
+// than a factor 2^24.  Because the product that reads P_{j-1} may still be running
 // when the softmax of step j wants to correct O~, every step first waits for
 // the previous step's P V product (one barrier phase per step, so the wait
 // is never more than one phase behind).
@@ -49,7 +49,7 @@ constexpr int kOffKV = kQBytes;
 constexpr int kOffBar = kOffKV + kStages * kKVBytes;
 constexpr int kNumBars = 2 + 2 * kStages + 2 + 2 + 1 + 1 + 1 + 1;
 constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16;
-constexpr float kRescaleThreshold = 8.0f;              // log2 units
+constexpr float kRescaleThreshold = 24.0f;             // log2 units
 static_assert(kSmemBytes <= 232448, "shared memory");
 
 struct Unit {
