@@ -21,6 +21,10 @@ cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, cons
 cudaError_t launch_combine(int d, const CombineParams& p, cudaStream_t stream);
 cudaError_t launch_fwd256(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
                           int grid, cudaStream_t stream);
+cudaError_t launch_bwd256_kv(bool dk_pass, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                             const CUtensorMap& tdo, const BwdParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_bwd256_dq(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                             const CUtensorMap& tdo, const BwdParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const BwdParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_bwd_dq(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
@@ -100,10 +104,9 @@ int device_state(DeviceState** out) {
 
 bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Head dims of the forward pass (64, 96, 128, 256) and of the backward pass
-// (64, 96, 128).
+// Head dims of the library: 64, 96, 128 and 256 (forward and backward).
 bool fwd_head_dim(int d) { return d == 64 || d == 96 || d == 128 || d == 256; }
-bool bwd_head_dim(int d) { return d == 64 || d == 96 || d == 128; }
+bool bwd_head_dim(int d) { return fwd_head_dim(d); }
 
 int validate(int B, int H, int Nq, int Nk, int d, float scale, bool backward = false) {
   if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return FA_ERR_INVALID_ARG;
@@ -278,7 +281,7 @@ const char* fa_strerror(int status) {
     case FA_OK: return "FA_OK";
     case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: null or misaligned pointer, bad size or scale";
     case FA_ERR_UNSUPPORTED:
-      return "FA_ERR_UNSUPPORTED: head dim must be 64, 96, 128 (or 256, forward only) on an sm_103 GPU";
+      return "FA_ERR_UNSUPPORTED: head dim must be 64, 96, 128 or 256 (fa_bwd_noalloc: not 256) on an sm_103 GPU";
     case FA_ERR_CUDA: return "FA_ERR_CUDA: CUDA runtime or launch failure";
     case FA_ERR_NO_MEMORY: return "FA_ERR_NO_MEMORY: workspace allocation failed";
     case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a device-side wait gave up";
@@ -426,9 +429,15 @@ int fa_bwd_general(const void* q, const void* k, const void* v, const void* o, c
   const int BH = B * H;
   const size_t rows = (size_t)BH * Nq;
 
-  CUtensorMap tq, tk, tv, tdo;
+  // Tensor maps: 128-row boxes; at d = 256 also 64-row ones (the query steps
+  // of the key/value kernel, the key steps of the dQ kernel).
+  const bool wide = d == 256;
+  CUtensorMap tq, tk, tv, tdo, tq64, tk64, tv64, tdo64;
   if (encode_bhnd(&tq, q, BH, Nq, d) || encode_bhnd(&tk, k, B * Hkv, Nk, d) ||
       encode_bhnd(&tv, v, B * Hkv, Nk, d) || encode_bhnd(&tdo, dout, BH, Nq, d))
+    return FA_ERR_CUDA;
+  if (wide && (encode_bhnd(&tq64, q, BH, Nq, d, 64) || encode_bhnd(&tk64, k, B * Hkv, Nk, d, 64) ||
+               encode_bhnd(&tv64, v, B * Hkv, Nk, d, 64) || encode_bhnd(&tdo64, dout, BH, Nq, d, 64)))
     return FA_ERR_CUDA;
 
   fa::BwdParams p;
@@ -492,10 +501,19 @@ int fa_bwd_general(const void* q, const void* k, const void* v, const void* o, c
   const int grid_kv = p.num_units_kv < s->sm_count ? p.num_units_kv : s->sm_count;
   if (ce == cudaSuccess)
     ce = timed(FA_KERNEL_BWD_PRE, st, [&] { return fa::launch_bwd_preprocess(d, o, dout, dvec, (int)rows, st); });
-  if (ce == cudaSuccess)
-    ce = timed(FA_KERNEL_BWD, st, [&] { return fa::launch_bwd_dkdv(d, tq, tk, tv, tdo, p, grid_kv, st); });
-  if (ce == cudaSuccess)
-    ce = timed(FA_KERNEL_BWD_DQ, st, [&] { return fa::launch_bwd_dq(d, tq, tk, tv, tdo, p, grid_q, st); });
+  if (!wide) {
+    if (ce == cudaSuccess)
+      ce = timed(FA_KERNEL_BWD, st, [&] { return fa::launch_bwd_dkdv(d, tq, tk, tv, tdo, p, grid_kv, st); });
+    if (ce == cudaSuccess)
+      ce = timed(FA_KERNEL_BWD_DQ, st, [&] { return fa::launch_bwd_dq(d, tq, tk, tv, tdo, p, grid_q, st); });
+  } else {
+    // Head dim 256: dV pass, dK pass, then dQ.
+    for (int pass = 0; pass < 2 && ce == cudaSuccess; ++pass)
+      ce = timed(FA_KERNEL_BWD, st,
+                 [&] { return fa::launch_bwd256_kv(pass == 1, tq64, tk, tv, tdo64, p, grid_kv, st); });
+    if (ce == cudaSuccess)
+      ce = timed(FA_KERNEL_BWD_DQ, st, [&] { return fa::launch_bwd256_dq(tq, tk64, tv64, tdo, p, grid_q, st); });
+  }
   cudaFreeAsync(ws, st);
   return ce == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }

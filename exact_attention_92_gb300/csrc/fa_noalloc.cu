@@ -99,6 +99,7 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
     return FA_ERR_INVALID_ARG;
   int e = fa::internal_validate(B, H, N, d, scale);
   if (e) return e;
+  if (d == 256) return FA_ERR_UNSUPPORTED;  // runs the head-dim 64 / 96 / 128 kernels only
   const size_t rows = (size_t)B * H * N;
   const size_t need = rows * sizeof(float);
   if (need > (size_t)FA_BWD_NOALLOC_SCRATCH_BYTES) return FA_ERR_SCRATCH_TOO_SMALL;

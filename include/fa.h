@@ -15,8 +15,8 @@
  *    dO, dQ, dK, dV are bf16, shape [B, H, N, d], contiguous row-major (d is
  *    the fastest index).  LSE is fp32, shape [B, H, N], natural logarithm.
  *  - Pointers must be non-null and 16-byte aligned.
- *  - d must be 64, 96 or 128, and for the forward entry points may also be
- *    256 (FA_ERR_UNSUPPORTED otherwise).  B, H, N >= 1.
+ *  - d must be 64, 96, 128 or 256 (FA_ERR_UNSUPPORTED otherwise; see
+ *    fa_bwd_noalloc for its own limit).  B, H, N >= 1.
  *    N need not be a multiple of the tile size.  Queries and keys have the
  *    same length N, except in fa_fwd_general / fa_bwd_general.
  *  - causal != 0 applies the mask of "FlashAttention V2 in depth" section 5.1:
@@ -139,7 +139,9 @@ int fa_fwd_general(const void* q, const void* k, const void* v, void* o, float* 
  *   dout    : in,  bf16 [B,H,N,d] (gradient of the loss w.r.t. O)
  *   dq,dk,dv: out, bf16 [B,H,N,d]
  * Workspace: D, B*H*N*4 bytes from cudaMallocAsync on `stream`.  The results
- * are bitwise reproducible from run to run.
+ * are bitwise reproducible from run to run.  At d = 256 the dK and dV
+ * accumulators of a key tile do not fit in tensor memory together, so the
+ * key/value kernel runs twice (a dV pass and a dK pass, recomputing S^T).
  */
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
            void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale, void* stream);
@@ -191,7 +193,8 @@ int fa_bwd_general(const void* q, const void* k, const void* v, const void* o, c
  *  - Arguments, layouts and ownership as fa_bwd; the caller still passes
  *    (and owns) every input and output.
  *  - Returns FA_ERR_SCRATCH_TOO_SMALL, before any device work, when
- *    B*H*N*4 exceeds FA_BWD_NOALLOC_SCRATCH_BYTES.
+ *    B*H*N*4 exceeds FA_BWD_NOALLOC_SCRATCH_BYTES, and FA_ERR_UNSUPPORTED
+ *    for d = 256 (it runs the kernels of head dims 64, 96 and 128).
  *  - The first call on a device sets up that device (with it current): it
  *    looks up the array's device address, and the library's status word,
  *    and keeps them.  Make that first call before any stream capture; a

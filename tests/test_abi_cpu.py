@@ -88,7 +88,7 @@ def test_general_argument_errors(lib):
         assert call(scale=0.0) == fa.FA_ERR_INVALID_ARG
         assert call(B=1 << 16, H=1 << 10, Nq=1 << 10) == fa.FA_ERR_INVALID_ARG  # 2^36 query rows
     assert fwd(splits=-2) == fa.FA_ERR_INVALID_ARG
-    assert bwd(d=256) == fa.FA_ERR_UNSUPPORTED  # head dim 256: forward only
+    assert lib.fa_bwd_noalloc(*ptrs, 1, 1, 128, 256, 1, 0.06, None) == fa.FA_ERR_UNSUPPORTED
     assert lib.fa_fwd_general(*ptrs[:4], P(0x5004), 1, 4, 2, 100, 300, 96, 2, 0.1, 0, None) == fa.FA_ERR_INVALID_ARG
     assert fa.FA_CAUSAL_NONE == 0 and fa.FA_CAUSAL_TOP_LEFT == 1 and fa.FA_CAUSAL_BOTTOM_RIGHT == 2
 

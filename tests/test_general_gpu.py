@@ -132,6 +132,9 @@ BWD_SHAPES = [
     (1, 2, 2, 1, 8192, 128), (1, 2, 2, 128, 8192, 64), (1, 1, 1, 1000, 8192, 96),
     (1, 2, 2, 1000, 8192, 128), (1, 1, 1, 300, 100, 128), (1, 2, 2, 257, 130, 96),
     (2, 3, 3, 200, 200, 96), (1, 1, 1, 640, 640, 96), (1, 4, 2, 200, 700, 96), (1, 4, 1, 129, 383, 64),
+    # head dim 256 (its own kernels: dV and dK passes over 64-row query steps, dQ over 64-key steps)
+    (1, 1, 1, 1, 4096, 256), (1, 2, 2, 1000, 4096, 256), (1, 1, 1, 300, 100, 256), (2, 3, 3, 200, 200, 256),
+    (1, 4, 2, 200, 700, 256), (1, 1, 1, 63, 63, 256), (1, 2, 2, 640, 640, 256),
 ]
 
 
@@ -190,10 +193,36 @@ def test_backward_d96_b8_h21_n2048(fa, causal):
             check_grad(dq[b, h, rows[b, h]], ref, "dQ", f"head {(b, h)}")
 
 
-def test_general_repeatable(fa):
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_d256_b2_h8_n2048(fa, causal):
+    """Head dim 256 backward at N = 2048 (B=2, H=8, hidden 2048): dK, dV in
+    full on 3 seeded heads, dQ on 1024 seeded rows of every head."""
+    B, H, N, d = 2, 8, 2048, 256
+    case = inputs.make_case(B, H, N, d, causal, seed=7600 + int(causal), with_do=True)
+    tq, tk, tv, tdo = dev(case.q), dev(case.k), dev(case.v), dev(case.do)
+    o, lse = fa.forward(tq, tk, tv, causal=causal)
+    dq, dk, dv = fa.backward(tq, tk, tv, o, lse, tdo, causal=causal)
+    assert fa.fa_poll_status() == 0
+    dq, dk, dv = host(dq), host(dk), host(dv)
+    Q, K, V, DO = (case.f64(n) for n in ("q", "k", "v", "do"))
+    rng = np.random.default_rng(case.seed + 11)
+    for i in rng.choice(B * H, 3, replace=False):
+        b, h = int(i) // H, int(i) % H
+        rq, rk, rv = att.backward_head(Q[b, h], K[b, h], V[b, h], DO[b, h], case.scale, causal)
+        check_grad(dk[b, h], rk, "dK", f"head {(b, h)}")
+        check_grad(dv[b, h], rv, "dV", f"head {(b, h)}")
+    rows = inputs.sample_rows_per_head(case.seed, B, H, N)
+    for b in range(B):
+        for h in range(H):
+            ref = att.backward_dq_rows_head(Q[b, h], K[b, h], V[b, h], DO[b, h], case.scale, causal, rows[b, h])
+            check_grad(dq[b, h, rows[b, h]], ref, "dQ", f"head {(b, h)}")
+
+
+@pytest.mark.parametrize("d", [96, 256])
+def test_general_repeatable(fa, d):
     """No atomics with unequal lengths either: identical bits run to run."""
     torch = torch_cuda()
-    q, k, v, do = make(1, 4, 2, 333, 1111, 96, seed=7500, with_do=True)
+    q, k, v, do = make(1, 4, 2, 333, 1111, d, seed=7500, with_do=True)
     outs = []
     for _ in range(2):
         _, _, (tq, tk, tv, o, lse) = run_fwd(fa, q, k, v, "bottom_right")
