@@ -625,8 +625,8 @@ def general_targets(fa, device, peaks, args):
         ("d=96 B=8 H=21 N=2048 non-causal", 8, 21, 21, 2048, 2048, 96, False, True),
         ("d=96 B=8 H=21 N=2048 causal", 8, 21, 21, 2048, 2048, 96, "top_left", True),
         ("d=96 B=4 H=21 N=4096 causal", 4, 21, 21, 4096, 4096, 96, "top_left", True),
-        ("d=256 B=4 H=8 N=4096 non-causal", 4, 8, 8, 4096, 4096, 256, False, False),
-        ("d=256 B=4 H=8 N=4096 causal", 4, 8, 8, 4096, 4096, 256, "top_left", False),
+        ("d=256 B=4 H=8 N=4096 non-causal", 4, 8, 8, 4096, 4096, 256, False, True),
+        ("d=256 B=4 H=8 N=4096 causal", 4, 8, 8, 4096, 4096, 256, "top_left", True),
         ("d=256 B=1 H=8 N=16384 causal", 1, 8, 8, 16384, 16384, 256, "top_left", False),
         ("decode GQA B=8 H=32 Hkv=8 Nq=1 Nk=8192 d=128 bottom-right", 8, 32, 8, 1, 8192, 128, "bottom_right", False),
         ("chunk B=1 H=32 Nq=1024 Nk=8192 d=128 bottom-right", 1, 32, 32, 1024, 8192, 128, "bottom_right", True),
