@@ -327,6 +327,18 @@ int fa_fwd_general(const void* q, const void* k, const void* v, void* o, float* 
   e = device_state(&s);
   if (e) return e;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int causal_off = causal_offset(causal, Nq, Nk);
+  // Grouped query heads with fewer than 128 query rows (decoding, short
+  // chunks): the G query heads of a key/value head share one tile as G * Nq
+  // rows -- the caller's contiguous [B, H, Nq, d] seen as [B, Hkv, G * Nq, d],
+  // so O and L land where they belong -- and K, V are read once per group.
+  // Row r of such a tile is query position r % Nq for the causal mask.
+  const int G = H / Hkv;
+  const bool pack = G > 1 && Nq < 128;
+  if (pack) {
+    H = Hkv;
+    Nq *= G;
+  }
   const int BH = B * H;
   // Work units: (batch*head, query block, key split).  A query block is 256
   // rows (two 128-row tiles) with 128-key tiles, or at d = 256 one 128-row
@@ -355,7 +367,8 @@ int fa_fwd_general(const void* q, const void* k, const void* v, void* o, float* 
   p.Nq = Nq;
   p.Nk = Nk;
   p.causal = causal != FA_CAUSAL_NONE ? 1 : 0;
-  p.causal_off = causal_offset(causal, Nq, Nk);
+  p.causal_off = causal_off;
+  p.q_period = pack ? Nq / G : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.num_splits = S;
   p.kv_tiles_per_split = per_split;

@@ -62,9 +62,25 @@ struct FwdParams {
   float* o_part;               // fp32 [S,B,H,Nq,d]         (num_splits > 1)
   float* lse_part;             // fp32 [S,B,H,Nq]           (num_splits > 1)
   int store32;                 // o is 32-byte aligned: 32-byte stores
+  // 0: row i of a head is query position i.  > 0: the query heads of a
+  // key/value group are packed as the rows of one head (the caller's
+  // [B, H, Nq, d] seen as [B, Hkv, G*Nq, d]) and row r is query position
+  // r % q_period (= Nq) for the causal mask.
+  int q_period;
   unsigned int* status;
   unsigned long long timeout_ns;
 };
+
+// Query position of row r (see FwdParams::q_period).
+__host__ __device__ inline int query_pos(int r, int q_period) { return q_period > 0 ? r % q_period : r; }
+
+// Largest query position among rows [r0, r1] (r0 <= r1).
+__host__ __device__ inline int max_query_pos(int r0, int r1, int q_period) {
+  if (q_period <= 0) return r1;
+  if (r1 - r0 + 1 >= q_period) return q_period - 1;
+  const int a = r0 % q_period, b = r1 % q_period;
+  return a <= b ? b : q_period - 1;
+}
 
 struct CombineParams {
   int rows;                    // B*H*Nq

@@ -116,7 +116,7 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
       int h = hi;
       if (p.causal) {
         // The last key any row of the tile sees; none if it is negative.
-        const int last_key = min(p.Nq, row0 + kTileM) - 1 + p.causal_off;
+        const int last_key = max_query_pos(row0, min(p.Nq, row0 + kTileM) - 1, p.q_period) + p.causal_off;
         h = last_key < 0 ? 0 : min(hi, last_key / kTileN + 1);
       }
       w.n[t] = max(0, h - lo);
@@ -384,9 +384,10 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
         for (int c = 0; c < kTileN; ++c) x[c] = __uint_as_float(s[c]);
         const int kv0 = (w.kvb + j) * kTileN;
-        const bool need_mask = (kv0 + kTileN > p.Nk) || (p.causal && kv0 + kTileN - 1 > row0 + p.causal_off);
+        const bool need_mask = (kv0 + kTileN > p.Nk) ||
+                               (p.causal && (p.q_period > 0 || kv0 + kTileN - 1 > row0 + p.causal_off));
         if (need_mask) {
-          const int lim = p.causal ? min(p.Nk - 1, row + p.causal_off) : p.Nk - 1;  // last visible key
+          const int lim = p.causal ? min(p.Nk - 1, query_pos(row, p.q_period) + p.causal_off) : p.Nk - 1;  // last visible key
 #pragma unroll
           for (int c = 0; c < kTileN; ++c)
             if (kv0 + c > lim) x[c] = -INFINITY;

@@ -76,7 +76,7 @@ __device__ __forceinline__ Unit decode(const FwdParams& p, int u) {
   w.kvb = lo;
   int h = hi;
   if (p.causal) {
-    const int last_key = min(p.Nq, w.row0 + kTileM) - 1 + p.causal_off;
+    const int last_key = max_query_pos(w.row0, min(p.Nq, w.row0 + kTileM) - 1, p.q_period) + p.causal_off;
     h = last_key < 0 ? 0 : min(hi, last_key / kKeys + 1);
   }
   w.n = max(0, h - lo);
@@ -302,8 +302,8 @@ __global__ void __launch_bounds__(d256::kThreads, 1)
 #pragma unroll
         for (int c = 0; c < kKeys; ++c) x[c] = __uint_as_float(s[c]);
         const int kv0 = (w.kvb + j) * kKeys;
-        if ((kv0 + kKeys > p.Nk) || (p.causal && kv0 + kKeys - 1 > w.row0 + p.causal_off)) {
-          const int lim = p.causal ? min(p.Nk - 1, row + p.causal_off) : p.Nk - 1;  // last visible key
+        if ((kv0 + kKeys > p.Nk) || (p.causal && (p.q_period > 0 || kv0 + kKeys - 1 > w.row0 + p.causal_off))) {
+          const int lim = p.causal ? min(p.Nk - 1, query_pos(row, p.q_period) + p.causal_off) : p.Nk - 1;  // last visible key
 #pragma unroll
           for (int c = 0; c < kKeys; ++c)
             if (kv0 + c > lim) x[c] = -INFINITY;

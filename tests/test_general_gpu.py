@@ -82,6 +82,9 @@ FWD_SHAPES = [
     # head dim 256 (its own kernel: one query tile per CTA, 64-key tiles)
     (1, 2, 2, 1, 8192, 256), (1, 2, 2, 128, 8192, 256), (1, 2, 2, 1000, 8192, 256),
     (1, 1, 1, 300, 100, 256), (2, 3, 3, 200, 200, 256), (1, 4, 2, 200, 700, 256), (1, 1, 1, 63, 63, 256),
+    # grouped query heads with fewer than 128 query rows: the heads of a group share a tile
+    (2, 8, 2, 1, 4096, 128), (1, 8, 2, 37, 1000, 64), (1, 32, 1, 3, 5000, 96), (1, 4, 1, 5, 3000, 256),
+    (1, 6, 2, 100, 60, 128), (2, 4, 2, 127, 129, 128),
 ]
 
 
@@ -135,6 +138,7 @@ BWD_SHAPES = [
     # head dim 256 (its own kernels: dV and dK passes over 64-row query steps, dQ over 64-key steps)
     (1, 1, 1, 1, 4096, 256), (1, 2, 2, 1000, 4096, 256), (1, 1, 1, 300, 100, 256), (2, 3, 3, 200, 200, 256),
     (1, 4, 2, 200, 700, 256), (1, 1, 1, 63, 63, 256), (1, 2, 2, 640, 640, 256),
+    (1, 8, 2, 37, 1000, 64), (1, 6, 2, 100, 60, 128),
 ]
 
 
