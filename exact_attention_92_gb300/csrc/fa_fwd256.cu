@@ -7,8 +7,9 @@
 // softmax with the tensor core across key tiles instead: S is double
 // buffered, and while the softmax warps turn S_j into P_j, the tensor core
 // runs O += P_{j-1} V_{j-1} and S_{j+1} = Q K_{j+1}^T.  Key/value tiles are
-// 64 rows (32 KB at d = 256) so that Q (64 KB) and a 4-slot K/V ring fit in
-// shared memory.  Roles (192 threads):
+// 64 rows (32 KB at d = 256) so that Q (64 KB) and a 5-slot K/V ring fit in
+// shared memory (224 KB); a 4-slot ring left too few tile loads in flight
+// for the load latency (measured 5-9% slower).  Roles (192 threads):
 //   warp 5     TMA producer: Q once per unit, then K_j, V_j alternately.
 //   warp 4     MMA issuer (whole warp, one elected lane issues):
 //              S_j = Q K_j^T (M128 N64, K = 256) into S buffer j & 1 and
@@ -40,7 +41,7 @@ constexpr int kQChunk = kTileM * 128;                  // 128 rows x 64 columns 
 constexpr int kKVChunk = kKeys * 128;                  // 64 rows x 64 columns
 constexpr int kQBytes = 4 * kQChunk;                   // 64 KB
 constexpr int kKVBytes = 4 * kKVChunk;                 // 32 KB
-constexpr int kStages = 4;                             // K/V ring slots
+constexpr int kStages = 5;                             // K/V ring slots (2.5 steps of lookahead)
 constexpr int kThreads = 192;
 constexpr uint32_t kColO = 256;
 constexpr uint32_t kTmemCols = 512;
