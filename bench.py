@@ -406,12 +406,12 @@ def run_ours(args, world, rank, local):
     return line
 
 
-def e2e_run(args, fa, case, device, stream, B, H, N, d, causal, flops, world):
+def e2e_run(args, fa, case, device, stream, B, H, N, d, causal, flops, world, nbuf=2):
     """Steps from pinned host memory to pinned host memory through the C ABI:
     every step copies Q, K, V, dO host -> device, runs fa_fwd + fa_bwd and
     copies dQ, dK, dV device -> host.  As a training input pipeline would,
-    the copies run on their own streams into double buffers, so the next
-    step's inputs and the previous step's gradients move while a step
+    the copies run on their own streams into ``nbuf`` sets of buffers, so the
+    next steps' inputs and the previous steps' gradients move while a step
     computes (CUDA events order each buffer's copy-in, compute and copy-out).
     The timed region covers all K steps' copies and compute."""
     import numpy as np
@@ -423,28 +423,28 @@ def e2e_run(args, fa, case, device, stream, B, H, N, d, causal, flops, world):
 
     shape = (B, H, N, d)
     h_in = [pinned(x) for x in (case.q, case.k, case.v, case.do)]
-    h_out = [[torch.empty(shape, dtype=torch.bfloat16).pin_memory() for _ in range(3)] for _ in range(2)]
-    d_in = [[torch.empty(shape, dtype=torch.bfloat16, device=device) for _ in range(4)] for _ in range(2)]
-    d_out = [[torch.empty(shape, dtype=torch.bfloat16, device=device) for _ in range(3)] for _ in range(2)]
-    o = [torch.empty(shape, dtype=torch.bfloat16, device=device) for _ in range(2)]
-    lse = [torch.empty(shape[:3], dtype=torch.float32, device=device) for _ in range(2)]
+    h_out = [[torch.empty(shape, dtype=torch.bfloat16).pin_memory() for _ in range(3)] for _ in range(nbuf)]
+    d_in = [[torch.empty(shape, dtype=torch.bfloat16, device=device) for _ in range(4)] for _ in range(nbuf)]
+    d_out = [[torch.empty(shape, dtype=torch.bfloat16, device=device) for _ in range(3)] for _ in range(nbuf)]
+    o = [torch.empty(shape, dtype=torch.bfloat16, device=device) for _ in range(nbuf)]
+    lse = [torch.empty(shape[:3], dtype=torch.float32, device=device) for _ in range(nbuf)]
     s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
-    copied_in = [torch.cuda.Event() for _ in range(2)]
-    computed = [torch.cuda.Event() for _ in range(2)]
-    copied_out = [torch.cuda.Event() for _ in range(2)]
-    used = [False, False]
+    copied_in = [torch.cuda.Event() for _ in range(nbuf)]
+    computed = [torch.cuda.Event() for _ in range(nbuf)]
+    copied_out = [torch.cuda.Event() for _ in range(nbuf)]
+    used = [False] * nbuf
 
     def step(i):
-        b = i & 1
+        b = i % nbuf
         with torch.cuda.stream(s_in):
             if used[b]:
-                s_in.wait_event(computed[b])  # step i-2 no longer reads these inputs
+                s_in.wait_event(computed[b])  # step i-nbuf no longer reads these inputs
             for dst, src in zip(d_in[b], h_in):
                 dst.copy_(src, non_blocking=True)
             copied_in[b].record(s_in)
         stream.wait_event(copied_in[b])
         if used[b]:
-            stream.wait_event(copied_out[b])  # step i-2's gradients have left these buffers
+            stream.wait_event(copied_out[b])  # step i-nbuf's gradients have left these buffers
         q, k, v, do = d_in[b]
         dq, dk, dv = d_out[b]
         fa.fa_fwd(q, k, v, o[b], lse[b], causal, stream=stream)
@@ -478,7 +478,7 @@ def e2e_run(args, fa, case, device, stream, B, H, N, d, causal, flops, world):
     return {"value": round(flops * world * n / (ms_max / 1e3) / 1e12, 2), "unit": "TFLOP/s",
             "h2d_bytes_per_step": 4 * elem, "d2h_bytes_per_step": 3 * elem,
             "ms_per_step": round(ms_max / n, 4),
-            "copies": "pinned host buffers; copy-in, compute and copy-out on three streams, double-buffered"}
+            "copies": f"pinned host buffers; copy-in, compute and copy-out on three streams, {nbuf} buffer sets"}
 
 
 def bwd_targets(fa, device, peaks, args):
