@@ -803,24 +803,30 @@ def run_profile(case):
         shape, causal = (4, 16, 1024, 64), False
     elif case == "splitkv":
         shape, causal = (1, 1, 65536, 128), True
-    elif case == "fwd256":
+    elif case in ("fwd256", "bwd256"):
         shape, causal = (4, 8, 4096, 256), True
+    elif case == "decode":
+        shape, causal = (8, 32, 1, 128), "bottom_right"
     else:
         w = WORKLOAD
         shape, causal = (w["B"], w["H"], w["N"], w["d"]), w["causal"]
     q, k, v, do = (torch.randn(shape, generator=g, device=dev).to(torch.bfloat16) for _ in range(4))
+    if case == "decode":  # one query row per head over 8192 keys of 8 key/value heads
+        k, v = (torch.randn((8, 8, 8192, 128), generator=g, device=dev).to(torch.bfloat16) for _ in range(2))
     if case == "fwd":  # the GPT layer's peaky logits: Q, K ~ N(0, 3^2)
         q, k = (q.float() * 3.0).to(torch.bfloat16), (k.float() * 3.0).to(torch.bfloat16)
     o = torch.empty_like(q)
     lse = torch.empty(shape[:3], dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
-    if case == "bwd":
+    if case in ("bwd", "bwd256"):
         fa.fa_fwd(q, k, v, o, lse, causal)
     for _ in range(3):
         if case in ("fwd", "fwd_short", "fwd256"):
             fa.fa_fwd_ex(q, k, v, o, lse, causal, None, 1)
         elif case == "splitkv":
             fa.fa_fwd(q, k, v, o, lse, causal)
+        elif case == "decode":
+            fa.fa_fwd_general(q, k, v, o, lse, causal)
         else:
             fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, causal)
     torch.cuda.synchronize()
@@ -896,7 +902,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true", help="skip the forward-only and backward-only target cases")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip timing the CPU oracle")
-    ap.add_argument("--profile", choices=["fwd", "fwd_short", "splitkv", "fwd256", "bwd"],
+    ap.add_argument("--profile", choices=["fwd", "fwd_short", "splitkv", "fwd256", "decode", "bwd", "bwd256"],
                     help="3 launches of one kernel (or of the split-KV forward and its merge), for ncu")
     args = ap.parse_args(argv)
     if args.profile:
