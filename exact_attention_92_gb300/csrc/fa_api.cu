@@ -48,6 +48,7 @@ struct DeviceState {
   std::mutex mu;
   bool ready = false;
   int sm_count = 0;
+  double l2_bytes = 0.0;
   unsigned int* status = nullptr;  // device address of g_fa_status_word
 };
 
@@ -92,6 +93,7 @@ int device_state(DeviceState** out) {
         return FA_ERR_CUDA;
       }
       s.sm_count = prop.multiProcessorCount;
+      s.l2_bytes = (double)prop.l2CacheSize;
       s.status = static_cast<unsigned int*>(addr);
       s.ready = true;
     }
@@ -377,6 +379,19 @@ int fa_fwd_general(const void* q, const void* k, const void* v, void* o, float* 
   p.o = o;
   p.lse = lse;
   p.store32 = (reinterpret_cast<uintptr_t>(o) & 31) == 0 ? 1 : 0;
+  // Without the causal mask every unit has the same work, so the units can
+  // be listed window by window of heads without losing balance: a window is
+  // the fewest heads whose query blocks fill one round of CTAs, and the K, V
+  // of the heads in flight then stay in L2.  Only when the K and V of all
+  // heads exceed half the L2 (otherwise they stay there anyway).
+  {
+    const double kv_bytes = 4.0 * (double)B * Hkv * Nk * d;
+    if (causal == FA_CAUSAL_NONE && S == 1 && kv_bytes > s->l2_bytes / 2) {
+      const int grid = p.num_units < s->sm_count ? p.num_units : s->sm_count;
+      const int win = (grid + qblocks - 1) / qblocks;
+      p.head_window = win < BH ? win : 0;
+    }
+  }
   p.status = s->status;
   p.timeout_ns = g_timeout_ns.load();
 

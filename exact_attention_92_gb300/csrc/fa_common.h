@@ -67,6 +67,11 @@ struct FwdParams {
   // [B, H, Nq, d] seen as [B, Hkv, G*Nq, d]) and row r is query position
   // r % q_period (= Nq) for the causal mask.
   int q_period;
+  // > 0: units are listed head window by head window (that many heads at a
+  // time, all of their query blocks) instead of query block by query block
+  // over all heads, so the K and V read by the CTAs in flight stay in L2.
+  // Used without the causal mask, where every unit has the same work.
+  int head_window;
   unsigned int* status;
   unsigned long long timeout_ns;
 };

@@ -97,10 +97,21 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
   const int split = u % p.num_splits;
   const int r = u / p.num_splits;
   const int BH = p.B * p.H;
-  w.bh = r % BH;
   // Query blocks in decreasing order: with the causal mask the last blocks
   // carry the most key tiles, so they start first (longest job first).
-  const int qb = p.num_q_blocks - 1 - r / BH;
+  // Without the mask, head windows (FwdParams::head_window).
+  int qb;
+  if (p.head_window > 0) {
+    const int per_window = p.head_window * p.num_q_blocks;
+    const int win = r / per_window;
+    const int heads = min(p.head_window, BH - win * p.head_window);
+    const int rr = r - win * per_window;
+    w.bh = win * p.head_window + rr % heads;
+    qb = p.num_q_blocks - 1 - rr / heads;
+  } else {
+    w.bh = r % BH;
+    qb = p.num_q_blocks - 1 - r / BH;
+  }
   w.q0 = qb * (kTileM * kQTilesPerCta);
   const int nkv = (p.Nk + kTileN - 1) / kTileN;
   const int lo = split * p.kv_tiles_per_split;

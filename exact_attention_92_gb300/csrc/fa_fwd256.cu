@@ -68,8 +68,18 @@ __device__ __forceinline__ Unit decode(const FwdParams& p, int u) {
   w.split = u % p.num_splits;
   const int r = u / p.num_splits;
   const int BH = p.B * p.H;
-  w.bh = r % BH;
-  const int qt = p.num_q_blocks - 1 - r / BH;
+  int qt;
+  if (p.head_window > 0) {  // see FwdParams::head_window
+    const int per_window = p.head_window * p.num_q_blocks;
+    const int win = r / per_window;
+    const int heads = min(p.head_window, BH - win * p.head_window);
+    const int rr = r - win * per_window;
+    w.bh = win * p.head_window + rr % heads;
+    qt = p.num_q_blocks - 1 - rr / heads;
+  } else {
+    w.bh = r % BH;
+    qt = p.num_q_blocks - 1 - r / BH;
+  }
   w.row0 = qt * kTileM;
   const int nkv = (p.Nk + kKeys - 1) / kKeys;
   const int lo = w.split * p.kv_tiles_per_split;
