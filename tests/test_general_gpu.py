@@ -138,7 +138,7 @@ BWD_SHAPES = [
     # head dim 256 (its own kernels: dV and dK passes over 64-row query steps, dQ over 64-key steps)
     (1, 1, 1, 1, 4096, 256), (1, 2, 2, 1000, 4096, 256), (1, 1, 1, 300, 100, 256), (2, 3, 3, 200, 200, 256),
     (1, 4, 2, 200, 700, 256), (1, 1, 1, 63, 63, 256), (1, 2, 2, 640, 640, 256),
-    (1, 8, 2, 37, 1000, 64), (1, 6, 2, 100, 60, 128),
+    (1, 8, 2, 37, 1000, 64), (1, 6, 2, 100, 60, 128), (1, 8, 2, 300, 1000, 256), (2, 4, 1, 70, 50, 256),
 ]
 
 
