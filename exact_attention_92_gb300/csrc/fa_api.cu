@@ -9,6 +9,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -105,6 +106,15 @@ int device_state(DeviceState** out) {
 }
 
 bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Stream-ordered workspace.  For failure-path tests, the environment variable
+// FA_TEST_FAIL_ALLOC (any value but "0") makes every workspace allocation
+// report failure without allocating.
+cudaError_t ws_alloc(void** ptr, size_t bytes, cudaStream_t st) {
+  const char* f = std::getenv("FA_TEST_FAIL_ALLOC");
+  if (f != nullptr && std::strcmp(f, "0") != 0) return cudaErrorMemoryAllocation;
+  return cudaMallocAsync(ptr, bytes, st);
+}
 
 // Head dims of the library: 64, 96, 128 and 256 (forward and backward).
 bool fwd_head_dim(int d) { return d == 64 || d == 96 || d == 128 || d == 256; }
@@ -399,7 +409,7 @@ int fa_fwd_general(const void* q, const void* k, const void* v, void* o, float* 
   const size_t rows = (size_t)BH * Nq;
   if (S > 1) {
     const size_t bytes = (size_t)S * rows * ((size_t)d + 1) * sizeof(float);
-    if (cudaMallocAsync(&ws, bytes, st) != cudaSuccess) {
+    if (ws_alloc(&ws, bytes, st) != cudaSuccess) {
       cudaGetLastError();
       return FA_ERR_NO_MEMORY;
     }
@@ -505,7 +515,7 @@ int fa_bwd_general(const void* q, const void* k, const void* v, const void* o, c
 
   // Workspace: D [rows].
   void* ws = nullptr;
-  if (cudaMallocAsync(&ws, rows * sizeof(float), st) != cudaSuccess) {
+  if (ws_alloc(&ws, rows * sizeof(float), st) != cudaSuccess) {
     cudaGetLastError();
     return FA_ERR_NO_MEMORY;
   }

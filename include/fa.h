@@ -31,7 +31,10 @@
  *    cudaMallocAsync on `stream` and returned with cudaFreeAsync on the same
  *    stream, so it is stream-ordered.
  *  - Return value: FA_OK, or an fa_status code.  Argument errors are detected
- *    on the host before anything is launched.  A device-side wait that gives
+ *    on the host before anything is launched.  A workspace allocation that
+ *    fails returns FA_ERR_NO_MEMORY before any launch (for tests of that
+ *    path, the environment variable FA_TEST_FAIL_ALLOC set to anything but
+ *    "0" makes every workspace allocation fail).  A device-side wait that gives
  *    up (see fa_set_wait_timeout_ns) is reported later by fa_poll_status.
  */
 #ifndef FA_GB300_H

@@ -9,7 +9,7 @@ from exact_attention_92_gb300 import inputs
 from oracle import attention as att
 
 from gpu_util import case_tensors, ensure_built, host, torch_cuda
-from parity import check_o
+from parity import check_grad, check_o
 
 pytestmark = pytest.mark.gpu
 
@@ -81,3 +81,27 @@ def test_launch_counter_without_events(fa):
     delta = [a - b for a, b in zip(after, before)]
     assert delta[fa.FA_KERNEL_FWD] == 1 and delta[fa.FA_KERNEL_COMBINE] == 0
     assert delta[fa.FA_KERNEL_BWD_PRE] == 1 and delta[fa.FA_KERNEL_BWD] == 1 and delta[fa.FA_KERNEL_BWD_DQ] == 1
+
+
+def test_workspace_allocation_failure_is_reported(fa, monkeypatch):
+    """A workspace allocation that fails (injected on the host with
+    FA_TEST_FAIL_ALLOC) is reported as FA_ERR_NO_MEMORY before any launch;
+    the stream and the device stay usable and the next call is correct."""
+    torch = torch_cuda()
+    case = inputs.make_case(1, 2, 512, 64, True, seed=5, with_do=True)
+    q, k, v, do = case_tensors(case)
+    o, lse = fa.forward(q, k, v, causal=True)
+    monkeypatch.setenv("FA_TEST_FAIL_ALLOC", "1")
+    with pytest.raises(fa.FaError) as e:
+        fa.backward(q, k, v, o, lse, do, causal=True)
+    assert e.value.status == fa.FA_ERR_NO_MEMORY
+    with pytest.raises(fa.FaError) as e:
+        fa.forward(q, k, v, causal=True, num_splits=2)  # split partials need workspace
+    assert e.value.status == fa.FA_ERR_NO_MEMORY
+    monkeypatch.delenv("FA_TEST_FAIL_ALLOC")
+    assert fa.fa_poll_status() == fa.FA_OK
+    dq, dk, dv = fa.backward(q, k, v, o, lse, do, causal=True)
+    assert fa.fa_poll_status() == fa.FA_OK
+    rq, rk, rv = att.backward(case.f64("q"), case.f64("k"), case.f64("v"), case.f64("do"), case.scale, True)
+    for name, g, r in (("dQ", dq, rq), ("dK", dk, rk), ("dV", dv, rv)):
+        check_grad(host(g), r, name, "after an allocation failure")
