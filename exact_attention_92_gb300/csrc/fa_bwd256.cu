@@ -68,7 +68,7 @@ struct KvCfg {
   static constexpr int kOffDO = kOffQ + kQStages * kStepBytes;
   static constexpr int kOffRv = kOffDO + kDoStages * kStepBytes;  // kRvStages x (64 L + 64 D) floats
   static constexpr int kOffBar = kOffRv + kRvStages * 2 * kStep * 4;
-  static constexpr int kNumBars = 4 + 2 * kQStages + 2 * kDoStages + 2 * kRvStages + 2 + 2 + 2 + 1;
+  static constexpr int kNumBars = 4 + 2 * kQStages + 2 * kDoStages + 2 * kRvStages + 2 + 2 + 2 + 2 + 1;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16;
   static_assert(kSmemBytes <= 232448, "shared memory");
 };
@@ -83,7 +83,7 @@ struct DqCfg {
   static constexpr int kOffK = 2 * kBigBytes;
   static constexpr int kOffV = kOffK + kKStages * kStepBytes;
   static constexpr int kOffBar = kOffV + kVStages * kStepBytes;
-  static constexpr int kNumBars = 4 + 2 * kKStages + 2 * kVStages + 2 + 2 + 2 + 1;
+  static constexpr int kNumBars = 4 + 2 * kKStages + 2 * kVStages + 2 + 2 + 2 + 2 + 1;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16;
   static_assert(kSmemBytes <= 232448, "shared memory");
 };
@@ -133,13 +133,19 @@ __device__ __forceinline__ DqUnit decode_dq(const BwdParams& p, int u) {
 }
 
 // S (or S^T) = A B^T over d = 256: A is a 128-row operand (chunks of
-// kChunkBig), B a 64-row one (chunks of kChunkStep), both K-major.
+// kChunkBig), B a 64-row one (chunks of kChunkStep), both K-major.  Each
+// MMA here is only 32 cycles of tensor work, so the issue cost counts: the
+// descriptors are built once and a K-step adds a constant to their low
+// halves (the start address field).
 __device__ __forceinline__ void issue_scores(uint32_t d_tmem, uint32_t a_base, uint32_t b_base) {
   constexpr uint32_t id = idesc_bf16(kBig, kStep, false, false);
+  constexpr uint32_t hi = sdesc_hi(1024);
+  const uint32_t a_lo = sdesc_lo(a_base, 16);
+  const uint32_t b_lo = sdesc_lo(b_base, 16);
 #pragma unroll
   for (int kk = 0; kk < kD / 16; ++kk)
-    mma_ss_w(d_tmem, sdesc_sw128(a_base + (kk / 4) * kChunkBig + (kk % 4) * 32, 16, 1024),
-             sdesc_sw128(b_base + (kk / 4) * kChunkStep + (kk % 4) * 32, 16, 1024), id, kk > 0 ? 1u : 0u);
+    mma_ss_lh_w(d_tmem, a_lo + (((kk / 4) * kChunkBig + (kk % 4) * 32) >> 4), hi,
+                b_lo + (((kk / 4) * kChunkStep + (kk % 4) * 32) >> 4), hi, id, kk > 0 ? 1u : 0u);
 }
 
 // acc (+)= X B: X packed bf16 in TMEM (128 rows x 64, 8 columns per 16),
@@ -147,10 +153,11 @@ __device__ __forceinline__ void issue_scores(uint32_t d_tmem, uint32_t a_base, u
 __device__ __forceinline__ void issue_accumulate(uint32_t acc_tmem, uint32_t x_tmem, uint32_t b_base,
                                                  bool accumulate) {
   constexpr uint32_t id = idesc_bf16(kBig, kD, false, true);
+  constexpr uint32_t hi = sdesc_hi(1024);
+  const uint32_t b_lo = sdesc_lo(b_base, kChunkStep);
 #pragma unroll
   for (int kk = 0; kk < kStep / 16; ++kk)
-    mma_ts_w(acc_tmem, x_tmem + kk * 8, sdesc_sw128(b_base + kk * 2048, kChunkStep, 1024), id,
-             (accumulate || kk > 0) ? 1u : 0u);
+    mma_ts_lh_w(acc_tmem, x_tmem + kk * 8, b_lo + ((kk * 2048) >> 4), hi, id, (accumulate || kk > 0) ? 1u : 0u);
 }
 
 }  // namespace b256
@@ -180,8 +187,9 @@ __global__ void __launch_bounds__(b256::kThreads, 1)
   uint64_t* do_empty = do_full + C::kDoStages;
   uint64_t* rv_full = do_empty + C::kDoStages;  // [kRvStages]: L (and D) of a query step
   uint64_t* rv_empty = rv_full + C::kRvStages;
-  uint64_t* s_full = rv_empty + C::kRvStages;  // [2]: scores of region r computed
-  uint64_t* p_ready = s_full + 2;              // [2]: packed operand of region r written
+  uint64_t* s_full = rv_empty + C::kRvStages;  // [2]: S^T of region r computed
+  uint64_t* dp_full = s_full + 2;              // [2]: dP^T of region r computed (dK pass)
+  uint64_t* p_ready = dp_full + 2;             // [2]: packed operand of region r written
   uint64_t* acc_full = p_ready + 2;            // the unit's accumulator complete
   uint64_t* acc_empty = acc_full + 1;          // ... and read out
   uint64_t* drain = acc_empty + 1;
@@ -210,6 +218,7 @@ __global__ void __launch_bounds__(b256::kThreads, 1)
     }
     for (int r = 0; r < 2; ++r) {
       mbar_init(&s_full[r], 1);
+      mbar_init(&dp_full[r], 1);
       mbar_init(&p_ready[r], 4);
     }
     mbar_init(acc_full, 1);
@@ -238,6 +247,10 @@ __global__ void __launch_bounds__(b256::kThreads, 1)
 
   if (warp == 5) {
     // ------------------------------------------------------------ producer
+    // Per step: the Q and dO copies first, then the step's L and D values
+    // (read from global memory into registers before the copies are
+    // issued, stored to the ring after), so the copies never wait behind
+    // those reads.
     uint32_t kc = 0, qc = 0;
     bool ok = true;
     for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units_kv; ++rnd) {
@@ -269,27 +282,18 @@ __global__ void __launch_bounds__(b256::kThreads, 1)
         const int row = qt * kStep;
         const size_t head = (size_t)qh * p.Nq;
         // L (log2 units; rows past Nq and rows that see no key get +inf, so
-        // their weights vanish) and D of the step, then the arrive that
-        // publishes them.
-        const uint32_t sr = qc % C::kRvStages;
-        ok = wait_all(&rv_empty[sr], ((qc / C::kRvStages) & 1) ^ 1, kWaitBwdLoad);
-        if (!ok) break;
+        // their weights vanish) and D of the step.
+        float2 l2, d2 = make_float2(0.f, 0.f);
         {
-          float2 l2, d2 = make_float2(0.f, 0.f);
           float* lp = &l2.x;
           float* dp = &d2.x;
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int qr = row + 2 * lane + e;
-            const float L = qr < p.Nq ? p.lse[head + qr] : INFINITY;
-            lp[e] = L == -INFINITY ? INFINITY : L * 1.4426950408889634f;
+            lp[e] = qr < p.Nq ? p.lse[head + qr] : INFINITY;
             if (DK) dp[e] = qr < p.Nq ? p.dvec[head + qr] : 0.f;
           }
-          reinterpret_cast<float2*>(sRv + sr * 2 * kStep)[lane] = l2;
-          reinterpret_cast<float2*>(sRv + sr * 2 * kStep + kStep)[lane] = d2;
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&rv_full[sr]);
         const uint32_t sq = qc % C::kQStages;
         ok = wait_all(&q_empty[sq], ((qc / C::kQStages) & 1) ^ 1, kWaitBwdLoad);
         if (!ok) break;
@@ -306,6 +310,16 @@ __global__ void __launch_bounds__(b256::kThreads, 1)
           for (int c = 0; c < 4; ++c)
             tma_load_3d(smem + C::kOffDO + sd * kStepBytes + c * kChunkStep, &tm_do, &do_full[sd], c * 64, row, qh);
         }
+        // The values, then the arrive that publishes them.
+        const uint32_t sr = qc % C::kRvStages;
+        ok = wait_all(&rv_empty[sr], ((qc / C::kRvStages) & 1) ^ 1, kWaitBwdLoad);
+        if (!ok) break;
+        l2.x = l2.x == -INFINITY ? INFINITY : l2.x * 1.4426950408889634f;
+        l2.y = l2.y == -INFINITY ? INFINITY : l2.y * 1.4426950408889634f;
+        reinterpret_cast<float2*>(sRv + sr * 2 * kStep)[lane] = l2;
+        reinterpret_cast<float2*>(sRv + sr * 2 * kStep + kStep)[lane] = d2;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&rv_full[sr]);
       }
       ++kc;
     }
@@ -334,6 +348,8 @@ __global__ void __launch_bounds__(b256::kThreads, 1)
     auto accumulate = [&](uint32_t g) -> bool {
       if (!wait_all(&p_ready[g & 1], (g >> 1) & 1, kWaitBwdMma)) return false;
       if (pend_first && pend_un > 0 && !wait_all(acc_empty, (pend_un - 1) & 1, kWaitBwdMma)) return false;
+      // dV pass: dO of step g is read by this accumulation only.
+      if (!DK && !wait_all(&do_full[g % C::kDoStages], (g / C::kDoStages) & 1, kWaitBwdMma)) return false;
       tc_fence_after();
       const uint32_t region = tmem + 128u * (g & 1);
       if constexpr (DK) {
@@ -358,37 +374,33 @@ __global__ void __launch_bounds__(b256::kThreads, 1)
       }
       const KvUnit w = decode_kv(p, u);
       ok = wait_all(k_full, un & 1, kWaitBwdMma);
-      if (ok && DK) ok = wait_all(v_full, un & 1, kWaitBwdMma);
       for (int ii = 0; ok && ii < w.count; ++ii, ++g) {
-        // Scores of step g into region g & 1 (its previous contents, step
-        // g - 2, were read by an accumulation issued earlier).
+        // Step g: S^T into region g & 1 (its previous contents, step g - 2,
+        // were read by an accumulation issued earlier), the accumulation of
+        // step g - 1, then (dK pass) dP^T.  With the accumulation ahead of
+        // dP^T, the Q tile of step g - 1 (read by S^T and by dK) is released
+        // one product earlier, and its slot reloads while dP^T runs.
         ok = wait_all(&q_full[g % C::kQStages], (g / C::kQStages) & 1, kWaitBwdMma);
         if (!ok) break;
         tc_fence_after();
         const uint32_t region = tmem + 128u * (g & 1);
-        issue_scores(region, sk, q_addr(g));  // S^T = K Q^T
+        issue_scores(region, sk, q_addr(g));                      // S^T = K Q^T
+        if (!DK) mma_commit_w(&q_empty[g % C::kQStages]);        // dV pass: Q read by S^T only
+        mma_commit_w(&s_full[g & 1]);
+        if (ii + 1 == w.count) mma_commit_w(k_empty);             // K: read by S^T only
+        if (pend) {
+          ok = accumulate(g - 1);
+          if (!ok) break;
+        }
         if constexpr (DK) {
-          ok = wait_all(&do_full[g % C::kDoStages], (g / C::kDoStages) & 1, kWaitBwdMma);
+          if (ii == 0) ok = wait_all(v_full, un & 1, kWaitBwdMma);
+          if (ok) ok = wait_all(&do_full[g % C::kDoStages], (g / C::kDoStages) & 1, kWaitBwdMma);
           if (!ok) break;
           tc_fence_after();
           issue_scores(region + 64, sv, do_addr(g));  // dP^T = V dO^T
           mma_commit_w(&do_empty[g % C::kDoStages]);  // dO: read by dP^T only
-        } else {
-          mma_commit_w(&q_empty[g % C::kQStages]);  // Q: read by S^T only
-        }
-        mma_commit_w(&s_full[g & 1]);
-        if (ii + 1 == w.count) {
-          mma_commit_w(k_empty);  // K: read by S^T only
-          if (DK) mma_commit_w(v_empty);
-        }
-        if constexpr (!DK) {
-          // dO of step g is needed by its accumulation, issued next round.
-          ok = wait_all(&do_full[g % C::kDoStages], (g / C::kDoStages) & 1, kWaitBwdMma);
-          if (!ok) break;
-        }
-        if (pend) {
-          ok = accumulate(g - 1);
-          if (!ok) break;
+          mma_commit_w(&dp_full[g & 1]);
+          if (ii + 1 == w.count) mma_commit_w(v_empty);
         }
         pend = true;
         pend_first = ii == 0;
@@ -457,8 +469,10 @@ __global__ void __launch_bounds__(b256::kThreads, 1)
         }
         uint32_t pk[32];
         if constexpr (DK) {
-          // dS^T = P^T * (dP^T - D), packed over this step's dP^T columns
-          // (computed by the same product commit as S^T).
+          // dS^T = P^T * (dP^T - D), packed over this step's dP^T columns.
+          ok = wait_all(&dp_full[g & 1], (g >> 1) & 1, kWaitBwdSoftmax);
+          if (!ok) break;
+          tc_fence_after();
           uint32_t dpv[64];
           tmem_ld32(tR + 64, dpv);
           tmem_ld32(tR + 96, dpv + 32);
@@ -530,8 +544,9 @@ __global__ void __launch_bounds__(b256::kThreads, 1)
   uint64_t* k_empty = k_full + C::kKStages;
   uint64_t* v_full = k_empty + C::kKStages;  // [kVStages]
   uint64_t* v_empty = v_full + C::kVStages;
-  uint64_t* s_full = v_empty + C::kVStages;  // [2]: S and dP of region r computed
-  uint64_t* p_ready = s_full + 2;            // [2]: dS of region r written
+  uint64_t* s_full = v_empty + C::kVStages;  // [2]: S of region r computed
+  uint64_t* dp_full = s_full + 2;            // [2]: dP of region r computed
+  uint64_t* p_ready = dp_full + 2;           // [2]: dS of region r written
   uint64_t* acc_full = p_ready + 2;
   uint64_t* acc_empty = acc_full + 1;
   uint64_t* drain = acc_empty + 1;
@@ -555,6 +570,7 @@ __global__ void __launch_bounds__(b256::kThreads, 1)
     }
     for (int r = 0; r < 2; ++r) {
       mbar_init(&s_full[r], 1);
+      mbar_init(&dp_full[r], 1);
       mbar_init(&p_ready[r], 4);
     }
     mbar_init(acc_full, 1);
@@ -655,23 +671,28 @@ __global__ void __launch_bounds__(b256::kThreads, 1)
       const DqUnit w = decode_dq(p, u);
       ok = wait_all(q_full, un & 1, kWaitBwdMma) && wait_all(do_full, un & 1, kWaitBwdMma);
       for (int jj = 0; ok && jj < w.count; ++jj, ++g) {
-        ok = wait_all(&k_full[g % C::kKStages], (g / C::kKStages) & 1, kWaitBwdMma) &&
-             wait_all(&v_full[g % C::kVStages], (g / C::kVStages) & 1, kWaitBwdMma);
+        // Step g: S, the accumulation of step g - 1, then dP.  With the
+        // accumulation ahead of dP, the K tile of step g - 1 (read by S and
+        // by dQ) is released one product earlier, and its slot reloads while
+        // dP runs.
+        ok = wait_all(&k_full[g % C::kKStages], (g / C::kKStages) & 1, kWaitBwdMma);
         if (!ok) break;
         tc_fence_after();
         const uint32_t region = tmem + 128u * (g & 1);
-        issue_scores(region, sq, k_addr(g));        // S = Q K^T
-        issue_scores(region + 64, sdo, v_addr(g));  // dP = dO V^T
-        mma_commit_w(&v_empty[g % C::kVStages]);    // V: read by dP only
+        issue_scores(region, sq, k_addr(g));  // S = Q K^T
         mma_commit_w(&s_full[g & 1]);
-        if (jj + 1 == w.count) {
-          mma_commit_w(q_empty);
-          mma_commit_w(do_empty);
-        }
+        if (jj + 1 == w.count) mma_commit_w(q_empty);
         if (pend) {
           ok = accumulate(g - 1);
           if (!ok) break;
         }
+        ok = wait_all(&v_full[g % C::kVStages], (g / C::kVStages) & 1, kWaitBwdMma);
+        if (!ok) break;
+        tc_fence_after();
+        issue_scores(region + 64, sdo, v_addr(g));  // dP = dO V^T
+        mma_commit_w(&v_empty[g % C::kVStages]);    // V: read by dP only
+        mma_commit_w(&dp_full[g & 1]);
+        if (jj + 1 == w.count) mma_commit_w(do_empty);
         pend = true;
         pend_first = jj == 0;
         pend_last = jj + 1 == w.count;
@@ -726,14 +747,17 @@ __global__ void __launch_bounds__(b256::kThreads, 1)
         uint32_t pv[64], dpv[64];
         tmem_ld32(tR, pv);
         tmem_ld32(tR + 32, pv + 32);
-        tmem_ld32(tR + 64, dpv);
-        tmem_ld32(tR + 96, dpv + 32);
         tmem_ld_wait<64>(pv);
-        tmem_ld_wait<64>(dpv);
         if (k_first + kStep - 1 >= p.Nk || (p.causal && k_first + kStep - 1 > q_lo + p.causal_off))
           p64_rowL<true>(pv, L, sl2, q + p.causal_off, k_first, p.Nk, p.causal != 0);
         else
           p64_rowL<false>(pv, L, sl2, q, k_first, p.Nk, false);
+        ok = wait_all(&dp_full[g & 1], (g >> 1) & 1, kWaitBwdSoftmax);
+        if (!ok) break;
+        tc_fence_after();
+        tmem_ld32(tR + 64, dpv);
+        tmem_ld32(tR + 96, dpv + 32);
+        tmem_ld_wait<64>(dpv);
         uint32_t pk[32];
         const float2 dv2 = make_float2(-Dq, -Dq);
 #pragma unroll
