@@ -274,6 +274,19 @@ __global__ void __launch_bounds__(384, 1)
         }
         const int row = qt * kTileM;
         const size_t head = (size_t)qh * p.Nq;
+        // L_i and D_i of the step, read from global memory before the waits
+        // below so that the reads overlap them instead of delaying the copies.
+        float4 l4, d4;
+        {
+          float* lp = &l4.x;
+          float* dp = &d4.x;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int qr = row + 4 * lane + e;
+            lp[e] = qr < p.Nq ? p.lse[head + qr] : INFINITY;
+            dp[e] = qr < p.Nq ? p.dvec[head + qr] : 0.f;
+          }
+        }
         // Q_i with L_i (log2 units; rows past Nq and rows that see no key
         // get +inf so their weights vanish).  The values are written before
         // the arrive that completes the stage together with the copy.
@@ -281,14 +294,9 @@ __global__ void __launch_bounds__(384, 1)
         ok = __all_sync(0xffffffffu, mbar_wait(&q_empty[sq], ((qc / C::kQStages) & 1) ^ 1, ctl, kWaitBwdLoad));
         if (!ok) break;
         {
-          float4 l4;
           float* lp = &l4.x;
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int qr = row + 4 * lane + e;
-            const float L = qr < p.Nq ? p.lse[head + qr] : INFINITY;
-            lp[e] = L == -INFINITY ? INFINITY : L * 1.4426950408889634f;
-          }
+          for (int e = 0; e < 4; ++e) lp[e] = lp[e] == -INFINITY ? INFINITY : lp[e] * 1.4426950408889634f;
           reinterpret_cast<float4*>(sLse + sq * 128)[lane] = l4;
         }
         __syncwarp();
@@ -302,16 +310,7 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t sd = qc % C::kDoStages;
         ok = __all_sync(0xffffffffu, mbar_wait(&do_empty[sd], ((qc / C::kDoStages) & 1) ^ 1, ctl, kWaitBwdLoad));
         if (!ok) break;
-        {
-          float4 d4;
-          float* dp = &d4.x;
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int qr = row + 4 * lane + e;
-            dp[e] = qr < p.Nq ? p.dvec[head + qr] : 0.f;
-          }
-          reinterpret_cast<float4*>(sDv + sd * 128)[lane] = d4;
-        }
+        reinterpret_cast<float4*>(sDv + sd * 128)[lane] = d4;
         __syncwarp();
         if (lane == 0) {
           mbar_arrive_expect_tx(&do_full[sd], C::kTileBytes);
