@@ -252,6 +252,7 @@ __global__ void __launch_bounds__(b256::kThreads, 1)
     // issued, stored to the ring after), so the copies never wait behind
     // those reads.
     uint32_t kc = 0, qc = 0;
+    uint32_t q_issued = 0, do_issued = 0, k_issued = 0, v_issued = 0;  // copies started (for the drain)
     bool ok = true;
     for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units_kv; ++rnd) {
       const int u = snake_unit(rnd);
@@ -263,6 +264,7 @@ __global__ void __launch_bounds__(b256::kThreads, 1)
         mbar_arrive_expect_tx(k_full, kBigBytes);
         for (int c = 0; c < 4; ++c) tma_load_3d(smem + C::kOffK + c * kChunkBig, &tm_k, k_full, c * 64, w.t * kBig, w.kvbh);
       }
+      ++k_issued;
       if constexpr (DK) {
         ok = wait_all(v_empty, (kc & 1) ^ 1, kWaitBwdLoad);
         if (!ok) break;
@@ -271,15 +273,34 @@ __global__ void __launch_bounds__(b256::kThreads, 1)
           for (int c = 0; c < 4; ++c)
             tma_load_3d(smem + C::kOffV + c * kChunkBig, &tm_v, v_full, c * 64, w.t * kBig, w.kvbh);
         }
+        ++v_issued;
       }
-      int qh = GQA ? q_head_of(w.kvbh, 0, p.H, p.Hkv) : w.kvbh;
-      int qt = w.first;
-      for (int ii = 0; ok && ii < w.count; ++ii, ++qc) {
-        if (ii > 0 && ++qt == w.first + w.per) {  // next query head of the group
-          qt = w.first;
-          ++qh;
+      // Step ii reads query rows [row, row + kStep) of query head qh.
+      auto step_pos = [&](int ii, int& qh, int& row) {
+        const int grp = ii / w.per;  // query head of the group
+        qh = GQA ? q_head_of(w.kvbh, 0, p.H, p.Hkv) + grp : w.kvbh;
+        row = (w.first + ii - grp * w.per) * kStep;
+      };
+      // Q of step ii into ring position pos.
+      auto load_q = [&](int ii, uint32_t pos) -> bool {
+        int qh, row;
+        step_pos(ii, qh, row);
+        const uint32_t sq = pos % C::kQStages;
+        if (!wait_all(&q_empty[sq], ((pos / C::kQStages) & 1) ^ 1, kWaitBwdLoad)) return false;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&q_full[sq], kStepBytes);
+          for (int c = 0; c < 4; ++c)
+            tma_load_3d(smem + C::kOffQ + sq * kStepBytes + c * kChunkStep, &tm_q, &q_full[sq], c * 64, row, qh);
         }
-        const int row = qt * kStep;
+        ++q_issued;
+        return true;
+      };
+      // dV pass: a Q slot frees when its S^T completes, a dO slot only when
+      // its accumulation does, so Q runs a step ahead of dO.
+      if (!DK) ok = load_q(0, qc);
+      for (int ii = 0; ok && ii < w.count; ++ii, ++qc) {
+        int qh, row;
+        step_pos(ii, qh, row);
         const size_t head = (size_t)qh * p.Nq;
         // L (log2 units; rows past Nq and rows that see no key get +inf, so
         // their weights vanish) and D of the step.
@@ -294,14 +315,8 @@ __global__ void __launch_bounds__(b256::kThreads, 1)
             if (DK) dp[e] = qr < p.Nq ? p.dvec[head + qr] : 0.f;
           }
         }
-        const uint32_t sq = qc % C::kQStages;
-        ok = wait_all(&q_empty[sq], ((qc / C::kQStages) & 1) ^ 1, kWaitBwdLoad);
+        if (DK || ii + 1 < w.count) ok = load_q(DK ? ii : ii + 1, DK ? qc : qc + 1);
         if (!ok) break;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&q_full[sq], kStepBytes);
-          for (int c = 0; c < 4; ++c)
-            tma_load_3d(smem + C::kOffQ + sq * kStepBytes + c * kChunkStep, &tm_q, &q_full[sq], c * 64, row, qh);
-        }
         const uint32_t sd = qc % C::kDoStages;
         ok = wait_all(&do_empty[sd], ((qc / C::kDoStages) & 1) ^ 1, kWaitBwdLoad);
         if (!ok) break;
@@ -310,6 +325,7 @@ __global__ void __launch_bounds__(b256::kThreads, 1)
           for (int c = 0; c < 4; ++c)
             tma_load_3d(smem + C::kOffDO + sd * kStepBytes + c * kChunkStep, &tm_do, &do_full[sd], c * 64, row, qh);
         }
+        ++do_issued;
         // The values, then the arrive that publishes them.
         const uint32_t sr = qc % C::kRvStages;
         ok = wait_all(&rv_empty[sr], ((qc / C::kRvStages) & 1) ^ 1, kWaitBwdLoad);
@@ -325,13 +341,11 @@ __global__ void __launch_bounds__(b256::kThreads, 1)
     }
     if (lane == 0) {
       // Every copy this warp started lands before the CTA can exit.
-      if (kc > 0) {
-        mbar_wait(k_full, (kc - 1) & 1, ctl, kWaitDrain);
-        if (DK) mbar_wait(v_full, (kc - 1) & 1, ctl, kWaitDrain);
-      }
-      for (uint32_t pos = qc > (uint32_t)C::kQStages ? qc - C::kQStages : 0u; pos < qc; ++pos)
+      if (k_issued > 0) mbar_wait(k_full, (k_issued - 1) & 1, ctl, kWaitDrain);
+      if (v_issued > 0) mbar_wait(v_full, (v_issued - 1) & 1, ctl, kWaitDrain);
+      for (uint32_t pos = q_issued > (uint32_t)C::kQStages ? q_issued - C::kQStages : 0u; pos < q_issued; ++pos)
         mbar_wait(&q_full[pos % C::kQStages], (pos / C::kQStages) & 1, ctl, kWaitDrain);
-      for (uint32_t pos = qc > (uint32_t)C::kDoStages ? qc - C::kDoStages : 0u; pos < qc; ++pos)
+      for (uint32_t pos = do_issued > (uint32_t)C::kDoStages ? do_issued - C::kDoStages : 0u; pos < do_issued; ++pos)
         mbar_wait(&do_full[pos % C::kDoStages], (pos / C::kDoStages) & 1, ctl, kWaitDrain);
     }
     __syncwarp();
@@ -601,6 +615,7 @@ __global__ void __launch_bounds__(b256::kThreads, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t uc = 0, kc = 0;
+      uint32_t q_issued = 0, do_issued = 0, k_issued = 0, v_issued = 0;  // copies started (for the drain)
       bool ok = true;
       for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units; ++rnd) {
         const int u = snake_unit(rnd);
@@ -611,11 +626,13 @@ __global__ void __launch_bounds__(b256::kThreads, 1)
         if (!ok) break;
         mbar_arrive_expect_tx(q_full, kBigBytes);
         for (int c = 0; c < 4; ++c) tma_load_3d(smem + C::kOffQ + c * kChunkBig, &tm_q, q_full, c * 64, w.t * kBig, w.bh);
+        ++q_issued;
         ok = mbar_wait(do_empty, (uc & 1) ^ 1, ctl, kWaitBwdLoad);
         if (!ok) break;
         mbar_arrive_expect_tx(do_full, kBigBytes);
         for (int c = 0; c < 4; ++c)
           tma_load_3d(smem + C::kOffDO + c * kChunkBig, &tm_do, do_full, c * 64, w.t * kBig, w.bh);
+        ++do_issued;
         for (int jj = 0; ok && jj < w.count; ++jj, ++kc) {
           const int key0 = jj * kStep;
           const uint32_t sk = kc % C::kKStages;
@@ -624,22 +641,22 @@ __global__ void __launch_bounds__(b256::kThreads, 1)
           mbar_arrive_expect_tx(&k_full[sk], kStepBytes);
           for (int c = 0; c < 4; ++c)
             tma_load_3d(smem + C::kOffK + sk * kStepBytes + c * kChunkStep, &tm_k, &k_full[sk], c * 64, key0, kvbh);
+          ++k_issued;
           const uint32_t sv = kc % C::kVStages;
           ok = mbar_wait(&v_empty[sv], ((kc / C::kVStages) & 1) ^ 1, ctl, kWaitBwdLoad);
           if (!ok) break;
           mbar_arrive_expect_tx(&v_full[sv], kStepBytes);
           for (int c = 0; c < 4; ++c)
             tma_load_3d(smem + C::kOffV + sv * kStepBytes + c * kChunkStep, &tm_v, &v_full[sv], c * 64, key0, kvbh);
+          ++v_issued;
         }
         ++uc;
       }
-      if (uc > 0) {
-        mbar_wait(q_full, (uc - 1) & 1, ctl, kWaitDrain);
-        mbar_wait(do_full, (uc - 1) & 1, ctl, kWaitDrain);
-      }
-      for (uint32_t pos = kc > (uint32_t)C::kKStages ? kc - C::kKStages : 0u; pos < kc; ++pos)
+      if (q_issued > 0) mbar_wait(q_full, (q_issued - 1) & 1, ctl, kWaitDrain);
+      if (do_issued > 0) mbar_wait(do_full, (do_issued - 1) & 1, ctl, kWaitDrain);
+      for (uint32_t pos = k_issued > (uint32_t)C::kKStages ? k_issued - C::kKStages : 0u; pos < k_issued; ++pos)
         mbar_wait(&k_full[pos % C::kKStages], (pos / C::kKStages) & 1, ctl, kWaitDrain);
-      for (uint32_t pos = kc > (uint32_t)C::kVStages ? kc - C::kVStages : 0u; pos < kc; ++pos)
+      for (uint32_t pos = v_issued > (uint32_t)C::kVStages ? v_issued - C::kVStages : 0u; pos < v_issued; ++pos)
         mbar_wait(&v_full[pos % C::kVStages], (pos / C::kVStages) & 1, ctl, kWaitDrain);
     }
     __syncwarp();
