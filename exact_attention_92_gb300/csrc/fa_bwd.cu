@@ -247,6 +247,7 @@ __global__ void __launch_bounds__(384, 1)
     // ------------------------------------------------------------ producer
     reg_dealloc<R::kRegsCtl>();
     uint32_t kc = 0, qc = 0;
+    uint32_t k_issued = 0, v_issued = 0, q_issued = 0, do_issued = 0;  // copies started (for the drain)
     bool ok = true;
     for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units_kv; ++rnd) {
       const int u = snake_unit(rnd);
@@ -259,6 +260,7 @@ __global__ void __launch_bounds__(384, 1)
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_3d(smem + C::kOffK + c * C::kChunkBytes, &tm_k, k_full, c * 64, w.t * kTileN, w.bh);
       }
+      ++k_issued;
       // Step ii: query tile first + ii % per of the (ii / per)-th query head
       // that reads this key/value head (with GQA, kept as running counters).
       int qh = GQA ? q_head_of(w.bh, 0, p.H, p.Hkv) : w.bh;
@@ -306,6 +308,7 @@ __global__ void __launch_bounds__(384, 1)
             tma_load_3d(smem + C::kOffQ + sq * C::kTileBytes + c * C::kChunkBytes, &tm_q, &q_full[sq], c * 64,
                         row, qh);
         }
+        ++q_issued;
         // dO_i with D_i.
         const uint32_t sd = qc % C::kDoStages;
         ok = __all_sync(0xffffffffu, mbar_wait(&do_empty[sd], ((qc / C::kDoStages) & 1) ^ 1, ctl, kWaitBwdLoad));
@@ -318,6 +321,7 @@ __global__ void __launch_bounds__(384, 1)
             tma_load_3d(smem + C::kOffDO + sd * C::kTileBytes + c * C::kChunkBytes, &tm_do, &do_full[sd],
                         c * 64, row, qh);
         }
+        ++do_issued;
         if (ii == 0) {
           // V_j, needed by the first dP^T, after the first step's Q and dO.
           ok = __all_sync(0xffffffffu, mbar_wait(v_empty, (kc & 1) ^ 1, ctl, kWaitBwdLoad));
@@ -327,19 +331,18 @@ __global__ void __launch_bounds__(384, 1)
             for (int c = 0; c < C::kChunks; ++c)
               tma_load_3d(smem + C::kOffV + c * C::kChunkBytes, &tm_v, v_full, c * 64, w.t * kTileN, w.bh);
           }
+          ++v_issued;
         }
       }
       ++kc;
     }
     if (lane == 0) {
       // Every copy this warp issued has landed before the CTA exits.
-      if (kc > 0) {
-        mbar_wait(k_full, (kc - 1) & 1, ctl, kWaitDrain);
-        mbar_wait(v_full, (kc - 1) & 1, ctl, kWaitDrain);
-      }
-      for (uint32_t pos = qc > (uint32_t)C::kQStages ? qc - C::kQStages : 0u; pos < qc; ++pos)
+      if (k_issued > 0) mbar_wait(k_full, (k_issued - 1) & 1, ctl, kWaitDrain);
+      if (v_issued > 0) mbar_wait(v_full, (v_issued - 1) & 1, ctl, kWaitDrain);
+      for (uint32_t pos = q_issued > (uint32_t)C::kQStages ? q_issued - C::kQStages : 0u; pos < q_issued; ++pos)
         mbar_wait(&q_full[pos % C::kQStages], (pos / C::kQStages) & 1, ctl, kWaitDrain);
-      for (uint32_t pos = qc > (uint32_t)C::kDoStages ? qc - C::kDoStages : 0u; pos < qc; ++pos)
+      for (uint32_t pos = do_issued > (uint32_t)C::kDoStages ? do_issued - C::kDoStages : 0u; pos < do_issued; ++pos)
         mbar_wait(&do_full[pos % C::kDoStages], (pos / C::kDoStages) & 1, ctl, kWaitDrain);
     }
     __syncwarp();
@@ -750,6 +753,7 @@ __global__ void __launch_bounds__(384, 1)
     reg_dealloc<R::kRegsCtl>();
     if (lane == 0) {
       uint32_t uc = 0, kc = 0;
+      uint32_t q_issued = 0, do_issued = 0, k_issued = 0, v_issued = 0;  // copies started (for the drain)
       bool ok = true;
       for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units; ++rnd) {
         const int u = snake_unit(rnd);
@@ -761,6 +765,7 @@ __global__ void __launch_bounds__(384, 1)
         mbar_arrive_expect_tx(q_full, C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_3d(smem + C::kOffQ + c * C::kChunkBytes, &tm_q, q_full, c * 64, w.t * kTileM, w.bh);
+        ++q_issued;
         for (int jj = 0; ok && jj < w.count; ++jj, ++kc) {
           const int key0 = (w.first + jj) * kTileN;
           const uint32_t sk = kc % C::kKStages;
@@ -770,6 +775,7 @@ __global__ void __launch_bounds__(384, 1)
           for (int c = 0; c < C::kChunks; ++c)
             tma_load_3d(smem + C::kOffK + sk * C::kTileBytes + c * C::kChunkBytes, &tm_k, &k_full[sk], c * 64, key0,
                         kvbh);
+          ++k_issued;
           if (jj == 0) {
             // dO_i, needed by the first dP, after the first K.
             ok = mbar_wait(do_empty, (uc & 1) ^ 1, ctl, kWaitBwdLoad);
@@ -777,6 +783,7 @@ __global__ void __launch_bounds__(384, 1)
             mbar_arrive_expect_tx(do_full, C::kTileBytes);
             for (int c = 0; c < C::kChunks; ++c)
               tma_load_3d(smem + C::kOffDO + c * C::kChunkBytes, &tm_do, do_full, c * 64, w.t * kTileM, w.bh);
+            ++do_issued;
           }
           const uint32_t sv = kc % C::kVStages;
           ok = mbar_wait(&v_empty[sv], ((kc / C::kVStages) & 1) ^ 1, ctl, kWaitBwdLoad);
@@ -785,17 +792,16 @@ __global__ void __launch_bounds__(384, 1)
           for (int c = 0; c < C::kChunks; ++c)
             tma_load_3d(smem + C::kOffV + sv * C::kTileBytes + c * C::kChunkBytes, &tm_v, &v_full[sv], c * 64, key0,
                         kvbh);
+          ++v_issued;
         }
         ++uc;
       }
       // Every copy this thread issued has landed before the CTA exits.
-      if (uc > 0) {
-        mbar_wait(q_full, (uc - 1) & 1, ctl, kWaitDrain);
-        mbar_wait(do_full, (uc - 1) & 1, ctl, kWaitDrain);
-      }
-      for (uint32_t pos = kc > (uint32_t)C::kKStages ? kc - C::kKStages : 0u; pos < kc; ++pos)
+      if (q_issued > 0) mbar_wait(q_full, (q_issued - 1) & 1, ctl, kWaitDrain);
+      if (do_issued > 0) mbar_wait(do_full, (do_issued - 1) & 1, ctl, kWaitDrain);
+      for (uint32_t pos = k_issued > (uint32_t)C::kKStages ? k_issued - C::kKStages : 0u; pos < k_issued; ++pos)
         mbar_wait(&k_full[pos % C::kKStages], (pos / C::kKStages) & 1, ctl, kWaitDrain);
-      for (uint32_t pos = kc > (uint32_t)C::kVStages ? kc - C::kVStages : 0u; pos < kc; ++pos)
+      for (uint32_t pos = v_issued > (uint32_t)C::kVStages ? v_issued - C::kVStages : 0u; pos < v_issued; ++pos)
         mbar_wait(&v_full[pos % C::kVStages], (pos / C::kVStages) & 1, ctl, kWaitDrain);
     }
     __syncwarp();
