@@ -23,7 +23,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfa.so")
 
-SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_fwd256.cu", "fa_bwd.cu", "fa_bwd256.cu", "fa_noalloc.cu"]
+SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_fwd256.cu", "fa_bwd.cu", "fa_bwd_pair.cu", "fa_bwd256.cu", "fa_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -47,15 +47,16 @@ def _deps():
 # Kernels that read tensor memory with tcgen05.ld: the destination registers
 # of such a load are only valid after tcgen05.wait::ld, so a register spill
 # between the two would store garbage.  The build refuses any spill in them.
-NO_SPILL_KERNELS = ("fa_fwd_kernel", "fa_fwd256_kernel", "fa_bwd_dkdv_kernel", "fa_bwd_dq_kernel",
-                    "fa_bwd256_kv_kernel", "fa_bwd256_dq_kernel")
+NO_SPILL_KERNELS = ("fa_fwd_kernel", "fa_fwd256_kernel", "fa_bwd_dkdv_kernel", "fa_bwd_dkdv_pair_kernel",
+                    "fa_bwd_dq_kernel", "fa_bwd256_kv_kernel", "fa_bwd256_dq_kernel")
 
 
 # Kernels that move registers between warpgroups with setmaxnreg, and the
 # per-thread count they must be launched with.  The split's shares are
 # static_asserted against this count in the source; if ptxas gave the entry
 # fewer registers, the warpgroup that asks for more would wait forever.
-REG_SPLIT_KERNELS = {"fa_fwd_kernel": 168, "fa_bwd_dkdv_kernel": 168, "fa_bwd_dq_kernel": 168}
+REG_SPLIT_KERNELS = {"fa_fwd_kernel": 168, "fa_bwd_dkdv_kernel": 168, "fa_bwd_dkdv_pair_kernel": 168,
+                     "fa_bwd_dq_kernel": 168}
 
 
 def check_spills(ptxas_log: str) -> None:

@@ -1,7 +1,8 @@
-// Element-wise pieces of the backward kernels (fa_bwd.cu, fa_bwd256.cu):
-// recomputing the softmax weights P (section 7.1 of "FlashAttention V2 in
-// depth") from the saved logsumexp over 64 columns held in registers, and
-// reading an fp32 accumulator out of tensor memory as packed bf16.
+// Element-wise pieces of the backward kernels (fa_bwd.cu, fa_bwd_pair.cu,
+// fa_bwd256.cu): recomputing the softmax weights P (section 7.1 of
+// "FlashAttention V2 in depth") from the saved logsumexp over 64 columns
+// held in registers, reading an fp32 accumulator out of tensor memory as
+// packed bf16, and where a 128-column tile's packed bf16 lands in TMEM.
 #pragma once
 
 #include "sm103_primitives.cuh"
@@ -9,6 +10,14 @@
 namespace fa {
 
 using namespace dev;
+
+// Packed column of the 16 columns [16 kk, 16 kk + 16) of a bf16 tile written
+// by the element-wise warps of the 128-column kernels: warp half h holds
+// columns [64 h, 64 h + 64) as bf16 pairs in [64 h, 64 h + 32) of its region
+// (second = true: in [64 h + 32, 64 h + 64)).
+__device__ __forceinline__ uint32_t packed_col(int kk, bool second) {
+  return 64u * (kk >> 2) + (second ? 32u : 0u) + 8u * (kk & 3);
+}
 
 // Rows of 32 consecutive TMEM columns, NC columns from `taddr`, scaled and
 // packed to bf16 pairs into w[NC / 2].

@@ -28,6 +28,9 @@ cudaError_t launch_bwd256_dq(const CUtensorMap& tq, const CUtensorMap& tk, const
                              const CUtensorMap& tdo, const BwdParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const BwdParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_bwd_dkdv_pair(const CUtensorMap& tq64, const CUtensorMap& tq, const CUtensorMap& tk,
+                                 const CUtensorMap& tv, const CUtensorMap& tdo64, const CUtensorMap& tdo,
+                                 const BwdParams& p, int sm_count, cudaStream_t stream);
 cudaError_t launch_bwd_dq(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tdo, const BwdParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_bwd_preprocess(int d, const void* o, const void* dout, float* dvec, int rows,
@@ -230,8 +233,8 @@ int internal_device_setup(unsigned int** status, int* sm_count) {
   return FA_OK;
 }
 int internal_validate(int B, int H, int N, int d, float scale) { return validate(B, H, N, N, d, scale, true); }
-int internal_encode_bhnd(CUtensorMap* m, const void* ptr, int BH, int N, int d) {
-  return encode_bhnd(m, ptr, BH, N, d);
+int internal_encode_bhnd(CUtensorMap* m, const void* ptr, int BH, int N, int d, int box_rows) {
+  return encode_bhnd(m, ptr, BH, N, d, box_rows);
 }
 unsigned long long internal_wait_timeout_ns() { return g_timeout_ns.load(); }
 // A launch of library kernel `kernel` by another file of the library, counted
@@ -468,14 +471,18 @@ int fa_bwd_general(const void* q, const void* k, const void* v, const void* o, c
   const size_t rows = (size_t)BH * Nq;
 
   // Tensor maps: 128-row boxes; at d = 256 also 64-row ones (the query steps
-  // of the key/value kernel, the key steps of the dQ kernel).
+  // of the key/value kernel, the key steps of the dQ kernel), at d = 128
+  // 64-row ones of Q and dO (each CTA's half of a query tile in the CTA-pair
+  // dK/dV kernel).
   const bool wide = d == 256;
+  const bool pair = d == 128;
   CUtensorMap tq, tk, tv, tdo, tq64, tk64, tv64, tdo64;
   if (encode_bhnd(&tq, q, BH, Nq, d) || encode_bhnd(&tk, k, B * Hkv, Nk, d) ||
       encode_bhnd(&tv, v, B * Hkv, Nk, d) || encode_bhnd(&tdo, dout, BH, Nq, d))
     return FA_ERR_CUDA;
-  if (wide && (encode_bhnd(&tq64, q, BH, Nq, d, 64) || encode_bhnd(&tk64, k, B * Hkv, Nk, d, 64) ||
-               encode_bhnd(&tv64, v, B * Hkv, Nk, d, 64) || encode_bhnd(&tdo64, dout, BH, Nq, d, 64)))
+  if ((wide || pair) && (encode_bhnd(&tq64, q, BH, Nq, d, 64) || encode_bhnd(&tdo64, dout, BH, Nq, d, 64)))
+    return FA_ERR_CUDA;
+  if (wide && (encode_bhnd(&tk64, k, B * Hkv, Nk, d, 64) || encode_bhnd(&tv64, v, B * Hkv, Nk, d, 64)))
     return FA_ERR_CUDA;
 
   fa::BwdParams p;
@@ -541,7 +548,10 @@ int fa_bwd_general(const void* q, const void* k, const void* v, const void* o, c
     ce = timed(FA_KERNEL_BWD_PRE, st, [&] { return fa::launch_bwd_preprocess(d, o, dout, dvec, (int)rows, st); });
   if (!wide) {
     if (ce == cudaSuccess)
-      ce = timed(FA_KERNEL_BWD, st, [&] { return fa::launch_bwd_dkdv(d, tq, tk, tv, tdo, p, grid_kv, st); });
+      ce = timed(FA_KERNEL_BWD, st, [&] {
+        return pair ? fa::launch_bwd_dkdv_pair(tq64, tq, tk, tv, tdo64, tdo, p, s->sm_count, st)
+                    : fa::launch_bwd_dkdv(d, tq, tk, tv, tdo, p, grid_kv, st);
+      });
     if (ce == cudaSuccess)
       ce = timed(FA_KERNEL_BWD_DQ, st, [&] { return fa::launch_bwd_dq(d, tq, tk, tv, tdo, p, grid_q, st); });
   } else {

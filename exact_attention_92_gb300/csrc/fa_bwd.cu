@@ -107,14 +107,6 @@ struct DkdvCfg {
   static_assert(kSmemBytes <= 232448, "shared memory");
 };
 
-// Packed column of the 16 columns [16 kk, 16 kk + 16) of a bf16 tile written
-// by the element-wise warps: warp half h holds columns [64 h, 64 h + 64) as
-// bf16 pairs in [64 h, 64 h + 32) of its region (second = true: in
-// [64 h + 32, 64 h + 64)).
-__device__ __forceinline__ uint32_t packed_col(int kk, bool second) {
-  return 64u * (kk >> 2) + (second ? 32u : 0u) + 8u * (kk & 3);
-}
-
 struct BwdUnit {
   int bh;     // the head: key/value head (dK/dV kernel), query head (dQ kernel)
   int t;      // the tile this CTA owns (key tile / query tile)

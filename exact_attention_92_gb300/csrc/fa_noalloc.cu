@@ -19,11 +19,14 @@ static __device__ __align__(256) unsigned char g_fa_bwd_scratch[FA_BWD_NOALLOC_S
 namespace fa {
 int internal_device_setup(unsigned int** status, int* sm_count);
 int internal_validate(int B, int H, int N, int d, float scale);
-int internal_encode_bhnd(CUtensorMap* m, const void* ptr, int BH, int N, int d);
+int internal_encode_bhnd(CUtensorMap* m, const void* ptr, int BH, int N, int d, int box_rows);
 unsigned long long internal_wait_timeout_ns();
 cudaError_t internal_timed_launch(int kernel, cudaStream_t stream, cudaError_t (*launch)(void*), void* ctx);
 cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const BwdParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_bwd_dkdv_pair(const CUtensorMap& tq64, const CUtensorMap& tq, const CUtensorMap& tk,
+                                 const CUtensorMap& tv, const CUtensorMap& tdo64, const CUtensorMap& tdo,
+                                 const BwdParams& p, int sm_count, cudaStream_t stream);
 cudaError_t launch_bwd_dq(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tdo, const BwdParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_bwd_preprocess(int d, const void* o, const void* dout, float* dvec, int rows,
@@ -69,9 +72,10 @@ struct Launch {
   const void* dout;
   float* dvec;
   int rows;
-  const CUtensorMap *tq, *tk, *tv, *tdo;
+  const CUtensorMap *tq, *tk, *tv, *tdo, *tq64, *tdo64;
   const fa::BwdParams* p;
   int grid;
+  int sm_count;
   cudaStream_t st;
 };
 cudaError_t run_pre(void* c) {
@@ -80,6 +84,8 @@ cudaError_t run_pre(void* c) {
 }
 cudaError_t run_dkdv(void* c) {
   const Launch& l = *static_cast<const Launch*>(c);
+  // Head dim 128: the CTA-pair kernel, as in fa_bwd_general.
+  if (l.d == 128) return fa::launch_bwd_dkdv_pair(*l.tq64, *l.tq, *l.tk, *l.tv, *l.tdo64, *l.tdo, *l.p, l.sm_count, l.st);
   return fa::launch_bwd_dkdv(l.d, *l.tq, *l.tk, *l.tv, *l.tdo, *l.p, l.grid, l.st);
 }
 cudaError_t run_dq(void* c) {
@@ -113,9 +119,11 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int BH = B * H;
 
-  CUtensorMap tq, tk, tv, tdo;
-  if (fa::internal_encode_bhnd(&tq, q, BH, N, d) || fa::internal_encode_bhnd(&tk, k, BH, N, d) ||
-      fa::internal_encode_bhnd(&tv, v, BH, N, d) || fa::internal_encode_bhnd(&tdo, dout, BH, N, d))
+  CUtensorMap tq, tk, tv, tdo, tq64, tdo64;
+  if (fa::internal_encode_bhnd(&tq, q, BH, N, d, 128) || fa::internal_encode_bhnd(&tk, k, BH, N, d, 128) ||
+      fa::internal_encode_bhnd(&tv, v, BH, N, d, 128) || fa::internal_encode_bhnd(&tdo, dout, BH, N, d, 128))
+    return FA_ERR_CUDA;
+  if (d == 128 && (fa::internal_encode_bhnd(&tq64, q, BH, N, d, 64) || fa::internal_encode_bhnd(&tdo64, dout, BH, N, d, 64)))
     return FA_ERR_CUDA;
 
   // Scratch layout: D [rows] fp32, every entry written by the preprocess
@@ -151,7 +159,7 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
   p.timeout_ns = fa::internal_wait_timeout_ns();
 
   const int grid = p.num_units < sm_count ? p.num_units : sm_count;
-  Launch l{d, o, dout, dvec, (int)rows, &tq, &tk, &tv, &tdo, &p, grid, st};
+  Launch l{d, o, dout, dvec, (int)rows, &tq, &tk, &tv, &tdo, &tq64, &tdo64, &p, grid, sm_count, st};
   cudaError_t ce = fa::internal_timed_launch(FA_KERNEL_BWD_PRE, st, run_pre, &l);
   if (ce == cudaSuccess) ce = fa::internal_timed_launch(FA_KERNEL_BWD, st, run_dkdv, &l);
   if (ce == cudaSuccess) ce = fa::internal_timed_launch(FA_KERNEL_BWD_DQ, st, run_dq, &l);
