@@ -39,7 +39,10 @@ WORKLOAD = dict(B=2, H=16, N=4096, d=128, causal=True)
 STEP_WORKLOAD = "fwd+bwd B=2 H=16 N=4096 d=128 causal"
 L2_FLUSH_BYTES = 256 << 20  # twice the 129 MB L2
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNEL_NAMES = ["fa_fwd_kernel", "fa_combine_kernel", "fa_bwd_preprocess", "fa_bwd_dkdv_kernel", "fa_bwd_dq_kernel"]
+# The library's launch counters by id (FA_KERNEL_*), named for the kernels
+# that id launches at head dim 128: the dK/dV id runs the CTA-pair kernel.
+KERNEL_NAMES = ["fa_fwd_kernel", "fa_combine_kernel", "fa_bwd_preprocess", "fa_bwd_dkdv_pair_kernel",
+                "fa_bwd_dq_kernel"]
 
 
 def workload_flops(B, H, N, d, causal):
@@ -64,6 +67,7 @@ KERNEL_SOURCES = {
     "fa_fwd256_kernel": ["fa_fwd256.cu", "sm103_primitives.cuh", "fa_common.h"],
     "fa_combine_kernel": ["fa_fwd.cu", "sm103_primitives.cuh", "fa_common.h"],
     "fa_bwd_dkdv_kernel": ["fa_bwd.cu", "bwd_elementwise.cuh", "sm103_primitives.cuh", "fa_common.h"],
+    "fa_bwd_dkdv_pair_kernel": ["fa_bwd_pair.cu", "bwd_elementwise.cuh", "sm103_primitives.cuh", "fa_common.h"],
     "fa_bwd_preprocess": ["fa_bwd.cu", "bwd_elementwise.cuh", "sm103_primitives.cuh", "fa_common.h"],
     "fa_bwd_dq_kernel": ["fa_bwd.cu", "bwd_elementwise.cuh", "sm103_primitives.cuh", "fa_common.h"],
 }
@@ -339,7 +343,7 @@ def run_ours(args, world, rank, local):
     # Algorithmic FLOPs per kernel: the backward's 2.5 F splits into the
     # dK/dV kernel's S, dP, dV and dK products (2 F) and the dQ product
     # (0.5 F); the dQ kernel's recomputed S and dP are not counted.
-    dom_flops = {"fa_fwd_kernel": f, "fa_bwd_dkdv_kernel": 0.8 * b, "fa_bwd_dq_kernel": 0.2 * b}.get(dom)
+    dom_flops = {"fa_fwd_kernel": f, "fa_bwd_dkdv_pair_kernel": 0.8 * b, "fa_bwd_dq_kernel": 0.2 * b}.get(dom)
     peaks, peak_src = load_peaks()
     roofline = None
     if dom_flops is not None:

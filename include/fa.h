@@ -245,7 +245,8 @@ int fa_selftest_wait_timeout(uint64_t timeout_ns, void* stream);
  * kernel is bracketed by two CUDA events recorded on the launch's stream.
  * Kernel ids: FA_KERNEL_FWD (forward main kernel), FA_KERNEL_COMBINE
  * (split-KV merge), FA_KERNEL_BWD_PRE (D preprocess), FA_KERNEL_BWD
- * (backward dK/dV kernel), FA_KERNEL_BWD_DQ (backward dQ kernel).
+ * (backward dK/dV kernel; at head dim 128 the CTA-pair kernel),
+ * FA_KERNEL_BWD_DQ (backward dQ kernel).
  *   fa_timing_enable(on) : 1 starts recording (and drops old records), 0 stops.
  *   fa_timing_read(kernel, launches, total_ms) : waits for the recorded
  *       events of that kernel, returns how many launches were recorded and
