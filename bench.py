@@ -67,7 +67,8 @@ KERNEL_SOURCES = {
     "fa_fwd256_kernel": ["fa_fwd256.cu", "sm103_primitives.cuh", "fa_common.h"],
     "fa_combine_kernel": ["fa_fwd.cu", "sm103_primitives.cuh", "fa_common.h"],
     "fa_bwd_dkdv_kernel": ["fa_bwd.cu", "bwd_elementwise.cuh", "sm103_primitives.cuh", "fa_common.h"],
-    "fa_bwd_dkdv_pair_kernel": ["fa_bwd_pair.cu", "bwd_elementwise.cuh", "sm103_primitives.cuh", "fa_common.h"],
+    "fa_bwd_dkdv_pair_kernel": ["fa_bwd_pair.cu", "bwd_elementwise.cuh", "sm103_pair.cuh", "sm103_primitives.cuh",
+                                "fa_common.h"],
     "fa_bwd_preprocess": ["fa_bwd.cu", "bwd_elementwise.cuh", "sm103_primitives.cuh", "fa_common.h"],
     "fa_bwd_dq_kernel": ["fa_bwd.cu", "bwd_elementwise.cuh", "sm103_primitives.cuh", "fa_common.h"],
 }
