@@ -139,6 +139,9 @@ BWD_SHAPES = [
     (1, 1, 1, 1, 4096, 256), (1, 2, 2, 1000, 4096, 256), (1, 1, 1, 300, 100, 256), (2, 3, 3, 200, 200, 256),
     (1, 4, 2, 200, 700, 256), (1, 1, 1, 63, 63, 256), (1, 2, 2, 640, 640, 256),
     (1, 8, 2, 37, 1000, 64), (1, 6, 2, 100, 60, 128), (1, 8, 2, 300, 1000, 256), (2, 4, 1, 70, 50, 256),
+    # head dim 128, whose dK/dV run on CTA pairs (two neighbouring key tiles a unit): an odd number of key
+    # tiles (the last pair's second tile past Nk), grouped heads, more query rows than keys
+    (1, 2, 2, 640, 640, 128), (1, 4, 2, 200, 700, 128), (1, 2, 2, 700, 389, 128), (2, 3, 3, 257, 513, 128),
 ]
 
 

@@ -36,7 +36,8 @@ def _call_noalloc(lib, q, k, v, o, lse, do, dq, dk, dv, causal, scale, stream):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("shape,causal", [((2, 4, 1000, 128), True), ((1, 8, 640, 64), False), ((1, 3, 333, 96), True)])
+@pytest.mark.parametrize("shape,causal", [((2, 4, 1000, 128), True), ((1, 2, 640, 128), False), ((1, 8, 640, 64), False),
+                                          ((1, 3, 333, 96), True)])
 def test_noalloc_matches_fa_bwd_on_two_calls(shape, causal):
     torch = torch_cuda()
     fa = ensure_built()
