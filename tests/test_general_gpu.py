@@ -85,6 +85,9 @@ FWD_SHAPES = [
     # grouped query heads with fewer than 128 query rows: the heads of a group share a tile
     (2, 8, 2, 1, 4096, 128), (1, 8, 2, 37, 1000, 64), (1, 32, 1, 3, 5000, 96), (1, 4, 1, 5, 3000, 256),
     (1, 6, 2, 100, 60, 128), (2, 4, 2, 127, 129, 128),
+    # a few rows per key/value head (decoding steps), grouped and not: 2 x 4, 5, 3, 8 x 1, 8 rows
+    (1, 8, 2, 2, 3000, 64), (1, 1, 1, 5, 700, 128), (3, 4, 4, 3, 1000, 64), (1, 16, 2, 1, 257, 128),
+    (2, 2, 2, 8, 33, 128),
 ]
 
 
