@@ -110,6 +110,43 @@ int device_state(DeviceState** out) {
 
 bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Number of key splits with the causal mask (no packed query heads, query
+// blocks of q_block rows over key tiles of key_tile keys): units then carry
+// unequal work -- the key tiles their last row sees -- and the longest-first
+// order balances them, so the count is chosen on an estimate of the
+// slowest SM's load in key-tile steps:
+//   max(the largest unit split S ways, the average load per SM, plus 2% a
+//   split for the extra units) + the split partials' traffic (written by
+//   the forward, read by the merge: about half a step per MB at head dim
+//   128, measured on B=1 H=1..4 N=16K..64K).
+int choose_splits_causal(long long BH, int qblocks, int q_block, int key_tile, int Nq, int nkv, int causal_off,
+                         int d, int min_tiles, int sm_count) {
+  long long total = 0;
+  int max1 = 0;
+  for (int qb = 0; qb < qblocks; ++qb) {
+    const int last_key = std::min(Nq, (qb + 1) * q_block) - 1 + causal_off;
+    const int n = last_key < 0 ? 0 : std::min(nkv, last_key / key_tile + 1);
+    total += n;
+    max1 = std::max(max1, n);
+  }
+  const double avg = (double)(total * BH) / sm_count;
+  const double rows = (double)BH * Nq;
+  int best_s = 1;
+  double best = std::max((double)max1, avg);
+  // Powers of two only: with 3 splits the unit list's mix of long and short
+  // splits broke the longest-first deal (measured 30% slower than 2 or 4).
+  for (int s = 2; s <= 16; s *= 2) {
+    if (nkv / s < min_tiles) break;
+    const double load = std::max((double)((max1 + s - 1) / s), avg * (1.0 + 0.02 * (s - 1)));
+    const double cost = load + 0.5e-6 * s * rows * d * 4.0;
+    if (cost < best) {
+      best = cost;
+      best_s = s;
+    }
+  }
+  return best_s;
+}
+
 // Stream-ordered workspace.  For failure-path tests, the environment variable
 // FA_TEST_FAIL_ALLOC (any value but "0") makes every workspace allocation
 // report failure without allocating.
@@ -363,7 +400,12 @@ int fa_fwd_general(const void* q, const void* k, const void* v, void* o, float* 
   const int key_tile = wide ? 64 : 128;
   const int nkv = (Nk + key_tile - 1) / key_tile;
   const int qblocks = (Nq + q_block - 1) / q_block;
-  int S = num_splits == 0 ? choose_splits((long long)BH * qblocks, nkv, wide ? 8 : 4, s->sm_count) : num_splits;
+  int S = num_splits;
+  if (S == 0) {
+    S = choose_splits((long long)BH * qblocks, nkv, wide ? 8 : 4, s->sm_count);
+    if (S > 1 && causal != FA_CAUSAL_NONE && !pack && !wide)
+      S = choose_splits_causal(BH, qblocks, q_block, key_tile, Nq, nkv, causal_off, d, 4, s->sm_count);
+  }
   if (S > nkv) S = nkv;
   if (S < 1) S = 1;
   const int per_split = (nkv + S - 1) / S;
