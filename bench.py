@@ -786,7 +786,8 @@ def run_profile(case):
     """Two warm-up launches, then one launch, of the forward kernel on the GPT
     layer (B=8 H=32 N=4096 d=128 causal), on B=4 H=16 N=1024 d=64
     non-causal (``fwd_short``, 33.6 MB: the DRAM figures there are those of
-    a problem below the L2 size) or on B=4 H=8 N=4096 d=256 causal
+    a problem below the L2 size), on B=4 H=32 N=4096 d=64 non-causal
+    (``fwd64``, 268 MB) or on B=4 H=8 N=4096 d=256 causal
     (``fwd256``); of the split-KV forward and its merge on one head of 65536
     tokens (``splitkv``); or of the backward on the fwd+bwd workload; for
     ``ncu -s 2 -c 1`` captures."""
@@ -806,6 +807,8 @@ def run_profile(case):
         shape, causal = (8, 32, 4096, 128), True
     elif case == "fwd_short":
         shape, causal = (4, 16, 1024, 64), False
+    elif case == "fwd64":
+        shape, causal = (4, 32, 4096, 64), False
     elif case == "splitkv":
         shape, causal = (1, 1, 65536, 128), True
     elif case in ("fwd256", "bwd256"):
@@ -826,7 +829,7 @@ def run_profile(case):
     if case in ("bwd", "bwd256"):
         fa.fa_fwd(q, k, v, o, lse, causal)
     for _ in range(3):
-        if case in ("fwd", "fwd_short", "fwd256"):
+        if case in ("fwd", "fwd_short", "fwd64", "fwd256"):
             fa.fa_fwd_ex(q, k, v, o, lse, causal, None, 1)
         elif case == "splitkv":
             fa.fa_fwd(q, k, v, o, lse, causal)
@@ -907,7 +910,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true", help="skip the forward-only and backward-only target cases")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip timing the CPU oracle")
-    ap.add_argument("--profile", choices=["fwd", "fwd_short", "splitkv", "fwd256", "decode", "bwd", "bwd256"],
+    ap.add_argument("--profile", choices=["fwd", "fwd_short", "fwd64", "splitkv", "fwd256", "decode", "bwd", "bwd256"],
                     help="3 launches of one kernel (or of the split-KV forward and its merge), for ncu")
     args = ap.parse_args(argv)
     if args.profile:

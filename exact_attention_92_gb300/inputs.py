@@ -21,6 +21,12 @@ algorithm, "FlashAttention V2 in depth", section 6):
 * ``identical_keys``: every key of a head equals that head's key row 0.
 * ``dominant_key``: one key row j* (drawn from [0, N/4)) is multiplied by 50
   after bf16 rounding and rounded to bf16 again.
+* ``rising_keys``: 1 is added to every query component and j / (4 sqrt(d))
+  to every component of key row j before the bf16 rounding, so a query's
+  logits grow by about a quarter per key (some 46 in log2 units per 128
+  keys): each new key tile raises every row's running maximum by far more
+  than any correction threshold, and the running output must be rescaled
+  at every tile.
 """
 
 from __future__ import annotations
@@ -102,8 +108,13 @@ def make_case(
 ) -> Case:
     rng = np.random.default_rng(seed)
     shape = (B, H, N, d)
-    q = normal_bits(rng, shape, q_std)
-    k = normal_bits(rng, shape, k_std)
+    if degenerate == "rising_keys":
+        q = bf16_bits(rng.standard_normal(size=shape, dtype=np.float32) * np.float32(q_std) + np.float32(1.0))
+        ramp = (np.arange(N, dtype=np.float32) / np.float32(4.0 * np.sqrt(d)))[:, None]
+        k = bf16_bits(rng.standard_normal(size=shape, dtype=np.float32) * np.float32(k_std) + ramp)
+    else:
+        q = normal_bits(rng, shape, q_std)
+        k = normal_bits(rng, shape, k_std)
     v = normal_bits(rng, shape, v_std)
     do = normal_bits(rng, shape, 1.0) if with_do else None
     jstar = None
@@ -114,7 +125,7 @@ def make_case(
         row = bits_to_f32(k[:, :, jstar, :]) * np.float32(50.0)
         k = k.copy()
         k[:, :, jstar, :] = bf16_bits(row)
-    elif degenerate is not None:
+    elif degenerate is not None and degenerate != "rising_keys":
         raise ValueError(f"unknown degenerate case {degenerate!r}")
     return Case(B, H, N, d, causal, seed, q, k, v, do, jstar)
 

@@ -124,6 +124,21 @@ def test_b4_h16_n1024_d64(fa, c):
         assert checked > 0
 
 
+@pytest.mark.parametrize("d", [64, 96, 128, 256])
+@pytest.mark.parametrize("causal", [False, True])
+def test_rising_keys_rescale_every_tile(fa, d, causal):
+    """Logits that climb by some 46 log2 units per 128-key tile: every row's
+    running maximum moves past the correction threshold at every key tile,
+    so the O~ correction (and, at d=64, its wait for the tile's previous
+    P V product) runs at every step ("FlashAttention V2 in depth" 6.1)."""
+    case = inputs.make_case(2, 3, 1000, d, causal, seed=70 + d + int(causal), degenerate="rising_keys")
+    q, k = case.f64("q"), case.f64("k")
+    s = case.scale * np.einsum("bhc,bhmc->bhm", q[:, :, -1], k)  # logits of the last query row
+    tile_max = s[..., :896].reshape(2, 3, 7, 128).max(-1)
+    assert np.all(np.diff(tile_max, axis=-1) * np.log2(np.e) > 24.0)
+    check_full(fa, case, what=f"rising keys d{d} causal{int(causal)}")
+
+
 SWEEP = inputs.workload_cases()[3]
 
 
