@@ -359,11 +359,25 @@ def run_ours(args, world, rank, local):
     # C ABI, gradients -> pinned host, every step.
     e2e = e2e_run(args, fa, case, device, stream, B, H, N, d, causal, f + b, world)
 
-    extra = fwd_targets(fa, device, peaks, args) if (rank == 0 and not args.no_extra) else None
-    extra_bwd = bwd_targets(fa, device, peaks, args) if (rank == 0 and not args.no_extra) else None
-    extra_gqa = gqa_targets(fa, device, peaks, args) if (rank == 0 and not args.no_extra) else None
-    extra_short = short_targets(fa, device, peaks, args) if (rank == 0 and not args.no_extra) else None
-    extra_general = general_targets(fa, device, peaks, args) if (rank == 0 and not args.no_extra) else None
+    # Secondary workloads, each with its own clock record (they follow one
+    # another without pauses, so a power-capped stretch shows up here).
+    target_clocks = {}
+
+    def sampled(name, fn):
+        if rank != 0 or args.no_extra:
+            return None
+        cs = ClockSampler(local)
+        cs.start()
+        try:
+            return fn(fa, device, peaks, args)
+        finally:
+            target_clocks[name] = cs.stop()
+
+    extra = sampled("fwd_targets", fwd_targets)
+    extra_bwd = sampled("bwd_targets", bwd_targets)
+    extra_gqa = sampled("gqa_targets", gqa_targets)
+    extra_short = sampled("short_targets", short_targets)
+    extra_general = sampled("general_targets", general_targets)
 
     if rank != 0:
         return None
@@ -404,6 +418,8 @@ def run_ours(args, world, rank, local):
         line["short_targets"] = extra_short
     if extra_general is not None:
         line["general_targets"] = extra_general
+    if target_clocks:
+        line["target_clocks"] = target_clocks
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tf, dt, desc = oracle_sample()
         line["cpu_baseline"] = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
