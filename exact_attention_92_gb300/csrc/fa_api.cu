@@ -147,6 +147,31 @@ int choose_splits_causal(long long BH, int qblocks, int q_block, int key_tile, i
   return best_s;
 }
 
+// Number of key splits when each (batch*head) unit has a single query tile
+// (decoding steps, or grouped query heads packed into one tile): a step is
+// then a chain of one tile's S, softmax and P V, paced by latency rather
+// than by the tensor pipe or memory, and each unit pays a fixed start and
+// finish (its Q and first K, V from memory, the partial write-out) of about
+// three steps (fitted on GQA decoding at head dim 64 and 128 with 8K and
+// 32K keys).  So the count minimises waves x (key tiles per split + 3).
+int choose_splits_single_tile(long long units, int nkv, int min_tiles, int sm_count) {
+  constexpr int kUnitSteps = 3;
+  int best = 1;
+  long long best_cost = -1;
+  for (int s = 1; s <= 16; ++s) {
+    if (s > 1 && nkv / s < min_tiles) break;
+    const int per = (nkv + s - 1) / s;
+    const long long u = units * ((nkv + per - 1) / per);  // non-empty splits
+    const long long waves = (u + sm_count - 1) / sm_count;
+    const long long cost = waves * (per + kUnitSteps);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
+}
+
 // Stream-ordered workspace.  For failure-path tests, the environment variable
 // FA_TEST_FAIL_ALLOC (any value but "0") makes every workspace allocation
 // report failure without allocating.
@@ -403,7 +428,9 @@ int fa_fwd_general(const void* q, const void* k, const void* v, void* o, float* 
   int S = num_splits;
   if (S == 0) {
     S = choose_splits((long long)BH * qblocks, nkv, wide ? 8 : 4, s->sm_count);
-    if (S > 1 && causal != FA_CAUSAL_NONE && !pack && !wide)
+    if (S > 1 && !wide && Nq <= fa::kTileM && (pack || causal == FA_CAUSAL_NONE || Nq == 1))
+      S = choose_splits_single_tile(BH, nkv, 4, s->sm_count);
+    else if (S > 1 && causal != FA_CAUSAL_NONE && !pack && !wide)
       S = choose_splits_causal(BH, qblocks, q_block, key_tile, Nq, nkv, causal_off, d, 4, s->sm_count);
   }
   if (S > nkv) S = nkv;
