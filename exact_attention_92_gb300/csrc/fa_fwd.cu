@@ -405,12 +405,14 @@ __global__ void __launch_bounds__(384, 1)
         }
         float mx0 = x[0], mx1 = x[1], mx2 = x[2], mx3 = x[3];
 #pragma unroll
-        for (int c = 4; c < kTileN; c += 8) {
+        for (int c = 4; c + 8 <= kTileN; c += 8) {
           mx0 = fmax3(mx0, x[c], x[c + 1]);
           mx1 = fmax3(mx1, x[c + 2], x[c + 3]);
           mx2 = fmax3(mx2, x[c + 4], x[c + 5]);
           mx3 = fmax3(mx3, x[c + 6], x[c + 7]);
         }
+        mx0 = fmax3(mx0, x[kTileN - 4], x[kTileN - 3]);  // the last four columns
+        mx1 = fmax3(mx1, x[kTileN - 2], x[kTileN - 1]);
         const float m_tile = fmax3(fmaxf(mx0, mx1), mx2, mx3) * sl2;
         // m_ref stays -inf while the row has seen no key; the first key it
         // sees then takes the rescale path with f = 0 (l and O~ are 0).

@@ -321,12 +321,14 @@ __global__ void __launch_bounds__(d256::kThreads, 1)
         }
         float mx0 = x[0], mx1 = x[1], mx2 = x[2], mx3 = x[3];
 #pragma unroll
-        for (int c = 4; c < kKeys; c += 8) {
+        for (int c = 4; c + 8 <= kKeys; c += 8) {
           mx0 = fmax3(mx0, x[c], x[c + 1]);
           mx1 = fmax3(mx1, x[c + 2], x[c + 3]);
           mx2 = fmax3(mx2, x[c + 4], x[c + 5]);
           mx3 = fmax3(mx3, x[c + 6], x[c + 7]);
         }
+        mx0 = fmax3(mx0, x[kKeys - 4], x[kKeys - 3]);  // the last four columns
+        mx1 = fmax3(mx1, x[kKeys - 2], x[kKeys - 1]);
         const float m_tile = fmax3(fmaxf(mx0, mx1), mx2, mx3) * sl2;
         float f = 1.f;
         bool rescale = false;
