@@ -238,6 +238,11 @@ __global__ void __launch_bounds__(384, 1)
   if (warp == 9) {
     // ------------------------------------------------------------ producer
     reg_dealloc<R::kRegsCtl>();
+    // Launched while the D preprocess may still run: wait for it before
+    // reading D, then let the dQ kernel (which needs nothing from this one)
+    // take over SMs as this grid's CTAs finish.
+    pdl_wait();
+    pdl_trigger();
     uint32_t kc = 0, qc = 0;
     uint32_t k_issued = 0, v_issued = 0, q_issued = 0, do_issued = 0;  // copies started (for the drain)
     bool ok = true;
@@ -1046,6 +1051,9 @@ template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_preprocess(const __nv_bfloat16* __restrict__ o,
                                                          const __nv_bfloat16* __restrict__ dout,
                                                          float* __restrict__ dvec, int rows) {
+  // Launched while the kernel before it (the forward, writing O) may still
+  // run: its writes are read here.
+  pdl_wait();
   constexpr int kVec = (D == 96) ? 3 : 1;     // 16-byte pieces per lane (lanes per row a power of two)
   constexpr int kLanes = D / (8 * kVec);      // lanes per row
   constexpr int kSlots = 256 / kLanes;        // rows per pass
@@ -1111,7 +1119,8 @@ static cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, c
   cudaError_t e = cudaFuncSetAttribute(fa_bwd_dkdv_kernel<D, GQA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  fa_bwd_dkdv_kernel<D, GQA><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, p);
+  e = launch_pdl(fa_bwd_dkdv_kernel<D, GQA>, dim3(grid), dim3(C::kThreads), C::kSmemBytes, stream, tq, tk, tv, tdo, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -1122,7 +1131,10 @@ static cudaError_t launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, con
   cudaError_t e =
       cudaFuncSetAttribute(fa_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  fa_bwd_dq_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, p);
+  // May start as the dK/dV kernel's CTAs finish: it reads only the inputs,
+  // L and D, and D was complete before any dK/dV CTA let it start.
+  e = launch_pdl(fa_bwd_dq_kernel<D>, dim3(grid), dim3(C::kThreads), C::kSmemBytes, stream, tq, tk, tv, tdo, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -1158,8 +1170,10 @@ static cudaError_t launch_pre_t(const void* o, const void* dout, float* dvec, in
   constexpr int kVec = (D == 96) ? 3 : 1;
   const int per_block = (256 / (D / (8 * kVec))) * 4;  // rows per 256-thread block (4 passes)
   const int grid = (rows + per_block - 1) / per_block;
-  fa_bwd_preprocess<D><<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(o),
-                                                  static_cast<const __nv_bfloat16*>(dout), dvec, rows);
+  const cudaError_t e = launch_pdl(fa_bwd_preprocess<D>, dim3(grid), dim3(256), 0, stream,
+                                   static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout),
+                                   dvec, rows);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

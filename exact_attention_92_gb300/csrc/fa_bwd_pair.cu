@@ -200,6 +200,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(384, 1)
   if (warp == 9) {
     // ------------------------------------------------------------ producer
     reg_dealloc<R::kRegsCtl>();
+    // Launched while the D preprocess may still run: wait for it before
+    // reading D, then let the dQ kernel (which needs nothing from this one)
+    // take over SMs as this grid's CTAs finish.
+    pdl_wait();
+    pdl_trigger();
     const uint32_t k_full_l = at_leader(k_full), v_full_l = at_leader(v_full);
     uint32_t kc = 0, qc = 0;
     uint32_t k_issued = 0, v_issued = 0, q_issued = 0, do_issued = 0;  // copies started (for the drain)
@@ -611,7 +616,8 @@ static cudaError_t launch_pair_t(const CUtensorMap& tq64, const CUtensorMap& tq,
   }
   const long long units = (long long)p.B * p.Hkv * ((p.kv_tiles_used + 1) / 2);
   const int pairs = (int)(units < mp ? units : mp);
-  kern<<<2 * pairs, pr::kThreads, pr::kSmemBytes, stream>>>(tq64, tq, tk, tv, tdo64, tdo, p);
+  e = launch_pdl(kern, dim3(2 * pairs), dim3(pr::kThreads), pr::kSmemBytes, stream, tq64, tq, tk, tv, tdo64, tdo, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

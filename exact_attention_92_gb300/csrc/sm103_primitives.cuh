@@ -5,6 +5,7 @@
 
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
 #include "fa_common.h"
@@ -112,6 +113,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, WaitCt
   if (mbar_try_wait(b, parity)) return true;
   return mbar_wait_slow(b, parity, ctl, where);
 }
+
+// ------------------------------------------------- programmatic dependent launch
+// A kernel launched with programmatic stream serialization may start while
+// the kernel before it in the stream is still running: pdl_wait() blocks the
+// calling thread until that kernel has completed and its memory writes are
+// visible; pdl_trigger() lets the kernel after this one start early (once
+// every CTA of this grid has triggered or exited).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // --------------------------------------------------------------------- TMA
 
@@ -391,4 +401,23 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 }  // namespace dev
+
+// Launch with programmatic stream serialization: the kernel may start while
+// the previous kernel of the stream finishes (see pdl_wait / pdl_trigger).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 }  // namespace fa
