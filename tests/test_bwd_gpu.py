@@ -75,6 +75,36 @@ def test_gradients_bitwise_repeatable(fa, d):
 
 
 @pytest.mark.parametrize("d", [64, 128])
+def test_back_to_back_calls_on_shared_buffers(fa, d):
+    """Forward and backward calls of two problems queued on one stream with no
+    synchronisation, writing the same O and L: each call's gradients equal,
+    bit for bit, those of the same problem run alone.  The backward's kernels
+    may start before the kernel ahead of them in the stream has ended, so
+    this checks that each waits for what it reads (the new O, the new D)."""
+    torch = torch_cuda()
+    cases = [inputs.make_case(2, 4, 1000, d, True, seed=300 + d + i, with_do=True) for i in range(2)]
+    tens = [case_tensors(c) for c in cases]
+    alone = []
+    for q, k, v, do in tens:
+        o, lse = fa.forward(q, k, v, causal=True)
+        alone.append(fa.backward(q, k, v, o, lse, do, causal=True))
+    torch.cuda.synchronize()
+    q0 = tens[0][0]
+    o = torch.empty_like(q0)
+    lse = torch.empty(q0.shape[:3], dtype=torch.float32, device="cuda")
+    outs = [tuple(torch.empty_like(q0) for _ in range(3)) for _ in range(6)]
+    for i, (dq, dk, dv) in enumerate(outs):
+        q, k, v, do = tens[i % 2]
+        fa.fa_fwd(q, k, v, o, lse, True)
+        fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, True)
+    torch.cuda.synchronize()
+    assert fa.fa_poll_status() == fa.FA_OK
+    for i, got in enumerate(outs):
+        for name, x, y in zip(("dQ", "dK", "dV"), got, alone[i % 2]):
+            assert torch.equal(x, y), f"call {i}: {name} differs from the problem run alone"
+
+
+@pytest.mark.parametrize("d", [64, 128])
 def test_outputs_only_16_byte_aligned(fa, d):
     """Gradient buffers that are 16- but not 32-byte aligned take the 16-byte
     store path; the results are the same bits as with aligned buffers."""
