@@ -251,6 +251,13 @@ __global__ void __launch_bounds__(b256::kThreads, 1)
     // (read from global memory into registers before the copies are
     // issued, stored to the ring after), so the copies never wait behind
     // those reads.
+    // Launched while the kernel ahead may still run.  The dV pass follows
+    // the D preprocess: it waits for it (it reads no D itself, but the
+    // kernels after it rely on D being complete once it has let them
+    // launch).  The dK pass follows the dV pass, which it does not read:
+    // D was complete before the dV pass let it launch.
+    if constexpr (!DK) pdl_wait();
+    pdl_trigger();
     uint32_t kc = 0, qc = 0;
     uint32_t q_issued = 0, do_issued = 0, k_issued = 0, v_issued = 0;  // copies started (for the drain)
     bool ok = true;
@@ -815,7 +822,8 @@ static cudaError_t launch_kv256_t(const CUtensorMap& tq, const CUtensorMap& tk, 
   constexpr int smem = b256::KvCfg<DK>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(fa_bwd256_kv_kernel<DK, GQA>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  fa_bwd256_kv_kernel<DK, GQA><<<grid, b256::kThreads, smem, stream>>>(tq, tk, tv, tdo, p);
+  e = launch_pdl(fa_bwd256_kv_kernel<DK, GQA>, dim3(grid), dim3(b256::kThreads), smem, stream, tq, tk, tv, tdo, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -837,7 +845,11 @@ cudaError_t launch_bwd256_dq(const CUtensorMap& tq, const CUtensorMap& tk, const
   cudaError_t e =
       cudaFuncSetAttribute(fa_bwd256_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, b256::DqCfg::kSmemBytes);
   if (e != cudaSuccess) return e;
-  fa_bwd256_dq_kernel<<<grid, b256::kThreads, b256::DqCfg::kSmemBytes, stream>>>(tq, tk, tv, tdo, p);
+  // May start as the dK pass's CTAs finish: it reads only the inputs, L and
+  // D, and D was complete before the dV pass let the dK pass launch.
+  e = launch_pdl(fa_bwd256_dq_kernel, dim3(grid), dim3(b256::kThreads), b256::DqCfg::kSmemBytes, stream, tq, tk, tv,
+                 tdo, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

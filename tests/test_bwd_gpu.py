@@ -74,7 +74,7 @@ def test_gradients_bitwise_repeatable(fa, d):
         assert np.array_equal(x, y)
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_back_to_back_calls_on_shared_buffers(fa, d):
     """Forward and backward calls of two problems queued on one stream with no
     synchronisation, writing the same O and L: each call's gradients equal,
