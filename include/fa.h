@@ -28,7 +28,8 @@
  *    backward's kernels are launched with programmatic stream serialization
  *    (each may start while the kernel ahead of it in the stream finishes,
  *    and waits on the device for what it reads); work the caller queues
- *    after a call still starts only once all of the call's kernels are done.
+ *    after a call, if not itself launched with programmatic serialization,
+ *    still starts only once all of the call's kernels are done.
  *  - The caller owns every buffer it passes; the library never frees or keeps
  *    them.  Temporary device workspace (the fp32 split-KV partials of the
  *    forward pass, the fp32 D vector of the backward pass) is taken with
