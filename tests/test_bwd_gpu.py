@@ -93,10 +93,15 @@ def test_back_to_back_calls_on_shared_buffers(fa, d):
     o = torch.empty_like(q0)
     lse = torch.empty(q0.shape[:3], dtype=torch.float32, device="cuda")
     outs = [tuple(torch.empty_like(q0) for _ in range(3)) for _ in range(6)]
+    side = torch.cuda.Stream()  # the last three calls on a stream of their own
+    side.wait_stream(torch.cuda.current_stream())
     for i, (dq, dk, dv) in enumerate(outs):
         q, k, v, do = tens[i % 2]
-        fa.fa_fwd(q, k, v, o, lse, True)
-        fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, True)
+        st = side if i >= 3 else None
+        if i == 3:
+            side.wait_stream(torch.cuda.current_stream())
+        fa.fa_fwd(q, k, v, o, lse, True, stream=st)
+        fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, True, stream=st)
     torch.cuda.synchronize()
     assert fa.fa_poll_status() == fa.FA_OK
     for i, got in enumerate(outs):
