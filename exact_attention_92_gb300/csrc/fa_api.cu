@@ -154,21 +154,28 @@ int choose_splits_causal(long long BH, int qblocks, int q_block, int key_tile, i
 // finish (its Q and first K, V from memory, the partial write-out) of about
 // three steps (fitted on GQA decoding at head dim 64 and 128 with 8K and
 // 32K keys).  So the count minimises waves x (key tiles per split + 3).
-int choose_splits_single_tile(long long units, int nkv, int min_tiles, int sm_count) {
-  constexpr int kUnitSteps = 3;
+// With both query tiles on a unit's rows (dual mode, `chains` = 2) a unit's
+// key tiles take half as many steps, and its second partial result one step
+// more; dual mode asks for at least 8 key tiles a split (four steps a tile).
+// Returns the count, and its estimated cost in *cost (-1: none qualifies).
+int choose_splits_single_tile(long long units, int nkv, int min_tiles, int sm_count, int chains,
+                              long long* cost_out = nullptr) {
+  const int unit_steps = chains == 2 ? 4 : 3;
   int best = 1;
   long long best_cost = -1;
   for (int s = 1; s <= 16; ++s) {
     if (s > 1 && nkv / s < min_tiles) break;
     const int per = (nkv + s - 1) / s;
+    if (chains == 2 && per < 8) break;
     const long long u = units * ((nkv + per - 1) / per);  // non-empty splits
     const long long waves = (u + sm_count - 1) / sm_count;
-    const long long cost = waves * (per + kUnitSteps);
+    const long long cost = waves * ((per + chains - 1) / chains + unit_steps);
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       best = s;
     }
   }
+  if (cost_out) *cost_out = best_cost;
   return best;
 }
 
@@ -425,13 +432,29 @@ int fa_fwd_general(const void* q, const void* k, const void* v, void* o, float* 
   const int key_tile = wide ? 64 : 128;
   const int nkv = (Nk + key_tile - 1) / key_tile;
   const int qblocks = (Nq + q_block - 1) / q_block;
+  // Units of a single query tile (decoding) leave the second tile of a CTA
+  // idle: with enough key tiles both tiles then take the unit's rows and
+  // half of its key tiles each (dual mode), their partial results merged,
+  // when the step model above prefers that to one tile per unit.
+  bool dual = false;
   int S = num_splits;
   if (S == 0) {
     S = choose_splits((long long)BH * qblocks, nkv, wide ? 8 : 4, s->sm_count);
-    if (S > 1 && !wide && Nq <= fa::kTileM && (pack || causal == FA_CAUSAL_NONE || Nq == 1))
-      S = choose_splits_single_tile(BH, nkv, 4, s->sm_count);
-    else if (S > 1 && causal != FA_CAUSAL_NONE && !pack && !wide)
+    if (!wide && Nq <= fa::kTileM) {
+      long long c1 = -1, c2 = -1;
+      const int s1 = choose_splits_single_tile(BH, nkv, 4, s->sm_count, 1, &c1);
+      const int s2 = choose_splits_single_tile(BH, nkv, 4, s->sm_count, 2, &c2);
+      if (c2 >= 0 && c2 < c1) {
+        dual = true;
+        S = s2;
+      } else if (S > 1 && (pack || causal == FA_CAUSAL_NONE || Nq == 1)) {
+        S = s1;
+      } else if (S > 1 && causal != FA_CAUSAL_NONE && !pack) {
+        S = choose_splits_causal(BH, qblocks, q_block, key_tile, Nq, nkv, causal_off, d, 4, s->sm_count);
+      }
+    } else if (S > 1 && causal != FA_CAUSAL_NONE && !pack && !wide) {
       S = choose_splits_causal(BH, qblocks, q_block, key_tile, Nq, nkv, causal_off, d, 4, s->sm_count);
+    }
   }
   if (S > nkv) S = nkv;
   if (S < 1) S = 1;
@@ -476,26 +499,28 @@ int fa_fwd_general(const void* q, const void* k, const void* v, void* o, float* 
   }
   p.status = s->status;
   p.timeout_ns = g_timeout_ns.load();
+  p.dual = dual ? 1 : 0;
 
   void* ws = nullptr;
   const size_t rows = (size_t)BH * Nq;
-  if (S > 1) {
-    const size_t bytes = (size_t)S * rows * ((size_t)d + 1) * sizeof(float);
+  const int parts = dual ? 2 * S : S;  // partial results to merge
+  if (parts > 1) {
+    const size_t bytes = (size_t)parts * rows * ((size_t)d + 1) * sizeof(float);
     if (ws_alloc(&ws, bytes, st) != cudaSuccess) {
       cudaGetLastError();
       return FA_ERR_NO_MEMORY;
     }
     p.o_part = static_cast<float*>(ws);
-    p.lse_part = p.o_part + (size_t)S * rows * d;
+    p.lse_part = p.o_part + (size_t)parts * rows * d;
   }
   const int grid = p.num_units < s->sm_count ? p.num_units : s->sm_count;
   cudaError_t ce = timed(FA_KERNEL_FWD, st, [&] {
     return wide ? fa::launch_fwd256(tq, tk, tv, p, grid, st) : fa::launch_fwd(d, tq, tk, tv, p, grid, st);
   });
-  if (ce == cudaSuccess && S > 1) {
+  if (ce == cudaSuccess && parts > 1) {
     fa::CombineParams c;
     c.rows = (int)rows;
-    c.num_splits = S;
+    c.num_splits = parts;
     c.o_part = p.o_part;
     c.lse_part = p.lse_part;
     c.o = o;

@@ -74,6 +74,11 @@ struct FwdParams {
   int head_window;
   unsigned int* status;
   unsigned long long timeout_ns;
+  // 1: every unit has at most 128 query rows (decoding), and both query
+  // tiles of a unit hold those rows, tile t taking the key tiles kvb + t,
+  // kvb + t + 2, ... of the unit's split; each tile writes its own partial
+  // result (partial 2 * split + t of 2 * num_splits, merged afterwards).
+  int dual;
 };
 
 // Query position of row r (see FwdParams::q_period).

@@ -92,6 +92,16 @@ struct Unit {
   int split;
 };
 
+// Key tile (from kvb) of query tile t's j-th step, and the unit's first
+// query row of tile t (both tiles hold the same rows in dual mode).
+template <bool DUAL>
+__device__ __forceinline__ int step_key_tile(int t, int j) { return DUAL ? 2 * j + t : j; }
+template <bool DUAL>
+__device__ __forceinline__ int tile_row0(const Unit& w, int t) {
+  return DUAL ? w.q0 : w.q0 + kTileM * t;
+}
+
+template <bool DUAL>
 __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
   Unit w;
   const int split = u % p.num_splits;
@@ -118,6 +128,18 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
   const int hi = min(nkv, lo + p.kv_tiles_per_split);
   w.kvb = lo;
   w.split = split;
+  if constexpr (DUAL) {
+    // Both tiles: the rows of tile 0; the keys they see split by parity.
+    int h = hi;
+    if (p.causal) {
+      const int last_key = max_query_pos(w.q0, min(p.Nq, w.q0 + kTileM) - 1, p.q_period) + p.causal_off;
+      h = last_key < 0 ? 0 : min(hi, last_key / kTileN + 1);
+    }
+    const int nk = w.q0 < p.Nq ? max(0, h - lo) : 0;
+    w.n[0] = (nk + 1) / 2;
+    w.n[1] = nk / 2;
+    return w;
+  }
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     const int row0 = w.q0 + kTileM * t;
@@ -134,6 +156,12 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
     }
   }
   return w;
+}
+
+// Key tiles a unit streams through the K/V ring (both tiles' in dual mode).
+template <bool DUAL>
+__device__ __forceinline__ int unit_key_tiles(const Unit& w) {
+  return DUAL ? w.n[0] + w.n[1] : max(w.n[0], w.n[1]);
 }
 
 // S = Q K^T: 16-wide K-steps walk 32 bytes inside a 128-byte swizzle row
@@ -161,7 +189,9 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint3
     mma_ts_lh_w(tmem_o, tmem_p + kk * 8, v_lo + ((kk * 2048) >> 4), hi, idesc, (accumulate || kk > 0) ? 1u : 0u);
 }
 
-template <int D>
+// DUAL: p.dual (both query tiles on one unit's rows), a separate
+// instantiation so the usual path carries none of it.
+template <int D, bool DUAL>
 __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -228,7 +258,7 @@ __global__ void __launch_bounds__(384, 1)
       for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units; ++rnd) {
         const int u = snake_unit(rnd);
         if (u >= p.num_units) continue;
-        const Unit w = decode_unit(p, u);
+        const Unit w = decode_unit<DUAL>(p, u);
         const int kvbh = p.Hkv == p.H ? w.bh : kv_head_of(w.bh, p.H, p.Hkv);  // K, V head
         for (int t = 0; ok && t < 2; ++t) {
           if (w.n[t] == 0) continue;
@@ -237,11 +267,11 @@ __global__ void __launch_bounds__(384, 1)
           mbar_arrive_expect_tx(&q_full[t], C::kTileBytes);
           for (int c = 0; c < C::kChunks; ++c)
             tma_load_3d(sQ + t * C::kTileBytes + c * C::kChunkBytes, &tm_q, &q_full[t], c * 64,
-                        w.q0 + kTileM * t, w.bh);
+                        tile_row0<DUAL>(w, t), w.bh);
           ++qc[t];
         }
-        const int nmax = max(w.n[0], w.n[1]);
-        for (int j = 0; ok && j < nmax; ++j) {
+        const int nk = unit_key_tiles<DUAL>(w);
+        for (int j = 0; ok && j < nk; ++j) {
           for (int which = 0; which < 2; ++which) {
             const uint32_t slot = rc % C::kStages;
             ok = mbar_wait(&kv_empty[slot], ((rc / C::kStages) & 1) ^ 1, ctl, kWaitKvEmpty);
@@ -281,7 +311,7 @@ __global__ void __launch_bounds__(384, 1)
       for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units; ++rnd) {
         const int u = snake_unit(rnd);
         if (u >= p.num_units) continue;
-        const Unit w = decode_unit(p, u);
+        const Unit w = decode_unit<DUAL>(p, u);
         const int nmax = max(w.n[0], w.n[1]);
         if (nmax == 0) continue;
         for (int t = 0; ok && t < 2; ++t) {
@@ -290,6 +320,53 @@ __global__ void __launch_bounds__(384, 1)
           ++qc[t];
         }
         if (!ok) break;
+        if constexpr (DUAL) {
+          // Dual mode: tile t's step j reads key tile 2j + t (K at position
+          // rc + 2 (2j + t), V one after it); each K and V has one reader
+          // and is released after its product.
+          for (int t = 0; ok && t < 2; ++t) {
+            if (w.n[t] == 0) continue;
+            const uint32_t pos_k = rc + 2 * t;
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait(&kv_full[pos_k % C::kStages], (pos_k / C::kStages) & 1, ctl, kWaitKvFull));
+            if (!ok) break;
+            tc_fence_after();
+            issue_qk<D>(tmem + C::col_s(t), q_lo0 + t * kTileStep, k_lo0 + (pos_k % C::kStages) * kTileStep, hi);
+            mma_commit_w(&s_full[t]);
+            if (w.n[t] == 1) mma_commit_w(&q_empty[t]);  // Q_t's last product
+            mma_commit_w(&kv_empty[pos_k % C::kStages]);
+          }
+          for (int j = 0; ok && j < nmax; ++j) {
+            for (int t = 0; t < 2; ++t) {
+              if (j >= w.n[t]) continue;
+              const uint32_t pos_v = rc + 2 * (2 * j + t) + 1;
+              ok = __all_sync(0xffffffffu,
+                              mbar_wait(&kv_full[pos_v % C::kStages], (pos_v / C::kStages) & 1, ctl, kWaitKvFull));
+              if (!ok) break;
+              ok = __all_sync(0xffffffffu, mbar_wait(&p_full[t], pc[t] & 1, ctl, kWaitPFull));
+              ++pc[t];
+              if (!ok) break;
+              tc_fence_after();
+              issue_pv<D>(tmem + C::col_o(t), tmem + C::col_s(t), v_lo0 + (pos_v % C::kStages) * kTileStep, hi, j > 0);
+              mma_commit_w(&kv_empty[pos_v % C::kStages]);
+              if (j + 1 < w.n[t]) {
+                const uint32_t pos_k = rc + 2 * (2 * (j + 1) + t);
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(&kv_full[pos_k % C::kStages], (pos_k / C::kStages) & 1, ctl, kWaitKvFull));
+                if (!ok) break;
+                tc_fence_after();
+                issue_qk<D>(tmem + C::col_s(t), q_lo0 + t * kTileStep, k_lo0 + (pos_k % C::kStages) * kTileStep, hi);
+                mma_commit_w(&s_full[t]);
+                if (j + 2 == w.n[t]) mma_commit_w(&q_empty[t]);  // Q_t's last product
+                mma_commit_w(&kv_empty[pos_k % C::kStages]);
+              } else {
+                mma_commit_w(&o_full[t]);
+              }
+            }
+          }
+          rc += 2 * unit_key_tiles<DUAL>(w);
+          continue;
+        }
         {
           const uint32_t slot_k = rc % C::kStages;
           ok = __all_sync(0xffffffffu, mbar_wait(&kv_full[slot_k], (rc / C::kStages) & 1, ctl, kWaitKvFull));
@@ -358,16 +435,18 @@ __global__ void __launch_bounds__(384, 1)
     for (int rnd = 0; ok && rnd * (int)gridDim.x < p.num_units; ++rnd) {
       const int u = snake_unit(rnd);
       if (u >= p.num_units) continue;
-      const Unit w = decode_unit(p, u);
-      const int row0 = w.q0 + kTileM * t;
+      const Unit w = decode_unit<DUAL>(p, u);
+      const int row0 = tile_row0<DUAL>(w, t);
       const int row = row0 + r_in_tile;
-      const int split = w.split;
+      // Partial result this tile writes (one per split; two in dual mode).
+      const int part = DUAL ? 2 * w.split + t : w.split;
+      const bool partial = DUAL || p.num_splits > 1;
       if (w.n[t] == 0) {
         // No row of the tile sees a key (of this split): O = 0, L = -inf
         // (an empty partial when the keys are split).
         if (row < p.Nq) {
-          if (p.num_splits > 1) {
-            const size_t prow = ((size_t)split * p.B * p.H + w.bh) * p.Nq + row;
+          if (partial) {
+            const size_t prow = ((size_t)part * p.B * p.H + w.bh) * p.Nq + row;
             float4* dst = reinterpret_cast<float4*>(p.o_part + prow * D);
             for (int c = 0; c < D / 4; ++c) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
             p.lse_part[prow] = -INFINITY;
@@ -394,7 +473,7 @@ __global__ void __launch_bounds__(384, 1)
         float x[kTileN];
 #pragma unroll
         for (int c = 0; c < kTileN; ++c) x[c] = __uint_as_float(s[c]);
-        const int kv0 = (w.kvb + j) * kTileN;
+        const int kv0 = (w.kvb + step_key_tile<DUAL>(t, j)) * kTileN;
         const bool need_mask = (kv0 + kTileN > p.Nk) ||
                                (p.causal && (p.q_period > 0 || kv0 + kTileN - 1 > row0 + p.causal_off));
         if (need_mask) {
@@ -492,7 +571,7 @@ __global__ void __launch_bounds__(384, 1)
       // A row that saw no key has l = 0: O = 0, L = -inf.
       const float inv_l = l_bf > 0.f ? 1.0f / l_bf : 0.f;
       const float lse = l > 0.f ? (m_ref + lg2_approx(l)) * 0.69314718055994530942f : -INFINITY;
-      if (p.num_splits == 1) {
+      if (!partial) {
         // O = O~ / l in bf16, 64 columns (128 bytes of the row) at a time,
         // stored with whole row segments per warp store; rows past N are
         // skipped.
@@ -528,7 +607,7 @@ __global__ void __launch_bounds__(384, 1)
         }
         if (row < p.Nq) p.lse[(size_t)w.bh * p.Nq + row] = lse;
       } else {
-        const size_t prow = ((size_t)split * p.B * p.H + w.bh) * p.Nq + row;
+        const size_t prow = ((size_t)part * p.B * p.H + w.bh) * p.Nq + row;
         float4* dst = reinterpret_cast<float4*>(p.o_part + prow * D);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
@@ -608,22 +687,26 @@ __global__ void __launch_bounds__(256) fa_combine_kernel(const CombineParams p) 
 
 // ------------------------------------------------------------------ launch
 
-template <int D>
+template <int D, bool DUAL>
 static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 const FwdParams& p, int grid, cudaStream_t stream) {
   using C = FwdCfg<D>;
-  cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  cudaError_t e =
+      cudaFuncSetAttribute(fa_fwd_kernel<D, DUAL>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  fa_fwd_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
+  fa_fwd_kernel<D, DUAL><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdParams& p, int grid, cudaStream_t stream) {
   switch (d) {
-    case 64: return launch_fwd_t<64>(tq, tk, tv, p, grid, stream);
-    case 96: return launch_fwd_t<96>(tq, tk, tv, p, grid, stream);
-    case 128: return launch_fwd_t<128>(tq, tk, tv, p, grid, stream);
+    case 64: return p.dual ? launch_fwd_t<64, true>(tq, tk, tv, p, grid, stream)
+                           : launch_fwd_t<64, false>(tq, tk, tv, p, grid, stream);
+    case 96: return p.dual ? launch_fwd_t<96, true>(tq, tk, tv, p, grid, stream)
+                           : launch_fwd_t<96, false>(tq, tk, tv, p, grid, stream);
+    case 128: return p.dual ? launch_fwd_t<128, true>(tq, tk, tv, p, grid, stream)
+                            : launch_fwd_t<128, false>(tq, tk, tv, p, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }

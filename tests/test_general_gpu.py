@@ -88,6 +88,9 @@ FWD_SHAPES = [
     # a few rows per key/value head (decoding steps), grouped and not: 2 x 4, 5, 3, 8 x 1, 8 rows
     (1, 8, 2, 2, 3000, 64), (1, 1, 1, 5, 700, 128), (3, 4, 4, 3, 1000, 64), (1, 16, 2, 1, 257, 128),
     (2, 2, 2, 8, 33, 128),
+    # single-tile units over long keys: both query tiles of a CTA take a unit's rows and split its
+    # key tiles (even / odd), with an odd count per split, a ragged last key tile, 100 and 64 rows
+    (4, 32, 8, 1, 8192, 64), (2, 16, 16, 100, 4000, 128), (8, 8, 8, 64, 6000, 96),
 ]
 
 
@@ -105,6 +108,21 @@ def test_forward(fa, shape, mode):
     if causal and off < 0:
         # rows that see no key: O = 0 exactly
         assert np.all(o[:, :, :-off] == 0.0), what
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_decoding_runs_dual_tiles(fa, d):
+    """GQA decoding at scale (B=8, 32 query heads over 8 key/value heads, one
+    query row, 8192 keys): the automatic plan puts both query tiles of a CTA
+    on a unit's rows (each tile writes a partial, so the merge kernel runs)
+    and the result matches the oracle."""
+    before = fa.fa_launch_count(fa.FA_KERNEL_COMBINE)
+    q, k, v, _ = make(8, 32, 8, 1, 8192, d, seed=7300 + d)
+    o, lse, _ = run_fwd(fa, q, k, v, "bottom_right")
+    assert fa.fa_launch_count(fa.FA_KERNEL_COMBINE) == before + 1
+    O, L, weights = oracle_fwd(q, k, v, "bottom_right")
+    check_o(o, O, f"decode d={d}", weights)
+    check_lse(lse, L, f"decode d={d}")
 
 
 @pytest.mark.parametrize("d", [96, 256])
