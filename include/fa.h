@@ -122,7 +122,11 @@ int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
  * attention).  The computation of fa_fwd ("FlashAttention V2 in depth",
  * section 6.1) per query row over the keys it sees; short query blocks over
  * long keys (decoding) are split along the keys as in fa_fwd_ex
- * (FlashAttention-2 abstract, point (2)).
+ * (FlashAttention-2 abstract, point (2)).  With num_splits = 0 and at most
+ * 128 query rows per (batch, key/value head) after grouping, the two query
+ * tiles of a CTA may take the even and the odd key tiles of one split; their
+ * fp32 partial results then go through the workspace and the merge as for
+ * a split.
  *   q, o    : bf16 [B,H,Nq,d];  k, v : bf16 [B,Hkv,Nk,d];  lse : fp32 [B,H,Nq]
  *   Nq, Nk  : >= 1
  *   Hkv     : >= 1 and divides H (FA_ERR_INVALID_ARG otherwise)
