@@ -44,6 +44,11 @@
 // Head dims 64, 96 and 128.  A 96-wide row is staged in the 128-wide layout
 // (two 64-column blocks; TMA fills columns 96..127 with zeros) while the
 // products use K = 96 (S) and N = 96 (O) exactly.
+//
+// Units of at most 128 query rows (decoding) would leave tile 1 idle: in
+// the dual instantiation both tiles hold the unit's rows, tile t takes the
+// key tiles kvb + t, kvb + t + 2, ... of its split, and each writes its own
+// fp32 partial result, merged afterwards like the split partials.
 #include <cuda_runtime.h>
 
 #include "sm103_primitives.cuh"
