@@ -27,10 +27,12 @@ from ._binding import (  # noqa: F401
     fa_bwd_general,
     fa_bwd_gqa,
     fa_bwd_noalloc,
+    fa_bwd_plan,
     fa_fwd,
     fa_fwd_ex,
     fa_fwd_general,
     fa_fwd_gqa,
+    fa_fwd_plan,
     fa_poll_status,
     fa_selftest_wait_timeout,
     fa_set_wait_timeout_ns,

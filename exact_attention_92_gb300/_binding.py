@@ -68,6 +68,24 @@ _SIGNATURES = {
 }
 
 
+class FwdPlan(ctypes.Structure):
+    """fa_fwd_plan_t (include/fa.h)."""
+    _fields_ = [(n, _i) for n in ("packed_heads", "unit_heads", "unit_rows", "query_block", "key_tile",
+                                  "key_tiles", "num_splits", "key_tiles_per_split", "dual", "partials",
+                                  "num_units", "grid", "head_window", "launches")] + [("workspace_bytes", _u64)]
+
+
+class BwdPlan(ctypes.Structure):
+    """fa_bwd_plan_t (include/fa.h)."""
+    _fields_ = [(n, _i) for n in ("q_tiles", "k_tiles", "q_tile_first", "kv_tiles_used", "dq_units", "dq_grid",
+                                  "kv_units", "kv_cta_pair", "kv_passes", "launches")] + [
+        (n, _u64) for n in ("zeroed_dq_bytes", "zeroed_dkdv_bytes", "workspace_bytes")]
+
+
+_SIGNATURES["fa_fwd_plan"] = ([_i] * 9 + [_u64, ctypes.POINTER(FwdPlan)], _i)
+_SIGNATURES["fa_bwd_plan"] = ([_i] * 8 + [ctypes.POINTER(BwdPlan)], _i)
+
+
 def load():
     """Load libfa.so once; raise FaError if it is not built."""
     global _lib
@@ -321,6 +339,29 @@ def fa_launch_count(kernel: int) -> int:
     n = ctypes.c_uint64(0)
     _check(load().fa_launch_count(int(kernel), ctypes.byref(n)), "fa_launch_count")
     return n.value
+
+
+def _plan_dict(plan):
+    return {name: getattr(plan, name) for name, _ in plan._fields_}
+
+
+def fa_fwd_plan(B, H, Hkv, Nq, Nk, d, causal, num_splits, sm_count, l2_bytes):
+    """C fa_fwd_plan: the launch plan of fa_fwd_general for these sizes on a
+    device with sm_count SMs and l2_bytes of L2, as a dict of the
+    fa_fwd_plan_t fields.  Host only; raises FaError on a refused size."""
+    plan = FwdPlan()
+    _check(load().fa_fwd_plan(int(B), int(H), int(Hkv), int(Nq), int(Nk), int(d), _causal_code(causal),
+                              int(num_splits), int(sm_count), int(l2_bytes), ctypes.byref(plan)), "fa_fwd_plan")
+    return _plan_dict(plan)
+
+
+def fa_bwd_plan(B, H, Hkv, Nq, Nk, d, causal, sm_count):
+    """C fa_bwd_plan: the launch plan of fa_bwd_general, as a dict of the
+    fa_bwd_plan_t fields.  Host only; raises FaError on a refused size."""
+    plan = BwdPlan()
+    _check(load().fa_bwd_plan(int(B), int(H), int(Hkv), int(Nq), int(Nk), int(d), _causal_code(causal),
+                              int(sm_count), ctypes.byref(plan)), "fa_bwd_plan")
+    return _plan_dict(plan)
 
 
 # ------------------------------------------------------- convenience calls

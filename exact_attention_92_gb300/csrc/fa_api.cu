@@ -242,6 +242,138 @@ int choose_splits(long long units, int nkv, int min_tiles, int sm_count) {
   return best;
 }
 
+// Size checks shared by the forward call and its plan.
+int check_fwd_sizes(int B, int H, int Hkv, int Nq, int Nk, int d, int causal, int num_splits) {
+  int e = validate(B, H, Nq, Nk, d, 1.0f);
+  if (e) return e;
+  if (Hkv < 1 || H % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (causal < FA_CAUSAL_NONE || causal > FA_CAUSAL_BOTTOM_RIGHT) return FA_ERR_INVALID_ARG;
+  if (num_splits < 0) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
+// The host-side decisions of a forward call (fa_fwd_plan_t), for sizes that
+// passed check_fwd_sizes.
+void plan_fwd(int B, int H, int Hkv, int Nq, int Nk, int d, int causal, int num_splits, int sm_count,
+              double l2_bytes, fa_fwd_plan_t* pl) {
+  std::memset(pl, 0, sizeof(*pl));
+  const int causal_off = causal_offset(causal, Nq, Nk);
+  // Grouped query heads with fewer than 128 query rows (decoding, short
+  // chunks): the G query heads of a key/value head share one tile as G * Nq
+  // rows -- the caller's contiguous [B, H, Nq, d] seen as [B, Hkv, G * Nq, d],
+  // so O and L land where they belong -- and K, V are read once per group.
+  // Row r of such a tile is query position r % Nq for the causal mask.
+  const int G = H / Hkv;
+  const bool pack = G > 1 && Nq < 128;
+  if (pack) {
+    H = Hkv;
+    Nq *= G;
+  }
+  const int BH = B * H;
+  // Work units: (batch*head, query block, key split).  A query block is 256
+  // rows (two 128-row tiles) with 128-key tiles, or at d = 256 one 128-row
+  // tile with 64-key tiles.
+  const bool wide = d == 256;
+  const int q_block = wide ? 128 : 256;
+  const int key_tile = wide ? 64 : 128;
+  const int nkv = (Nk + key_tile - 1) / key_tile;
+  const int qblocks = (Nq + q_block - 1) / q_block;
+  // Units of a single query tile (decoding) leave the second tile of a CTA
+  // idle: with enough key tiles both tiles then take the unit's rows and
+  // half of its key tiles each (dual mode), their partial results merged,
+  // when the step model above prefers that to one tile per unit.
+  bool dual = false;
+  int S = num_splits;
+  if (S == 0) {
+    S = choose_splits((long long)BH * qblocks, nkv, wide ? 8 : 4, sm_count);
+    if (!wide && Nq <= fa::kTileM) {
+      long long c1 = -1, c2 = -1;
+      const int s1 = choose_splits_single_tile(BH, nkv, 4, sm_count, 1, &c1);
+      const int s2 = choose_splits_single_tile(BH, nkv, 4, sm_count, 2, &c2);
+      if (c2 >= 0 && c2 < c1) {
+        dual = true;
+        S = s2;
+      } else if (S > 1 && (pack || causal == FA_CAUSAL_NONE || Nq == 1)) {
+        S = s1;
+      } else if (S > 1 && causal != FA_CAUSAL_NONE && !pack) {
+        S = choose_splits_causal(BH, qblocks, q_block, key_tile, Nq, nkv, causal_off, d, 4, sm_count);
+      }
+    } else if (S > 1 && causal != FA_CAUSAL_NONE && !pack && !wide) {
+      S = choose_splits_causal(BH, qblocks, q_block, key_tile, Nq, nkv, causal_off, d, 4, sm_count);
+    }
+  }
+  if (S > nkv) S = nkv;
+  if (S < 1) S = 1;
+  const int per_split = (nkv + S - 1) / S;
+  S = (nkv + per_split - 1) / per_split;  // no empty split
+
+  pl->packed_heads = pack ? 1 : 0;
+  pl->unit_heads = BH;
+  pl->unit_rows = Nq;
+  pl->query_block = q_block;
+  pl->key_tile = key_tile;
+  pl->key_tiles = nkv;
+  pl->num_splits = S;
+  pl->key_tiles_per_split = per_split;
+  pl->dual = dual ? 1 : 0;
+  const int parts = dual ? 2 * S : S;  // partial results to merge
+  pl->partials = parts > 1 ? parts : 0;
+  pl->num_units = BH * qblocks * S;
+  pl->grid = pl->num_units < sm_count ? pl->num_units : sm_count;
+  // Without the causal mask every unit has the same work, so the units can
+  // be listed window by window of heads without losing balance: a window is
+  // the fewest heads whose query blocks fill one round of CTAs, and the K, V
+  // of the heads in flight then stay in L2.  Only when the K and V of all
+  // heads exceed half the L2 (otherwise they stay there anyway).
+  const double kv_bytes = 4.0 * (double)B * Hkv * Nk * d;
+  if (causal == FA_CAUSAL_NONE && S == 1 && kv_bytes > l2_bytes / 2) {
+    const int win = (pl->grid + qblocks - 1) / qblocks;
+    pl->head_window = win < BH ? win : 0;
+  }
+  pl->launches = pl->partials > 0 ? 2 : 1;
+  pl->workspace_bytes = pl->partials > 0 ? (uint64_t)parts * BH * Nq * ((uint64_t)d + 1) * sizeof(float) : 0;
+}
+
+// Size checks shared by the backward call and its plan.
+int check_bwd_sizes(int B, int H, int Hkv, int Nq, int Nk, int d, int causal) {
+  int e = validate(B, H, Nq, Nk, d, 1.0f, true);
+  if (e) return e;
+  if (Hkv < 1 || H % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (causal < FA_CAUSAL_NONE || causal > FA_CAUSAL_BOTTOM_RIGHT) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
+// The host-side decisions of a backward call (fa_bwd_plan_t), for sizes
+// that passed check_bwd_sizes.
+void plan_bwd(int B, int H, int Hkv, int Nq, int Nk, int d, int causal, int sm_count, fa_bwd_plan_t* pl) {
+  std::memset(pl, 0, sizeof(*pl));
+  pl->q_tiles = (Nq + 127) / 128;
+  pl->k_tiles = (Nk + 127) / 128;
+  // With the causal mask: key tiles past the last key the last query row
+  // sees, and query tiles whose rows all see no key (a negative offset),
+  // take no part; their gradient rows are zero.
+  pl->kv_tiles_used = pl->k_tiles;
+  pl->q_tile_first = 0;
+  if (causal != FA_CAUSAL_NONE) {
+    const int off = causal_offset(causal, Nq, Nk);
+    const int last_key = Nq - 1 + off;  // >= 0 for both alignments
+    pl->kv_tiles_used = std::min(pl->k_tiles, last_key / 128 + 1);
+    if (off < 0) pl->q_tile_first = (-off) / 128;
+  }
+  pl->dq_units = B * H * (pl->q_tiles - pl->q_tile_first);
+  pl->dq_grid = pl->dq_units < sm_count ? pl->dq_units : sm_count;
+  pl->kv_cta_pair = d == 128 ? 1 : 0;
+  pl->kv_units = B * Hkv * (pl->kv_cta_pair ? (pl->kv_tiles_used + 1) / 2 : pl->kv_tiles_used);
+  pl->kv_passes = d == 256 ? 2 : 1;
+  pl->launches = 2 + pl->kv_passes;
+  const uint64_t row_bytes = (uint64_t)d * 2;
+  pl->zeroed_dq_bytes =
+      (uint64_t)B * H * std::min((uint64_t)Nq, (uint64_t)pl->q_tile_first * 128) * row_bytes;
+  pl->zeroed_dkdv_bytes =
+      2ull * B * Hkv * ((uint64_t)Nk - std::min((uint64_t)Nk, (uint64_t)pl->kv_tiles_used * 128)) * row_bytes;
+  pl->workspace_bytes = (uint64_t)B * H * Nq * sizeof(float);
+}
+
 // ---------------------------------------------------------------- timing
 
 struct TimingRec {
@@ -398,129 +530,76 @@ int fa_selftest_wait_timeout(uint64_t timeout_ns, void* stream) {
              : FA_ERR_CUDA;
 }
 
+int fa_fwd_plan(int B, int H, int Hkv, int Nq, int Nk, int d, int causal, int num_splits, int sm_count,
+                uint64_t l2_bytes, fa_fwd_plan_t* plan) {
+  if (plan == nullptr || sm_count < 1) return FA_ERR_INVALID_ARG;
+  const int e = check_fwd_sizes(B, H, Hkv, Nq, Nk, d, causal, num_splits);
+  if (e) return e;
+  plan_fwd(B, H, Hkv, Nq, Nk, d, causal, num_splits, sm_count, (double)l2_bytes, plan);
+  return FA_OK;
+}
+
 int fa_fwd_general(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv,
                    int Nq, int Nk, int d, int causal, float scale, int num_splits, void* stream) {
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return FA_ERR_INVALID_ARG;
-  int e = validate(B, H, Nq, Nk, d, scale);
+  if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_INVALID_ARG;
+  int e = check_fwd_sizes(B, H, Hkv, Nq, Nk, d, causal, num_splits);
   if (e) return e;
-  if (Hkv < 1 || H % Hkv != 0) return FA_ERR_INVALID_ARG;
-  if (causal < FA_CAUSAL_NONE || causal > FA_CAUSAL_BOTTOM_RIGHT) return FA_ERR_INVALID_ARG;
-  if (num_splits < 0) return FA_ERR_INVALID_ARG;
   DeviceState* s = nullptr;
   e = device_state(&s);
   if (e) return e;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int causal_off = causal_offset(causal, Nq, Nk);
-  // Grouped query heads with fewer than 128 query rows (decoding, short
-  // chunks): the G query heads of a key/value head share one tile as G * Nq
-  // rows -- the caller's contiguous [B, H, Nq, d] seen as [B, Hkv, G * Nq, d],
-  // so O and L land where they belong -- and K, V are read once per group.
-  // Row r of such a tile is query position r % Nq for the causal mask.
-  const int G = H / Hkv;
-  const bool pack = G > 1 && Nq < 128;
-  if (pack) {
-    H = Hkv;
-    Nq *= G;
-  }
-  const int BH = B * H;
-  // Work units: (batch*head, query block, key split).  A query block is 256
-  // rows (two 128-row tiles) with 128-key tiles, or at d = 256 one 128-row
-  // tile with 64-key tiles.
+  fa_fwd_plan_t pl;
+  plan_fwd(B, H, Hkv, Nq, Nk, d, causal, num_splits, s->sm_count, s->l2_bytes, &pl);
   const bool wide = d == 256;
-  const int q_block = wide ? 128 : 256;
-  const int key_tile = wide ? 64 : 128;
-  const int nkv = (Nk + key_tile - 1) / key_tile;
-  const int qblocks = (Nq + q_block - 1) / q_block;
-  // Units of a single query tile (decoding) leave the second tile of a CTA
-  // idle: with enough key tiles both tiles then take the unit's rows and
-  // half of its key tiles each (dual mode), their partial results merged,
-  // when the step model above prefers that to one tile per unit.
-  bool dual = false;
-  int S = num_splits;
-  if (S == 0) {
-    S = choose_splits((long long)BH * qblocks, nkv, wide ? 8 : 4, s->sm_count);
-    if (!wide && Nq <= fa::kTileM) {
-      long long c1 = -1, c2 = -1;
-      const int s1 = choose_splits_single_tile(BH, nkv, 4, s->sm_count, 1, &c1);
-      const int s2 = choose_splits_single_tile(BH, nkv, 4, s->sm_count, 2, &c2);
-      if (c2 >= 0 && c2 < c1) {
-        dual = true;
-        S = s2;
-      } else if (S > 1 && (pack || causal == FA_CAUSAL_NONE || Nq == 1)) {
-        S = s1;
-      } else if (S > 1 && causal != FA_CAUSAL_NONE && !pack) {
-        S = choose_splits_causal(BH, qblocks, q_block, key_tile, Nq, nkv, causal_off, d, 4, s->sm_count);
-      }
-    } else if (S > 1 && causal != FA_CAUSAL_NONE && !pack && !wide) {
-      S = choose_splits_causal(BH, qblocks, q_block, key_tile, Nq, nkv, causal_off, d, 4, s->sm_count);
-    }
-  }
-  if (S > nkv) S = nkv;
-  if (S < 1) S = 1;
-  const int per_split = (nkv + S - 1) / S;
-  S = (nkv + per_split - 1) / per_split;  // no empty split
+  const int BH = pl.unit_heads;
+  const int rows_per_head = pl.unit_rows;
 
   CUtensorMap tq, tk, tv;
-  if (encode_bhnd(&tq, q, BH, Nq, d) || encode_bhnd(&tk, k, B * Hkv, Nk, d, key_tile) ||
-      encode_bhnd(&tv, v, B * Hkv, Nk, d, key_tile))
+  if (encode_bhnd(&tq, q, BH, rows_per_head, d) || encode_bhnd(&tk, k, B * Hkv, Nk, d, pl.key_tile) ||
+      encode_bhnd(&tv, v, B * Hkv, Nk, d, pl.key_tile))
     return FA_ERR_CUDA;
 
   FwdParams p;
   std::memset(&p, 0, sizeof(p));
   p.B = B;
-  p.H = H;
+  p.H = pl.packed_heads ? Hkv : H;
   p.Hkv = Hkv;
-  p.Nq = Nq;
+  p.Nq = rows_per_head;
   p.Nk = Nk;
   p.causal = causal != FA_CAUSAL_NONE ? 1 : 0;
-  p.causal_off = causal_off;
-  p.q_period = pack ? Nq / G : 0;
+  p.causal_off = causal_offset(causal, Nq, Nk);
+  p.q_period = pl.packed_heads ? Nq : 0;  // query position of packed row r: r % Nq
   p.scale_log2 = scale * 1.4426950408889634f;
-  p.num_splits = S;
-  p.kv_tiles_per_split = per_split;
-  p.num_q_blocks = qblocks;
-  p.num_units = BH * p.num_q_blocks * S;
+  p.num_splits = pl.num_splits;
+  p.kv_tiles_per_split = pl.key_tiles_per_split;
+  p.num_q_blocks = (rows_per_head + pl.query_block - 1) / pl.query_block;
+  p.num_units = pl.num_units;
   p.o = o;
   p.lse = lse;
   p.store32 = (reinterpret_cast<uintptr_t>(o) & 31) == 0 ? 1 : 0;
-  // Without the causal mask every unit has the same work, so the units can
-  // be listed window by window of heads without losing balance: a window is
-  // the fewest heads whose query blocks fill one round of CTAs, and the K, V
-  // of the heads in flight then stay in L2.  Only when the K and V of all
-  // heads exceed half the L2 (otherwise they stay there anyway).
-  {
-    const double kv_bytes = 4.0 * (double)B * Hkv * Nk * d;
-    if (causal == FA_CAUSAL_NONE && S == 1 && kv_bytes > s->l2_bytes / 2) {
-      const int grid = p.num_units < s->sm_count ? p.num_units : s->sm_count;
-      const int win = (grid + qblocks - 1) / qblocks;
-      p.head_window = win < BH ? win : 0;
-    }
-  }
+  p.head_window = pl.head_window;
   p.status = s->status;
   p.timeout_ns = g_timeout_ns.load();
-  p.dual = dual ? 1 : 0;
+  p.dual = pl.dual;
 
   void* ws = nullptr;
-  const size_t rows = (size_t)BH * Nq;
-  const int parts = dual ? 2 * S : S;  // partial results to merge
-  if (parts > 1) {
-    const size_t bytes = (size_t)parts * rows * ((size_t)d + 1) * sizeof(float);
-    if (ws_alloc(&ws, bytes, st) != cudaSuccess) {
+  if (pl.partials > 0) {
+    if (ws_alloc(&ws, pl.workspace_bytes, st) != cudaSuccess) {
       cudaGetLastError();
       return FA_ERR_NO_MEMORY;
     }
     p.o_part = static_cast<float*>(ws);
-    p.lse_part = p.o_part + (size_t)parts * rows * d;
+    p.lse_part = p.o_part + (size_t)pl.partials * BH * rows_per_head * d;
   }
-  const int grid = p.num_units < s->sm_count ? p.num_units : s->sm_count;
   cudaError_t ce = timed(FA_KERNEL_FWD, st, [&] {
-    return wide ? fa::launch_fwd256(tq, tk, tv, p, grid, st) : fa::launch_fwd(d, tq, tk, tv, p, grid, st);
+    return wide ? fa::launch_fwd256(tq, tk, tv, p, pl.grid, st) : fa::launch_fwd(d, tq, tk, tv, p, pl.grid, st);
   });
-  if (ce == cudaSuccess && parts > 1) {
+  if (ce == cudaSuccess && pl.partials > 0) {
     fa::CombineParams c;
-    c.rows = (int)rows;
-    c.num_splits = parts;
+    c.rows = BH * rows_per_head;
+    c.num_splits = pl.partials;
     c.o_part = p.o_part;
     c.lse_part = p.lse_part;
     c.o = o;
@@ -547,20 +626,29 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   return fa_fwd_gqa(q, k, v, o, lse, B, H, H, N, d, causal, scale, 0, stream);
 }
 
+int fa_bwd_plan(int B, int H, int Hkv, int Nq, int Nk, int d, int causal, int sm_count, fa_bwd_plan_t* plan) {
+  if (plan == nullptr || sm_count < 1) return FA_ERR_INVALID_ARG;
+  const int e = check_bwd_sizes(B, H, Hkv, Nq, Nk, d, causal);
+  if (e) return e;
+  plan_bwd(B, H, Hkv, Nq, Nk, d, causal, sm_count, plan);
+  return FA_OK;
+}
+
 int fa_bwd_general(const void* q, const void* k, const void* v, const void* o, const float* lse,
                    const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int Nq, int Nk, int d,
                    int causal, float scale, void* stream) {
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dout) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return FA_ERR_INVALID_ARG;
-  int e = validate(B, H, Nq, Nk, d, scale, true);
+  if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_INVALID_ARG;
+  int e = check_bwd_sizes(B, H, Hkv, Nq, Nk, d, causal);
   if (e) return e;
-  if (Hkv < 1 || H % Hkv != 0) return FA_ERR_INVALID_ARG;
-  if (causal < FA_CAUSAL_NONE || causal > FA_CAUSAL_BOTTOM_RIGHT) return FA_ERR_INVALID_ARG;
   DeviceState* s = nullptr;
   e = device_state(&s);
   if (e) return e;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  fa_bwd_plan_t pl;
+  plan_bwd(B, H, Hkv, Nq, Nk, d, causal, s->sm_count, &pl);
   const int BH = B * H;
   const size_t rows = (size_t)BH * Nq;
 
@@ -568,8 +656,8 @@ int fa_bwd_general(const void* q, const void* k, const void* v, const void* o, c
   // of the key/value kernel, the key steps of the dQ kernel), at d = 128
   // 64-row ones of Q and dO (each CTA's half of a query tile in the CTA-pair
   // dK/dV kernel).
-  const bool wide = d == 256;
-  const bool pair = d == 128;
+  const bool wide = pl.kv_passes == 2;
+  const bool pair = pl.kv_cta_pair != 0;
   CUtensorMap tq, tk, tv, tdo, tq64, tk64, tv64, tdo64;
   if (encode_bhnd(&tq, q, BH, Nq, d) || encode_bhnd(&tk, k, B * Hkv, Nk, d) ||
       encode_bhnd(&tv, v, B * Hkv, Nk, d) || encode_bhnd(&tdo, dout, BH, Nq, d))
@@ -596,27 +684,19 @@ int fa_bwd_general(const void* q, const void* k, const void* v, const void* o, c
   p.dv = dv;
   p.store32 = ((reinterpret_cast<uintptr_t>(dq) | reinterpret_cast<uintptr_t>(dk) |
                 reinterpret_cast<uintptr_t>(dv)) & 31u) == 0 ? 1 : 0;
-  p.num_q_tiles = (Nq + 127) / 128;
-  p.num_k_tiles = (Nk + 127) / 128;
-  // With the causal mask: key tiles past the last key the last query row
-  // sees, and query tiles whose rows all see no key (a negative offset),
-  // take no part; their gradient rows are zero.
-  p.kv_tiles_used = p.num_k_tiles;
-  p.q_tile_first = 0;
-  if (p.causal) {
-    const int last_key = Nq - 1 + p.causal_off;  // >= 0 for both alignments
-    p.kv_tiles_used = std::min(p.num_k_tiles, last_key / 128 + 1);
-    if (p.causal_off < 0) p.q_tile_first = (-p.causal_off) / 128;
-  }
-  p.num_units = BH * (p.num_q_tiles - p.q_tile_first);
-  p.num_units_kv = B * Hkv * p.kv_tiles_used;
+  p.num_q_tiles = pl.q_tiles;
+  p.num_k_tiles = pl.k_tiles;
+  p.kv_tiles_used = pl.kv_tiles_used;
+  p.q_tile_first = pl.q_tile_first;
+  p.num_units = pl.dq_units;
+  p.num_units_kv = B * Hkv * pl.kv_tiles_used;  // key tiles; the pair kernel takes two a unit
   p.group = H / Hkv;
   p.status = s->status;
   p.timeout_ns = g_timeout_ns.load();
 
   // Workspace: D [rows].
   void* ws = nullptr;
-  if (ws_alloc(&ws, rows * sizeof(float), st) != cudaSuccess) {
+  if (ws_alloc(&ws, pl.workspace_bytes, st) != cudaSuccess) {
     cudaGetLastError();
     return FA_ERR_NO_MEMORY;
   }
@@ -636,7 +716,7 @@ int fa_bwd_general(const void* q, const void* k, const void* v, const void* o, c
     const size_t r1 = std::min((size_t)Nq, (size_t)p.q_tile_first * 128);
     ce = cudaMemset2DAsync(dq, (size_t)Nq * row_bytes, 0, r1 * row_bytes, (size_t)BH, st);
   }
-  const int grid_q = p.num_units < s->sm_count ? p.num_units : s->sm_count;
+  const int grid_q = pl.dq_grid;
   const int grid_kv = p.num_units_kv < s->sm_count ? p.num_units_kv : s->sm_count;
   if (ce == cudaSuccess)
     ce = timed(FA_KERNEL_BWD_PRE, st, [&] { return fa::launch_bwd_preprocess(d, o, dout, dvec, (int)rows, st); });
@@ -650,7 +730,7 @@ int fa_bwd_general(const void* q, const void* k, const void* v, const void* o, c
       ce = timed(FA_KERNEL_BWD_DQ, st, [&] { return fa::launch_bwd_dq(d, tq, tk, tv, tdo, p, grid_q, st); });
   } else {
     // Head dim 256: dV pass, dK pass, then dQ.
-    for (int pass = 0; pass < 2 && ce == cudaSuccess; ++pass)
+    for (int pass = 0; pass < pl.kv_passes && ce == cudaSuccess; ++pass)
       ce = timed(FA_KERNEL_BWD, st,
                  [&] { return fa::launch_bwd256_kv(pass == 1, tq64, tk, tv, tdo64, p, grid_kv, st); });
     if (ce == cudaSuccess)

@@ -51,7 +51,7 @@
 extern "C" {
 #endif
 
-#define FA_ABI_VERSION 4
+#define FA_ABI_VERSION 5
 
 typedef enum {
   FA_OK = 0,
@@ -185,6 +185,69 @@ int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const
 int fa_bwd_general(const void* q, const void* k, const void* v, const void* o, const float* lse,
                    const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int Nq, int Nk, int d,
                    int causal, float scale, void* stream);
+
+/*
+ * Launch plans: how fa_fwd_general and fa_bwd_general carry out a call of
+ * the given sizes, worked out on the host alone.  No device is touched, so a
+ * caller can learn the workspace a call takes, and a test can check the
+ * decisions, without a GPU.  The two calls follow exactly this plan, with
+ * sm_count and l2_bytes those of the current device.
+ *   sizes    : as fa_fwd_general / fa_bwd_general (num_splits for the forward)
+ *   sm_count : the device's SM count (>= 1);  l2_bytes : its L2 size in bytes
+ *   plan     : out, written on FA_OK only
+ * Returns FA_OK; the status the call would return for these sizes (its
+ * pointer checks aside); or FA_ERR_INVALID_ARG for a null plan or
+ * sm_count < 1.
+ */
+typedef struct {
+  int packed_heads;         /* 1: the H/Hkv query heads of a key/value head
+                               share query tiles (H/Hkv > 1 and Nq < 128)  */
+  int unit_heads;           /* (batch, head) pairs listed: B*H, or B*Hkv when packed */
+  int unit_rows;            /* query rows of each: Nq, or (H/Hkv)*Nq when packed */
+  int query_block;          /* query rows per unit: 256 (two 128-row tiles); 128 at d = 256 */
+  int key_tile;             /* keys per step: 128; 64 at d = 256 */
+  int key_tiles;            /* ceil(Nk / key_tile) */
+  int num_splits;           /* key splits S >= 1, none of them empty */
+  int key_tiles_per_split;  /* ceil(key_tiles / S) */
+  int dual;                 /* 1: both query tiles of a unit hold its rows, one
+                               taking the even, the other the odd key tiles of
+                               its split (decoding; automatic splits only) */
+  int partials;             /* fp32 partial results (O and L) merged by the
+                               combine kernel: S, or 2 S when dual; 0 = none */
+  int num_units;            /* unit_heads * ceil(unit_rows / query_block) * S */
+  int grid;                 /* CTAs of the forward kernel: min(num_units, sm_count) */
+  int head_window;          /* 0, or the heads per window when units are listed
+                               window by window so that the K, V in flight
+                               stay in L2 (no causal mask, S = 1, and the K, V
+                               of all heads above half of l2_bytes) */
+  int launches;             /* library kernels launched: 1, or 2 with the merge */
+  uint64_t workspace_bytes; /* workspace taken: partials * B*H*Nq * (d + 1) * 4 */
+} fa_fwd_plan_t;
+
+int fa_fwd_plan(int B, int H, int Hkv, int Nq, int Nk, int d, int causal, int num_splits, int sm_count,
+                uint64_t l2_bytes, fa_fwd_plan_t* plan);
+
+typedef struct {
+  int q_tiles;                /* ceil(Nq / 128) */
+  int k_tiles;                /* ceil(Nk / 128) */
+  int q_tile_first;           /* first query tile with a row that sees a key
+                                 (> 0 only bottom-right with Nq > Nk) */
+  int kv_tiles_used;          /* key tiles that some query row sees */
+  int dq_units;               /* units of the dQ kernel: B*H*(q_tiles - q_tile_first) */
+  int dq_grid;                /* its CTAs: min(dq_units, sm_count) */
+  int kv_units;               /* units of the dK/dV kernel: B*Hkv*kv_tiles_used,
+                                 at d = 128 B*Hkv*ceil(kv_tiles_used / 2) CTA pairs */
+  int kv_cta_pair;            /* 1 at d = 128: the dK/dV kernel runs on CTA pairs */
+  int kv_passes;              /* dK/dV launches: 2 at d = 256 (dV, then dK), else 1 */
+  int launches;               /* library kernels launched: D preprocess, kv_passes, dQ */
+  uint64_t zeroed_dq_bytes;   /* dQ bytes of the query tiles before q_tile_first,
+                                 zeroed with cudaMemset2DAsync */
+  uint64_t zeroed_dkdv_bytes; /* dK plus dV bytes of the key rows past
+                                 kv_tiles_used * 128, zeroed likewise */
+  uint64_t workspace_bytes;   /* workspace taken (D): B*H*Nq*4 */
+} fa_bwd_plan_t;
+
+int fa_bwd_plan(int B, int H, int Hkv, int Nq, int Nk, int d, int causal, int sm_count, fa_bwd_plan_t* plan);
 
 /*
  * Backward pass that allocates no device memory.  The paper has no

@@ -37,7 +37,7 @@ def test_no_driver_dependency():
 
 
 def test_version_and_strerror(lib):
-    assert fa.fa_abi_version() == 4
+    assert fa.fa_abi_version() == 5
     for code in range(6):
         assert fa.fa_strerror(code).startswith("FA_")
     assert "unknown" in fa.fa_strerror(99)

@@ -125,6 +125,33 @@ def test_decoding_runs_dual_tiles(fa, d):
     check_lse(lse, L, f"decode d={d}")
 
 
+@pytest.mark.parametrize("shape", [(1, 2, 2, 300, 4000, 96, "top_left"), (8, 32, 8, 1, 8192, 128, "bottom_right"),
+                                   (2, 4, 4, 1000, 1000, 256, "none"), (1, 4, 2, 300, 100, 128, "bottom_right"),
+                                   (1, 1, 1, 65536, 65536, 128, "top_left")],
+                         ids=lambda s: "B{}H{}Hkv{}Nq{}Nk{}d{}-{}".format(*s))
+def test_calls_follow_their_plans(fa, shape):
+    """fa_fwd_general and fa_bwd_general launch what fa_fwd_plan and
+    fa_bwd_plan report for this device: the merge exactly when partial
+    results are planned, two key/value passes at head dim 256."""
+    torch = torch_cuda()
+    B, H, Hkv, Nq, Nk, d, mode = shape
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    sm, l2 = props.multi_processor_count, getattr(props, "L2_cache_size", 126 << 20)
+    fplan = fa.fa_fwd_plan(B, H, Hkv, Nq, Nk, d, mode, 0, sm, l2)
+    bplan = fa.fa_bwd_plan(B, H, Hkv, Nq, Nk, d, mode, sm)
+    q, k, v, do = make(B, H, Hkv, Nq, Nk, d, seed=7400 + Nq + d, with_do=True)
+    kernels = (fa.FA_KERNEL_FWD, fa.FA_KERNEL_COMBINE, fa.FA_KERNEL_BWD_PRE, fa.FA_KERNEL_BWD, fa.FA_KERNEL_BWD_DQ)
+    before = [fa.fa_launch_count(kid) for kid in kernels]
+    _, _, (tq, tk, tv, o, lse) = run_fwd(fa, q, k, v, mode)
+    tdo = dev(do)
+    dq, dk, dv = torch.empty_like(tq), torch.empty_like(tk), torch.empty_like(tv)
+    fa.fa_bwd_general(tq, tk, tv, o, lse, tdo, dq, dk, dv, mode)
+    assert fa.fa_poll_status() == fa.FA_OK
+    got = [fa.fa_launch_count(kid) - b for kid, b in zip(kernels, before)]
+    assert got == [1, 1 if fplan["partials"] else 0, 1, bplan["kv_passes"], 1], (got, fplan, bplan)
+    assert fplan["launches"] == got[0] + got[1] and bplan["launches"] == sum(got[2:])
+
+
 @pytest.mark.parametrize("d", [96, 256])
 @pytest.mark.parametrize("splits", [1, 3, 16])
 @pytest.mark.parametrize("mode", ["top_left", "bottom_right"])
