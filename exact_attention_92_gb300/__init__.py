@@ -40,6 +40,7 @@ from ._binding import (  # noqa: F401
     fa_launch_count,
     fa_timing_enable,
     fa_timing_read,
+    fa_trim_workspace,
     forward,
     load,
 )

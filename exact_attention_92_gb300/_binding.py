@@ -62,6 +62,7 @@ _SIGNATURES = {
     "fa_selftest_wait_timeout": ([_u64, _vp], _i),
     "fa_strerror": ([_i], ctypes.c_char_p),
     "fa_abi_version": ([], _i),
+    "fa_trim_workspace": ([], _i),
     "fa_timing_enable": ([_i], _i),
     "fa_timing_read": ([_i, ctypes.POINTER(_i), ctypes.POINTER(ctypes.c_double)], _i),
     "fa_launch_count": ([_i, ctypes.POINTER(ctypes.c_uint64)], _i),
@@ -320,6 +321,12 @@ def fa_strerror(status: int) -> str:
 
 def fa_abi_version() -> int:
     return int(load().fa_abi_version())
+
+
+def fa_trim_workspace() -> None:
+    """C fa_trim_workspace: give back the workspace memory the library's pool
+    keeps reserved on the current device."""
+    _check(load().fa_trim_workspace(), "fa_trim_workspace")
 
 
 def fa_timing_enable(on: bool) -> None:

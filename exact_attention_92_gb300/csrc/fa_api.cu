@@ -54,6 +54,7 @@ struct DeviceState {
   int sm_count = 0;
   double l2_bytes = 0.0;
   unsigned int* status = nullptr;  // device address of g_fa_status_word
+  cudaMemPool_t pool = nullptr;    // the library's workspace pool on this device
 };
 
 DeviceState g_dev[kMaxDevices];
@@ -71,8 +72,8 @@ void load_encode() {
     g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
 }
 
-// Set-up of the current device: compute capability check, SM count and the
-// address of the status word (cleared).  It is kept once it has succeeded; a
+// Set-up of the current device: compute capability check, SM count, the
+// workspace pool and the address of the status word (cleared).  It is kept once it has succeeded; a
 // set-up that failed (for instance inside a stream capture, where the
 // clearing memset is not allowed) is tried again by the next call.  A device
 // that is not an sm_103 part is refused every time.
@@ -95,6 +96,32 @@ int device_state(DeviceState** out) {
       if (cudaMemset(addr, 0, sizeof(unsigned int)) != cudaSuccess) {
         cudaGetLastError();
         return FA_ERR_CUDA;
+      }
+      // Workspace pool: stream-ordered like the device's default pool, but
+      // it keeps freed memory reserved for later calls (no release
+      // threshold).  The default pool returns its memory at every
+      // synchronisation, so each call after one would map its workspace
+      // afresh: 170-200 us for the 67-134 MB of split partials of one
+      // 65536-token head.  fa_trim_workspace gives the memory back.
+      if (s.pool == nullptr) {
+        cudaMemPoolProps props;
+        std::memset(&props, 0, sizeof(props));
+        props.allocType = cudaMemAllocationTypePinned;
+        props.handleTypes = cudaMemHandleTypeNone;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t pool = nullptr;
+        if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) {
+          cudaGetLastError();
+          return FA_ERR_CUDA;
+        }
+        cuuint64_t keep = ~(cuuint64_t)0;
+        if (cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess) {
+          cudaGetLastError();
+          cudaMemPoolDestroy(pool);
+          return FA_ERR_CUDA;
+        }
+        s.pool = pool;
       }
       s.sm_count = prop.multiProcessorCount;
       s.l2_bytes = (double)prop.l2CacheSize;
@@ -179,13 +206,14 @@ int choose_splits_single_tile(long long units, int nkv, int min_tiles, int sm_co
   return best;
 }
 
-// Stream-ordered workspace.  For failure-path tests, the environment variable
-// FA_TEST_FAIL_ALLOC (any value but "0") makes every workspace allocation
-// report failure without allocating.
-cudaError_t ws_alloc(void** ptr, size_t bytes, cudaStream_t st) {
+// Stream-ordered workspace from the device's library pool (returned with
+// cudaFreeAsync on the same stream).  For failure-path tests, the
+// environment variable FA_TEST_FAIL_ALLOC (any value but "0") makes every
+// workspace allocation report failure without allocating.
+cudaError_t ws_alloc(cudaMemPool_t pool, void** ptr, size_t bytes, cudaStream_t st) {
   const char* f = std::getenv("FA_TEST_FAIL_ALLOC");
   if (f != nullptr && std::strcmp(f, "0") != 0) return cudaErrorMemoryAllocation;
-  return cudaMallocAsync(ptr, bytes, st);
+  return cudaMallocFromPoolAsync(ptr, bytes, pool, st);
 }
 
 // Head dims of the library: 64, 96, 128 and 256 (forward and backward).
@@ -492,6 +520,13 @@ int fa_timing_read(int kernel, int* launches, double* total_ms) {
 
 int fa_abi_version(void) { return FA_ABI_VERSION; }
 
+int fa_trim_workspace(void) {
+  DeviceState* s = nullptr;
+  const int e = device_state(&s);
+  if (e) return e;
+  return cudaMemPoolTrimTo(s->pool, 0) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 const char* fa_strerror(int status) {
   switch (status) {
     case FA_OK: return "FA_OK";
@@ -586,7 +621,7 @@ int fa_fwd_general(const void* q, const void* k, const void* v, void* o, float* 
 
   void* ws = nullptr;
   if (pl.partials > 0) {
-    if (ws_alloc(&ws, pl.workspace_bytes, st) != cudaSuccess) {
+    if (ws_alloc(s->pool, &ws, pl.workspace_bytes, st) != cudaSuccess) {
       cudaGetLastError();
       return FA_ERR_NO_MEMORY;
     }
@@ -696,7 +731,7 @@ int fa_bwd_general(const void* q, const void* k, const void* v, const void* o, c
 
   // Workspace: D [rows].
   void* ws = nullptr;
-  if (ws_alloc(&ws, pl.workspace_bytes, st) != cudaSuccess) {
+  if (ws_alloc(s->pool, &ws, pl.workspace_bytes, st) != cudaSuccess) {
     cudaGetLastError();
     return FA_ERR_NO_MEMORY;
   }

@@ -1,5 +1,5 @@
 // fa_bwd_noalloc: the backward pass with its workspace in a static device
-// array instead of cudaMallocAsync (see include/fa.h for who needs this).
+// array instead of the workspace pool (see include/fa.h for who needs this).
 //
 // The array below is the only scratch this entry point uses.  Host code may
 // not use its name as an address (that is a host-side stand-in): set-up, once

@@ -32,9 +32,14 @@
  *    still starts only once all of the call's kernels are done.
  *  - The caller owns every buffer it passes; the library never frees or keeps
  *    them.  Temporary device workspace (the fp32 split-KV partials of the
- *    forward pass, the fp32 D vector of the backward pass) is taken with
- *    cudaMallocAsync on `stream` and returned with cudaFreeAsync on the same
- *    stream, so it is stream-ordered.
+ *    forward pass, the fp32 D vector of the backward pass) is taken from
+ *    the library's own memory pool on the current device with
+ *    cudaMallocFromPoolAsync on `stream` and returned with cudaFreeAsync on
+ *    the same stream, so it is stream-ordered.  Unlike the device's default
+ *    pool, which gives its memory back at every synchronisation, this pool
+ *    keeps freed memory reserved for later calls (up to the most workspace
+ *    in use at once), so a call made after a synchronisation does not map
+ *    its workspace afresh; fa_trim_workspace gives the reserved memory back.
  *  - Return value: FA_OK, or an fa_status code.  Argument errors are detected
  *    on the host before anything is launched.  A workspace allocation that
  *    fails returns FA_ERR_NO_MEMORY before any launch (for tests of that
@@ -150,7 +155,7 @@ int fa_fwd_general(const void* q, const void* k, const void* v, void* o, float* 
  *   lse     : in,  fp32 [B,H,N]   (the forward logsumexp)
  *   dout    : in,  bf16 [B,H,N,d] (gradient of the loss w.r.t. O)
  *   dq,dk,dv: out, bf16 [B,H,N,d]
- * Workspace: D, B*H*N*4 bytes from cudaMallocAsync on `stream`.  The results
+ * Workspace: D, B*H*N*4 bytes from the library's pool on `stream`.  The results
  * are bitwise reproducible from run to run.  At d = 256 the dK and dV
  * accumulators of a key tile do not fit in tensor memory together, so the
  * key/value kernel runs twice (a dV pass and a dK pass, recomputing S^T).
@@ -253,7 +258,7 @@ int fa_bwd_plan(int B, int H, int Hkv, int Nq, int Nk, int d, int causal, int sm
  * Backward pass that allocates no device memory.  The paper has no
  * counterpart: this is a library convenience.
  *
- * fa_bwd takes its fp32 workspace (D, B*H*N*4 bytes) from cudaMallocAsync
+ * fa_bwd takes its fp32 workspace (D, B*H*N*4 bytes) from a memory pool
  * on every call.  Some callers cannot allow that: a caller that has handed
  * nearly all device memory to its own pool up front (weights, KV caches,
  * activations) and cannot have a library take memory in the middle of a
@@ -272,10 +277,11 @@ int fa_bwd_plan(int B, int H, int Hkv, int Nq, int Nk, int d, int causal, int sm
  *    for d = 256 (it runs the kernels of head dims 64, 96 and 128).
  *  - The first call on a device sets up that device (with it current): it
  *    looks up the array's device address, and the library's status word,
- *    and keeps them.  Make that first call before any stream capture; a
+ *    and keeps them (it also creates the library's workspace pool, which
+ *    stays empty unless other entry points use it).  Make that first call before any stream capture; a
  *    set-up that fails is not kept, and the next call tries again.
- *  - It calls no cudaMalloc/cudaMallocAsync/cudaFree and no allocating
- *    routine of any other library.
+ *  - It calls no cudaMalloc/cudaMallocAsync/cudaMallocFromPoolAsync/cudaFree
+ *    and no allocating routine of any other library.
  *  - All calls on a device share the one array, and it keeps the last
  *    call's contents; each call writes all of the part it reads (D) before
  *    reading it.  Two calls whose kernels overlap on the GPU
@@ -341,6 +347,15 @@ int fa_timing_read(int kernel, int* launches, double* total_ms);
  * or null `count`).
  */
 int fa_launch_count(int kernel, uint64_t* count);
+
+/*
+ * Give back to the device the memory that the library's workspace pool on
+ * the current device keeps reserved and no call is using (cudaMemPoolTrimTo
+ * to zero).  Workspace of calls still in flight is not touched; later calls
+ * take memory from the device again.  Returns FA_OK, FA_ERR_UNSUPPORTED (not
+ * an sm_103 device) or FA_ERR_CUDA.
+ */
+int fa_trim_workspace(void);
 
 /* Human-readable name of an fa_status code (static storage). */
 const char* fa_strerror(int status);

@@ -105,3 +105,33 @@ def test_workspace_allocation_failure_is_reported(fa, monkeypatch):
     rq, rk, rv = att.backward(case.f64("q"), case.f64("k"), case.f64("v"), case.f64("do"), case.scale, True)
     for name, g, r in (("dQ", dq, rq), ("dK", dk, rk), ("dV", dv, rv)):
         check_grad(host(g), r, name, "after an allocation failure")
+
+
+def test_workspace_pool_keeps_memory_until_trimmed(fa):
+    """The split partials of one 65536-token causal head come from the
+    library's pool, which keeps them reserved across synchronisations (a
+    second call maps nothing new) until fa_trim_workspace gives them back;
+    a call after the trim takes memory again and gives the same bits."""
+    torch = torch_cuda()
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    plan = fa.fa_fwd_plan(1, 1, 1, 65536, 65536, 128, fa.FA_CAUSAL_TOP_LEFT, 0, props.multi_processor_count,
+                          getattr(props, "L2_cache_size", 126 << 20))
+    assert plan["workspace_bytes"] > 0
+    g = torch.Generator(device="cuda").manual_seed(77)
+    q, k, v = (torch.randn((1, 1, 65536, 128), generator=g, device="cuda").to(torch.bfloat16) for _ in range(3))
+    o1, lse1 = fa.forward(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    free1 = torch.cuda.mem_get_info()[0]
+    o2, lse2 = fa.forward(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    free2 = torch.cuda.mem_get_info()[0]
+    fa.fa_trim_workspace()
+    free3 = torch.cuda.mem_get_info()[0]
+    o3, lse3 = fa.forward(q, k, v, causal=True)
+    assert fa.fa_poll_status() == fa.FA_OK
+    # The second call's outputs are new tensors from torch's cache (not the
+    # device); the workspace came back from the library's pool.
+    assert free1 - free2 <= o2.numel() * 2 + lse2.numel() * 4 + (8 << 20), (free1, free2)
+    assert free3 - free2 >= plan["workspace_bytes"], (free2, free3, plan["workspace_bytes"])
+    for a, b in ((o1, o2), (o1, o3), (lse1, lse2), (lse1, lse3)):
+        assert torch.equal(a, b)
