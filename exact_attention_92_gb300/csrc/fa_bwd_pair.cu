@@ -42,6 +42,8 @@
 // Each CTA's own L and D values for a step sit in a small local ring.
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "bwd_elementwise.cuh"
 #include "sm103_pair.cuh"
 #include "sm103_primitives.cuh"
@@ -599,9 +601,15 @@ static cudaError_t launch_pair_t(const CUtensorMap& tq64, const CUtensorMap& tq,
   auto* kern = fa_bwd_dkdv_pair_kernel<GQA>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pr::kSmemBytes);
   if (e != cudaSuccess) return e;
-  // Pairs resident at once (a pair needs two SMs of one cluster group).
-  static int max_pairs[2] = {0, 0};
-  int& mp = max_pairs[GQA ? 1 : 0];
+  // Pairs resident at once (a pair needs two SMs of one cluster group),
+  // asked once per device.
+  constexpr int kMaxDevices = 64;
+  static std::atomic<int> max_pairs[kMaxDevices];
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  int mp = max_pairs[dev].load(std::memory_order_relaxed);
   if (mp == 0) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (unsigned)(sm_count / 2), 1, 1);
@@ -613,6 +621,7 @@ static cudaError_t launch_pair_t(const CUtensorMap& tq64, const CUtensorMap& tq,
     if (e != cudaSuccess) return e;
     if (n <= 0) return cudaErrorInvalidConfiguration;
     mp = n;
+    max_pairs[dev].store(n, std::memory_order_relaxed);
   }
   const long long units = (long long)p.B * p.Hkv * ((p.kv_tiles_used + 1) / 2);
   const int pairs = (int)(units < mp ? units : mp);
