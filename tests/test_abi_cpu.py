@@ -165,3 +165,39 @@ def test_build_refuses_spills_in_tmem_kernels():
           "ptxas info    : Compiling entry function '_ZN2fa17fa_bwd_preprocessILi64EEEv' for 'sm_103a'\n"
           "    8 bytes stack frame, 8 bytes spill stores, 8 bytes spill loads\n")
     build.check_spills(ok)
+
+
+def _prototypes():
+    """(name, return type, parameter list) of every function include/fa.h declares."""
+    import re
+
+    text = open(_binding.HEADER).read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    protos = {}
+    for m in re.finditer(r"(int|uint64_t|const char\s*\*)\s+(fa_\w+)\s*\(([^)]*)\)\s*;", text):
+        params = [p.strip() for p in m.group(3).split(",") if p.strip() and p.strip() != "void"]
+        protos[m.group(2)] = (m.group(1).replace(" ", ""), params)
+    return protos
+
+
+def test_binding_signatures_match_the_header():
+    """Every ctypes signature of the binding has the header's parameter count
+    and types (pointers as pointers, 64-bit integers as 64-bit), so a drift
+    between fa.h and _binding.py cannot pass arguments in the wrong slots."""
+    protos = _prototypes()
+    assert set(protos) == set(fa.declared_symbols())
+    assert set(protos) == set(_binding._SIGNATURES), set(protos) ^ set(_binding._SIGNATURES)
+    ret = {"int": ctypes.c_int, "uint64_t": ctypes.c_uint64, "constchar*": ctypes.c_char_p}
+    for name, (rtype, params) in protos.items():
+        args, res = _binding._SIGNATURES[name]
+        assert res is ret[rtype], name
+        assert len(args) == len(params), (name, len(args), params)
+        for a, p in zip(args, params):
+            if "*" in p:
+                assert a is ctypes.c_void_p or issubclass(a, ctypes._Pointer), (name, p, a)
+            elif p.startswith("uint64_t"):
+                assert a is ctypes.c_uint64, (name, p, a)
+            elif p.startswith("float"):
+                assert a is ctypes.c_float, (name, p, a)
+            else:
+                assert p.startswith("int") and a is ctypes.c_int, (name, p, a)
