@@ -281,9 +281,10 @@ int check_fwd_sizes(int B, int H, int Hkv, int Nq, int Nk, int d, int causal, in
 }
 
 // The host-side decisions of a forward call (fa_fwd_plan_t), for sizes that
-// passed check_fwd_sizes.
-void plan_fwd(int B, int H, int Hkv, int Nq, int Nk, int d, int causal, int num_splits, int sm_count,
-              double l2_bytes, fa_fwd_plan_t* pl) {
+// passed check_fwd_sizes.  FA_ERR_INVALID_ARG when a forced split count
+// would make more units than a 32-bit unit index holds.
+int plan_fwd(int B, int H, int Hkv, int Nq, int Nk, int d, int causal, int num_splits, int sm_count,
+             double l2_bytes, fa_fwd_plan_t* pl) {
   std::memset(pl, 0, sizeof(*pl));
   const int causal_off = causal_offset(causal, Nq, Nk);
   // Grouped query heads with fewer than 128 query rows (decoding, short
@@ -334,6 +335,7 @@ void plan_fwd(int B, int H, int Hkv, int Nq, int Nk, int d, int causal, int num_
   if (S < 1) S = 1;
   const int per_split = (nkv + S - 1) / S;
   S = (nkv + per_split - 1) / per_split;  // no empty split
+  if ((long long)BH * qblocks * S > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
 
   pl->packed_heads = pack ? 1 : 0;
   pl->unit_heads = BH;
@@ -360,6 +362,7 @@ void plan_fwd(int B, int H, int Hkv, int Nq, int Nk, int d, int causal, int num_
   }
   pl->launches = pl->partials > 0 ? 2 : 1;
   pl->workspace_bytes = pl->partials > 0 ? (uint64_t)parts * BH * Nq * ((uint64_t)d + 1) * sizeof(float) : 0;
+  return FA_OK;
 }
 
 // Size checks shared by the backward call and its plan.
@@ -570,8 +573,10 @@ int fa_fwd_plan(int B, int H, int Hkv, int Nq, int Nk, int d, int causal, int nu
   if (plan == nullptr || sm_count < 1) return FA_ERR_INVALID_ARG;
   const int e = check_fwd_sizes(B, H, Hkv, Nq, Nk, d, causal, num_splits);
   if (e) return e;
-  plan_fwd(B, H, Hkv, Nq, Nk, d, causal, num_splits, sm_count, (double)l2_bytes, plan);
-  return FA_OK;
+  fa_fwd_plan_t pl;
+  const int e2 = plan_fwd(B, H, Hkv, Nq, Nk, d, causal, num_splits, sm_count, (double)l2_bytes, &pl);
+  if (e2 == FA_OK) *plan = pl;
+  return e2;
 }
 
 int fa_fwd_general(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv,
@@ -586,7 +591,8 @@ int fa_fwd_general(const void* q, const void* k, const void* v, void* o, float* 
   if (e) return e;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   fa_fwd_plan_t pl;
-  plan_fwd(B, H, Hkv, Nq, Nk, d, causal, num_splits, s->sm_count, s->l2_bytes, &pl);
+  e = plan_fwd(B, H, Hkv, Nq, Nk, d, causal, num_splits, s->sm_count, s->l2_bytes, &pl);
+  if (e) return e;
   const bool wide = d == 256;
   const int BH = pl.unit_heads;
   const int rows_per_head = pl.unit_rows;

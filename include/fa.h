@@ -202,7 +202,9 @@ int fa_bwd_general(const void* q, const void* k, const void* v, const void* o, c
  *   plan     : out, written on FA_OK only
  * Returns FA_OK; the status the call would return for these sizes (its
  * pointer checks aside); or FA_ERR_INVALID_ARG for a null plan or
- * sm_count < 1.
+ * sm_count < 1.  Both the forward call and its plan refuse, with
+ * FA_ERR_INVALID_ARG, a forced split count that would make more than
+ * 2^31 - 1 work units (query blocks times splits over all heads).
  */
 typedef struct {
   int packed_heads;         /* 1: the H/Hkv query heads of a key/value head

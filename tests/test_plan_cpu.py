@@ -78,6 +78,11 @@ def test_plan_argument_errors():
     assert fwd_status(1, 4, 2, 100, 300, 64, 3) == fa.FA_ERR_INVALID_ARG
     assert fwd_status(1, 4, 2, 100, 300, 64, 0, -1) == fa.FA_ERR_INVALID_ARG
     assert fwd_status(1, 4, 2, 100, 300, 64, 0, 0, 0) == fa.FA_ERR_INVALID_ARG
+    # A forced split count whose units (65536 query blocks x 131072 splits of
+    # one 2^24-token head) overflow a 32-bit unit index; the same head with
+    # the automatic count is fine.
+    assert fwd_status(1, 1, 1, 1 << 24, 1 << 24, 64, 0, 1 << 20) == fa.FA_ERR_INVALID_ARG
+    assert fwd_status(1, 1, 1, 1 << 24, 1 << 24, 64, 0, 0) == fa.FA_OK
     lib = fa.load()
     assert lib.fa_fwd_plan(1, 1, 1, 128, 128, 64, 0, 0, SM, L2, None) == fa.FA_ERR_INVALID_ARG
     assert lib.fa_bwd_plan(1, 1, 1, 128, 128, 64, 0, SM, None) == fa.FA_ERR_INVALID_ARG
