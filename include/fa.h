@@ -87,7 +87,8 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
  *                every query tile into S parts whose partial results (fp32 O
  *                and LSE per part, in workspace) are merged by a second
  *                kernel: L = log sum_s exp(L_s), O = sum_s exp(L_s - L) O_s.
- *                S is clamped to the number of 128-key tiles.
+ *                S is clamped to the number of key tiles (128 keys; 64
+ *                at d = 256), and lowered so that no split is empty.
  * Other arguments as fa_fwd.
  */
 int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
