@@ -147,10 +147,11 @@ int fa_fwd_general(const void* q, const void* k, const void* v, void* o, float* 
  * Backward pass.  "FlashAttention V2 in depth", section 7: P recomputed from
  * the saved logsumexp (section 7.1), D_i = rowsum(dO_i * O_i) from a separate
  * preprocess kernel (section 7.3), dK and dV with key/value tiles in the
- * outer loop (section 7.2, one CTA per key tile, no atomics), and dQ from a
- * second kernel with query tiles in the outer loop (one CTA per query tile,
- * no atomics) instead of the page's fp32 atomic accumulation across key
- * tiles.
+ * outer loop (section 7.2; a work unit per key tile, at d = 128 a CTA pair
+ * per two key tiles; no atomics), and dQ from a second kernel with query
+ * tiles in the outer loop (a work unit per query tile, no atomics) instead
+ * of the page's fp32 atomic accumulation across key tiles.  Units are dealt
+ * to persistent CTAs, at most one per SM.
  *   q, k, v : in,  bf16 [B,H,N,d] (the forward inputs)
  *   o       : in,  bf16 [B,H,N,d] (the forward output)
  *   lse     : in,  fp32 [B,H,N]   (the forward logsumexp)
