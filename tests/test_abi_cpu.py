@@ -201,3 +201,51 @@ def test_binding_signatures_match_the_header():
                 assert a is ctypes.c_float, (name, p, a)
             else:
                 assert p.startswith("int") and a is ctypes.c_int, (name, p, a)
+
+
+C_CLIENT = r"""
+#include <stdio.h>
+#include "fa.h"
+
+int main(void) {
+  fa_fwd_plan_t f;
+  fa_bwd_plan_t b;
+  if (fa_abi_version() != FA_ABI_VERSION) return 10;
+  /* GQA decoding, 8 x 32 query heads over 8 key/value heads, 8192 keys. */
+  if (fa_fwd_plan(8, 32, 8, 1, 8192, 128, FA_CAUSAL_BOTTOM_RIGHT, 0, 152, 132120576ull, &f) != FA_OK) return 11;
+  if (fa_bwd_plan(1, 4, 2, 300, 100, 128, FA_CAUSAL_BOTTOM_RIGHT, 152, &b) != FA_OK) return 12;
+  if (fa_fwd_plan(1, 1, 1, 128, 128, 48, 0, 0, 152, 0, &f) != FA_ERR_UNSUPPORTED) return 13;
+  if (fa_fwd(0, 0, 0, 0, 0, 1, 1, 128, 64, 0, 0.125f, 0) != FA_ERR_INVALID_ARG) return 14;
+  printf("%d %d %d %llu %d %d\n", f.packed_heads, f.dual, f.partials, (unsigned long long)f.workspace_bytes,
+         b.q_tile_first, b.launches);
+  printf("%s\n", fa_strerror(FA_ERR_NO_MEMORY));
+  return 0;
+}
+"""
+
+
+def test_header_is_plain_c(tmp_path, lib):
+    """include/fa.h is a C header: a C99 program that includes it compiles
+    with warnings as errors, links against libfa.so and calls the host-only
+    entry points (plans, version, strerror, an argument check)."""
+    import shutil
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "client.c"
+    src.write_text(C_CLIENT)
+    exe = tmp_path / "client"
+    libdir = os.path.dirname(_binding.LIB_PATH)
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        str(src), "-o", str(exe), "-L", libdir, "-lfa", f"-Wl,-rpath,{libdir}"],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert out.returncode == 0, (out.returncode, out.stderr)
+    first, second = out.stdout.splitlines()
+    plan = fa.fa_fwd_plan(8, 32, 8, 1, 8192, 128, fa.FA_CAUSAL_BOTTOM_RIGHT, 0, 152, 132120576)
+    bplan = fa.fa_bwd_plan(1, 4, 2, 300, 100, 128, fa.FA_CAUSAL_BOTTOM_RIGHT, 152)
+    assert first.split() == [str(plan["packed_heads"]), str(plan["dual"]), str(plan["partials"]),
+                             str(plan["workspace_bytes"]), str(bplan["q_tile_first"]), str(bplan["launches"])]
+    assert second.startswith("FA_ERR_NO_MEMORY")
