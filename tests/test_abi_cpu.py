@@ -249,3 +249,19 @@ def test_header_is_plain_c(tmp_path, lib):
     assert first.split() == [str(plan["packed_heads"]), str(plan["dual"]), str(plan["partials"]),
                              str(plan["workspace_bytes"]), str(bplan["q_tile_first"]), str(bplan["launches"])]
     assert second.startswith("FA_ERR_NO_MEMORY")
+
+
+def test_build_checks_the_register_split_budget():
+    """Kernels that move registers between warpgroups with setmaxnreg are
+    launched with the per-thread count their split is sized for; an entry
+    that ptxas gave any other count is refused (a warpgroup asking for more
+    than the launch holds would wait forever)."""
+    log = ("ptxas info    : Compiling entry function '_ZN2fa13fa_fwd_kernelILi128ELb0EEEv' for 'sm_103a'\n"
+           "ptxas info    : Used {} registers, used 1 barriers, 0 bytes cmem[0]\n"
+           "    0 bytes stack frame, 0 bytes spill stores, 0 bytes spill loads\n")
+    build.check_spills(log.format(build.REG_SPLIT_KERNELS["fa_fwd_kernel"]))
+    for regs in (160, 176):
+        with pytest.raises(RuntimeError):
+            build.check_spills(log.format(regs))
+    # A kernel without a register split may use any count.
+    build.check_spills(log.replace("fa_fwd_kernel", "fa_combine_kernel").format(40))
